@@ -1,0 +1,10 @@
+"""CPU oracle for the int4-weight quantized linear layer.
+
+TEST INFRASTRUCTURE ONLY. Nothing in the product package imports, calls or
+links anything here; only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may use it. It
+shares no code with the CUDA path.
+
+Everything is plain numpy in float64 / int64 (``w4_oracle.py``).
+"""
+from .w4_oracle import *  # noqa: F401,F403
