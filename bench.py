@@ -1,0 +1,355 @@
+#!/usr/bin/env python3
+"""Benchmark of the int4-weight linear layer on one node.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line on rank 0.
+
+Headline workload: W4A16 decode, M=1 token, K=4096, N=14336, group 128, fp16
+scales (symmetric). A step is one layer call at that token count: below 512
+tokens the layer runs the W4A16 path, so one call of ``w4a16_gemm`` is the
+whole hot path of a decode step. ``value`` is the weight bytes streamed per
+second (GB/s) with inputs resident in HBM; 16 distinct weight copies (485 MB,
+more than the 129 MB L2) rotate between calls, so every call reads HBM.
+Calls are replayed from a CUDA graph so launch latency on the host does not
+gate the GPU.
+
+The other rows of the hot path are measured in the same run and reported
+under ``rows``: per-token quantization + W4A8 GEMM on the prefill and
+diffusion shapes, and the W4AFP8 grouped expert GEMMs.
+
+Multi-GPU: the layer is replicated; each rank runs the same workload on its
+own GPU with no collective in the data path (weak scaling). The timed region
+is bracketed by a barrier and a synchronize, and rank 0 reports the maximum
+time over ranks.
+
+``--impl reference`` times the CPU oracle (numpy, float64) on the same
+workload and metric, each step a bounded column sample of the decode GEMV.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synthetic as S  # noqa: E402
+
+METRIC = "W4A8 GEMM TOPS (% int8/fp8 peak); W4A16 M=1 weight GB/s (% HBM)"
+DEC_M, DEC_K, DEC_N, DEC_G = 1, 4096, 14336, 128
+N_COPIES = 16
+GRAPH_CALLS = 200
+
+# DRAM bytes (read + write) per launch from ncu, keyed by the SHA-256 of the
+# kernel's source file at capture time; reported only while the source matches.
+TRAFFIC = {}
+
+
+def _sha(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs"), d.get("bf16_tflops"), d.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def decode_bytes(M=DEC_M, K=DEC_K, N=DEC_N, G=DEC_G, zeros=False):
+    """Algorithmic bytes of one W4A16 call: packed weights, scales (+zeros), x in, y out."""
+    b = K * N // 2 + (K // G) * N * 2 + M * K * 2 + M * N * 2
+    if zeros:
+        b += (K // G) * N * 2
+    return b
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import int4_weight_quantized_w4_gb300 as w4
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w4.load()
+    stream = torch.cuda.Stream(dev)
+    hbm, bf16_tf, bf16_tf_sus, peak_kind = measured_peaks()
+
+    def bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    # --- inputs resident in HBM ---
+    xb = S.activations_bf16(DEC_M, DEC_K, seed=0)
+    x = bf16(xb)
+    qws = [torch.from_numpy(S.random_words((DEC_K // 8, DEC_N), seed=1, tag=20 + i)).to(dev) for i in range(N_COPIES)]
+    sws = [torch.from_numpy(S.scales_f16((DEC_K // DEC_G, DEC_N), seed=2, tag=30 + i)).to(dev) for i in range(N_COPIES)]
+    y = torch.empty((DEC_M, DEC_N), dtype=torch.bfloat16, device=dev)
+
+    def call(i, xin=x, yout=y):
+        w4.w4a16_gemm(xin, qws[i % N_COPIES], sws[i % N_COPIES], DEC_G, y=yout, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3) * N_COPIES):
+            call(i)
+    torch.cuda.synchronize()
+
+    # one graph of GRAPH_CALLS calls, rotating weight copies
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(GRAPH_CALLS):
+            call(i)
+    replays = max(1, args.steps // GRAPH_CALLS)
+    steps = replays * GRAPH_CALLS
+    with torch.cuda.stream(stream):          # replay() launches on the current stream
+        for _ in range(max(args.warmup, 3)):
+            g.replay()
+    torch.cuda.synchronize()
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk, torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(replays):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        torch.distributed.barrier()
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / steps
+    nbytes = decode_bytes()
+    value = world * steps * nbytes / (ms * 1e-3) / 1e9
+    gbs_per_launch = nbytes / (ms_per_step * 1e-3) / 1e9
+
+    # --- end to end through the public API with host buffers ---
+    x_host = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).pin_memory()
+    y_host = torch.empty((DEC_M, DEC_N), dtype=torch.bfloat16).pin_memory()
+    e2e_steps = min(steps, 20000)
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            x.copy_(x_host, non_blocking=True)
+            call(i)
+            y_host.copy_(y, non_blocking=True)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(e2e_steps):
+            x.copy_(x_host, non_blocking=True)
+            call(i)
+            y_host.copy_(y, non_blocking=True)
+    stream.synchronize()
+    e2e_s = time.perf_counter() - t0
+    e2e_value = world * e2e_steps * nbytes / e2e_s / 1e9
+
+    traffic = None
+    src = os.path.join(ROOT, "int4_weight_quantized_w4_gb300", "csrc", "w4a16.cu")
+    rec = TRAFFIC.get("w4a16")
+    if rec and rec[1] == _sha(src):
+        traffic = rec[0]
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16 x int4 -> fp32 acc",
+        "data": "synthetic (seeded SplitMix64: x~N(0,1) bf16, uniform int4 codes, fp16 scales U[0.005,0.02])",
+        "config": {"workload": "w4a16_decode", "M": DEC_M, "K": DEC_K, "N": DEC_N, "group": DEC_G,
+                   "scales": "fp16", "zeros": False, "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2: {N_COPIES} rotating weight copies "
+                         f"({N_COPIES * nbytes / 1e6:.0f} MB)",
+                   "timing": f"CUDA graph of {GRAPH_CALLS} calls replayed {replays}x, CUDA events"},
+        "roofline": {"bound": "hbm", "achieved": round(gbs_per_launch, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(gbs_per_launch / hbm, 4), "traffic": traffic,
+                     "peak_source": f"{peak_kind} hbm_gbs", "kernel": "w4a16_kernel",
+                     "algorithmic_bytes_per_launch": nbytes},
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": DEC_M * DEC_K * 2,
+                "d2h_bytes_per_step": DEC_M * DEC_N * 2, "steps": e2e_steps,
+                "how": "per step: pinned H2D of x, w4a16_gemm, D2H of y; host wall clock"},
+        "gpu_launches": steps,
+        "clocks": clk.summary(),
+    }
+    return line
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle legs
+# ---------------------------------------------------------------------------
+
+def oracle_decode_sample(cols, seed=0):
+    """Inputs for the decode GEMV restricted to a column block (same generator streams)."""
+    xb = S.activations_bf16(DEC_M, DEC_K, seed=seed)
+    qw = S.random_words((DEC_K // 8, DEC_N), seed=1, tag=20)[:, cols]
+    sw = S.scales_f16((DEC_K // DEC_G, DEC_N), seed=2, tag=30)[:, cols]
+    return xb, np.ascontiguousarray(qw), np.ascontiguousarray(sw)
+
+
+def cpu_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(budget_s=10.0):
+    """Time the oracle's W4A16 on column blocks of the decode GEMV for ~budget_s."""
+    import oracle as O
+    ncols = 1024
+    xb, qw, sw = oracle_decode_sample(np.arange(ncols))
+    O.w4a16_linear(xb, qw, sw, DEC_G)   # warm
+    n, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < budget_s:
+        O.w4a16_linear(xb, qw, sw, DEC_G)
+        n += 1
+    dt = time.perf_counter() - t0
+    nbytes = decode_bytes(N=ncols)
+    return {"value": round(n * nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": cpu_threads(), "kind": "oracle",
+            "sample": f"{n} oracle W4A16 calls on a {ncols}-column block of the M=1 decode GEMV "
+                      f"(K=4096, group 128), {dt:.1f} s; numpy float64"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle as O
+    ncols = 8
+    xb, qw, sw = oracle_decode_sample(np.arange(ncols))
+    for _ in range(max(args.warmup, 3)):
+        O.w4a16_linear(xb, qw, sw, DEC_G)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        O.w4a16_linear(xb, qw, sw, DEC_G)
+    dt = time.perf_counter() - t0
+    nbytes = decode_bytes(N=ncols)
+    value = args.steps * nbytes / dt / 1e9
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (same generator as the GPU arm)",
+        "config": {"workload": "w4a16_decode", "M": DEC_M, "K": DEC_K, "N": DEC_N, "group": DEC_G,
+                   "scales": "fp16", "zeros": False,
+                   "sample": f"each step: the oracle on an {ncols}-column block of the GEMV"},
+        "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": cpu_threads(), "kind": "oracle",
+                         "sample": f"{args.steps} steps, each an {ncols}-column block of the M=1 decode GEMV"},
+        "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl")
+    line = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,189 @@
+/*
+ * w4.h -- C ABI of the int4-weight quantized linear layer for NVIDIA GB300 (sm_103a).
+ *
+ * The layer computes y = x . W^T with W stored as 4-bit codes q in 0..15
+ * ("uint4b8": the weight value is q - 8) and a scale per group of input
+ * columns, optionally plus an additive zero per group:
+ *     w[k, n] = (q[k, n] - 8) * s[k / group, n]  (+ z[k / group, n])
+ *
+ * Sources (page title, then the section the rule comes from):
+ *   [INC]  vLLM API docs, inc.schemes.inc_w4a8_linear: INCXPUW4A8LinearMethod
+ *          (class docstring; create_weights; apply_weights).
+ *   [CT]   vLLM v0.10.1.1 API docs, compressed_tensors_w4a8_int:
+ *          CompressedTensorsW4A8Int (__init__; create_weights).
+ *   [FP8]  vLLM API docs, quantization.w4afp8: W4AFP8Config (__init__;
+ *          get_checkpoint_weight_mapper); _repack_signed_int4_to_uint4b8.
+ *   [ZEN]  vLLM API docs, kernels.linear.mixed_precision.zentorch:
+ *          ZentorchWNA16LinearKernel (can_implement; _zentorch_woq_eligible).
+ *   [OMNI] vllm-omni quantization/cpu_int4.py (module docstring; pack_nibbles).
+ *
+ * Conventions shared by every entry point
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller. The library
+ *     allocates no device memory and keeps no pointer after the call returns.
+ *   - All matrices are row-major and contiguous. Base pointers of matrices must
+ *     be 16-byte aligned; scale/zero/bias vectors 8-byte aligned.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream). Calls are asynchronous on that stream.
+ *   - Arguments are validated on the host before anything is launched. A
+ *     status other than W4_OK means nothing was launched and nothing written;
+ *     w4_last_error() then returns a message (per calling thread).
+ *   - A call with zero rows (M == 0 or R == 0) does nothing and returns W4_OK.
+ *   - N and K must be multiples of 8 ([INC] _DIM_ALIGNMENT and create_weights:
+ *     both GEMM dims multiples of 8). group is -1 (one group spanning K,
+ *     [CT] create_weights) or a positive divisor of K ([ZEN] can_implement).
+ *     Group sizes the kernels do not tile return W4_ERR_UNSUPPORTED.
+ *   - The pipelined kernels bound every wait. If a wait runs out, the kernel
+ *     records W4_ERR_TIMEOUT in a device status word and returns;
+ *     w4_device_status() reads and clears it.
+ *   - The < 512-token choice between W4A8 and W4A16 ([INC] _MIN_TOKENS_FOR_INT8)
+ *     is the caller's: the library has no dispatch between paths.
+ */
+#ifndef W4_H_
+#define W4_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  W4_OK = 0,
+  W4_ERR_NULL = 1,        /* a required pointer is NULL */
+  W4_ERR_ALIGN = 2,       /* N or K not a multiple of 8, or a pointer misaligned */
+  W4_ERR_GROUP = 3,       /* group is neither -1 nor a positive divisor of K */
+  W4_ERR_DTYPE = 4,       /* dtype not accepted (e.g. bf16 scales to w4a8_gemm) */
+  W4_ERR_UNSUPPORTED = 5, /* valid per the layer's rules but outside what the kernels tile */
+  W4_ERR_SHAPE = 6,       /* negative or inconsistent sizes */
+  W4_ERR_CUDA = 7,        /* a CUDA runtime call failed (message in w4_last_error) */
+  W4_ERR_TIMEOUT = 8      /* a bounded wait inside a kernel ran out */
+} w4_status;
+
+typedef enum {
+  W4_BF16 = 0,
+  W4_FP16 = 1,
+  W4_INT8 = 2,
+  W4_FP8_E4M3 = 3
+} w4_dtype;
+
+/*
+ * Dynamic per-token symmetric activation quantization.
+ * [INC] apply_weights (dynamic_per_token_int8_quant_ref(x, True, 8): per-token,
+ * symmetric, 8 bits) for int8; [FP8] W4AFP8Config.__init__ (input_quant: 8-bit
+ * float, symmetric, per token, dynamic) for e4m3.
+ *
+ *   x      [M, K] bf16 (x_dtype must be W4_BF16)
+ *   q      [M, K] int8 (q_dtype W4_INT8) or e4m3fn codes (q_dtype W4_FP8_E4M3)
+ *   scale  [M] fp32
+ * Per row: amax = max_k |x|; s = amax / Q in fp32 with Q = 127 (int8) or 448
+ * (e4m3); s = 1 when amax == 0.  int8: q = clamp(rne(x / s), -127, 127).
+ * e4m3: q = e4m3(x / s), round to nearest even, saturating at +-448. The
+ * divide is the IEEE fp32 divide. Errors: NULL, ALIGN (K % 8), DTYPE, SHAPE.
+ */
+w4_status w4_quant_act_per_token(const void* x, int32_t x_dtype, int64_t M, int64_t K,
+                                 int32_t q_dtype, void* q, float* scale, void* stream);
+
+/*
+ * W4A8 linear: int8 activations x int4 GPTQ weights, fp16 group scales.
+ * [INC] apply_weights (int4_gemm_w4a8(quant_x, x_scale, ..., qweight,
+ * scales_fp16, ..., group_size, ..., bias)) and the class docstring (both scale
+ * tensors are read as fp16; bf16 scales are rejected, not misread).
+ *
+ *   qx       [M, K] int8            (from w4_quant_act_per_token)
+ *   x_scale  [M] fp32
+ *   qweight  [K/8, N] int32, GPTQ "NT": nibble j (bits 4j..4j+3) of word
+ *            [i, n] is the code of input column 8i+j, output n
+ *   w_scale  [G, N] fp16 with G = K/group (G = 1 for group -1); w_scale_dtype
+ *            must be W4_FP16
+ *   bias     [N] bf16 or NULL
+ *   y        [M, N] bf16
+ * y[m,n] = bf16( x_scale[m] * sum_g w_scale[g,n] * P[m,g,n] + bias[n] ), with
+ * P[m,g,n] = sum_{k in g} qx[m,k] * (q[k,n] - 8) formed exactly in integers
+ * and the group scale applied in fp32. group: -1 or a multiple of 16 dividing
+ * K (else UNSUPPORTED); K % 16 == 0.
+ */
+w4_status w4a8_gemm(const void* qx, const float* x_scale, const void* qweight,
+                    const void* w_scale, int32_t w_scale_dtype, int32_t group,
+                    const void* bias, void* y, int64_t M, int64_t N, int64_t K, void* stream);
+
+/*
+ * The integer group partials of w4a8_gemm, from the same tensor-core path:
+ *   partials [M, G, N] int32, P[m,g,n] = sum_{k in g} qx[m,k] * (q[k,n] - 8).
+ * Same argument rules as w4a8_gemm. Meant for verifying the integer core
+ * (|P| <= 127 * 8 * group must stay below 2^24, so group <= 16512).
+ */
+w4_status w4a8_group_partials(const void* qx, const void* qweight, int32_t group,
+                              int32_t* partials, int64_t M, int64_t N, int64_t K, void* stream);
+
+/*
+ * W4A16 linear for decode: bf16 activations x the same GPTQ qweight
+ * ([INC] class docstring: int4_gemm_w4a16 reads bit-identical weights) with
+ * fp16 or bf16 group scales and optional bf16 additive zeros
+ * ([OMNI] module docstring: w = (q - 8) * scale + zero).
+ *
+ *   x        [M, K] bf16
+ *   qweight  [K/8, N] int32 GPTQ (as in w4a8_gemm)
+ *   w_scale  [G, N], w_scale_dtype W4_FP16 or W4_BF16
+ *   zeros    [G, N] bf16 or NULL (symmetric)
+ *   bias     [N] bf16 or NULL
+ *   y        [M, N] bf16
+ * y[m,n] = bf16( sum_g [ s[g,n] * sum_{k in g} x[m,k] (q[k,n]-8)
+ *                        + z[g,n] * sum_{k in g} x[m,k] ] + bias[n] ),
+ * products exact, sums in fp32. Built for small M (tokens are processed in
+ * blocks of 8); group: -1 or a multiple of 32 dividing K; K % 32 == 0.
+ */
+w4_status w4a16_gemm(const void* x, const void* qweight, const void* w_scale, int32_t w_scale_dtype,
+                     const void* zeros, int32_t group, const void* bias, void* y,
+                     int64_t M, int64_t N, int64_t K, void* stream);
+
+/*
+ * W4AFP8 grouped expert linear ([FP8] W4AFP8Config: int4 group-128 routed
+ * experts, symmetric, fp8 per-token dynamic activations; get_checkpoint_weight_mapper:
+ * compressed-tensors "weight_packed" / "weight_scale" layout).
+ *
+ *   qx              [R, K] e4m3fn codes, rows grouped by expert
+ *   x_scale         [R] fp32
+ *   expert_offsets  DEVICE int32 [E+1]: rows of expert e are
+ *                   [offsets[e], offsets[e+1]); offsets[0] = 0, offsets[E] = R,
+ *                   non-decreasing (an expert may own no rows)
+ *   qweight         [E, N, K/8] int32: nibble j of word [e, n, i] is the code
+ *                   of input column 8i+j of output n of expert e
+ *   w_scale         [E, N, K/group] fp16 (w_scale_dtype W4_FP16)
+ *   y               [R, N] bf16
+ * y[r,n] = bf16( x_scale[r] * sum_g w_scale[e,n,g] * sum_{k in g} x[r,k] (q[e,n,k]-8) )
+ * with e the expert owning row r. group: a multiple of 16 dividing K, or -1.
+ * Offsets are not validated on the host (they live on the device); rows outside
+ * [0, R) are never written.
+ */
+w4_status w4afp8_moe_grouped_gemm(const void* qx, const float* x_scale, const int32_t* expert_offsets,
+                                  int32_t E, const void* qweight, const void* w_scale,
+                                  int32_t w_scale_dtype, int32_t group, void* y,
+                                  int64_t R, int64_t N, int64_t K, void* stream);
+
+/* Message for the last non-OK status returned to the calling thread ("" if none). */
+const char* w4_last_error(void);
+
+/* Name of a status code. */
+const char* w4_status_string(int32_t status);
+
+/*
+ * Synchronizes `stream`, then reads and clears the device status word that the
+ * pipelined kernels set when a bounded wait runs out. Returns W4_OK,
+ * W4_ERR_TIMEOUT, or W4_ERR_CUDA if the synchronize itself failed.
+ */
+w4_status w4_device_status(void* stream);
+
+/*
+ * Self-test of the bounded-wait machinery: launches one CTA that waits on an
+ * mbarrier nothing ever arrives at, with a limit of `spin_limit` polls (> 0).
+ * The wait runs out, the kernel records W4_ERR_TIMEOUT and returns; a
+ * following w4_device_status() returns W4_ERR_TIMEOUT and clears it.
+ */
+w4_status w4_selftest_bounded_wait(int64_t spin_limit, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4_H_ */

@@ -1,0 +1,188 @@
+"""int4-weight quantized linear layer for NVIDIA GB300 (sm_103a).
+
+A thin ctypes binding over the C ABI in ``include/w4.h`` (``libw4.so``). Each
+function has the name of the C entry point it calls and only marshals
+arguments: it checks tensor shapes and dtypes, allocates outputs with PyTorch
+when the caller passes none, and passes raw device pointers plus the current
+CUDA stream. Every step of the computation runs in the library's kernels;
+there is no fallback. If ``libw4.so`` has not been built the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "W4Error", "load", "library_path",
+    "w4_quant_act_per_token", "w4a8_gemm", "w4a8_group_partials", "w4a16_gemm",
+    "w4afp8_moe_grouped_gemm", "w4_device_status", "w4_selftest_bounded_wait",
+    "W4_OK", "W4_ERR_NULL", "W4_ERR_ALIGN", "W4_ERR_GROUP", "W4_ERR_DTYPE",
+    "W4_ERR_UNSUPPORTED", "W4_ERR_SHAPE", "W4_ERR_CUDA", "W4_ERR_TIMEOUT",
+    "EXPORTED_SYMBOLS",
+]
+
+(W4_OK, W4_ERR_NULL, W4_ERR_ALIGN, W4_ERR_GROUP, W4_ERR_DTYPE, W4_ERR_UNSUPPORTED,
+ W4_ERR_SHAPE, W4_ERR_CUDA, W4_ERR_TIMEOUT) = range(9)
+W4_BF16, W4_FP16, W4_INT8, W4_FP8_E4M3 = range(4)
+
+_DIR = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_DIR, "libw4.so")
+
+_P, _I32, _I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+# name -> (restype, argtypes); mirrors include/w4.h
+_SIGNATURES = {
+    "w4_quant_act_per_token": (_I32, [_P, _I32, _I64, _I64, _I32, _P, _P, _P]),
+    "w4a8_gemm": (_I32, [_P, _P, _P, _P, _I32, _I32, _P, _P, _I64, _I64, _I64, _P]),
+    "w4a8_group_partials": (_I32, [_P, _P, _I32, _P, _I64, _I64, _I64, _P]),
+    "w4a16_gemm": (_I32, [_P, _P, _P, _I32, _P, _I32, _P, _P, _I64, _I64, _I64, _P]),
+    "w4afp8_moe_grouped_gemm": (_I32, [_P, _P, _P, _I32, _P, _P, _I32, _I32, _P, _I64, _I64, _I64, _P]),
+    "w4_last_error": (ctypes.c_char_p, []),
+    "w4_status_string": (ctypes.c_char_p, [_I32]),
+    "w4_device_status": (_I32, [_P]),
+    "w4_selftest_bounded_wait": (_I32, [_I64, _P]),
+}
+EXPORTED_SYMBOLS = tuple(_SIGNATURES)
+
+_lib = None
+
+
+class W4Error(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(message)
+        self.status = status
+
+
+def load() -> ctypes.CDLL:
+    """Load ``libw4.so`` (once). Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(library_path):
+            raise RuntimeError(f"{library_path} is missing: build it first "
+                               "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(library_path)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype, fn.argtypes = res, args
+        _lib = lib
+    return _lib
+
+
+def _check(status: int, what: str):
+    if status != W4_OK:
+        lib = load()
+        msg = lib.w4_last_error().decode() or lib.w4_status_string(status).decode()
+        raise W4Error(status, f"{what}: {lib.w4_status_string(status).decode()}: {msg}")
+
+
+def _stream(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _cuda2d(t, name, dtypes):
+    if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dim() == 2 and t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous 2-D CUDA tensor")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name} must have dtype in {dtypes}, got {t.dtype}")
+
+
+def _scale_dtype(t):
+    return {torch.float16: W4_FP16, torch.bfloat16: W4_BF16}.get(t.dtype, -1)
+
+
+def w4_quant_act_per_token(x, q_dtype: str = "int8", q=None, scale=None, stream=None):
+    """Per-token symmetric quantization of bf16 ``x [M, K]``; returns ``(q, scale)``
+    with q int8 (``q_dtype="int8"``) or float8_e4m3fn (``"fp8"``) and fp32 scales."""
+    _cuda2d(x, "x", (torch.bfloat16,))
+    M, K = x.shape
+    if q_dtype == "int8":
+        qd, tdt = W4_INT8, torch.int8
+    elif q_dtype == "fp8":
+        qd, tdt = W4_FP8_E4M3, torch.float8_e4m3fn
+    else:
+        raise ValueError("q_dtype must be 'int8' or 'fp8'")
+    q = torch.empty((M, K), dtype=tdt, device=x.device) if q is None else q
+    scale = torch.empty((M,), dtype=torch.float32, device=x.device) if scale is None else scale
+    if q.shape != (M, K) or scale.shape != (M,):
+        raise ValueError("output shapes do not match x")
+    _check(load().w4_quant_act_per_token(_ptr(x), W4_BF16, M, K, qd, _ptr(q), _ptr(scale),
+                                         _stream(stream, x.device)), "w4_quant_act_per_token")
+    return q, scale
+
+
+def w4a8_gemm(qx, x_scale, qweight, w_scale, group: int, bias=None, y=None, stream=None):
+    """W4A8 linear: int8 ``qx [M, K]`` with fp32 ``x_scale [M]`` times GPTQ
+    ``qweight [K/8, N]`` with fp16 ``w_scale [G, N]``; returns bf16 ``y [M, N]``."""
+    _cuda2d(qx, "qx", (torch.int8,))
+    _cuda2d(qweight, "qweight", (torch.int32,))
+    M, K = qx.shape
+    N = qweight.shape[1]
+    if qweight.shape[0] * 8 != K or x_scale.shape != (M,) or w_scale.dim() != 2 or w_scale.shape[1] != N:
+        raise ValueError("inconsistent shapes for w4a8_gemm")
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=qx.device) if y is None else y
+    _check(load().w4a8_gemm(_ptr(qx), _ptr(x_scale), _ptr(qweight), _ptr(w_scale), _scale_dtype(w_scale),
+                            group, _ptr(bias), _ptr(y), M, N, K, _stream(stream, qx.device)), "w4a8_gemm")
+    return y
+
+
+def w4a8_group_partials(qx, qweight, group: int, out=None, stream=None):
+    """Integer group partials ``P [M, G, N]`` (int32) of the W4A8 product."""
+    _cuda2d(qx, "qx", (torch.int8,))
+    _cuda2d(qweight, "qweight", (torch.int32,))
+    M, K = qx.shape
+    N = qweight.shape[1]
+    G = 1 if group == -1 else (K // group if group > 0 else 0)
+    out = torch.empty((M, G, N), dtype=torch.int32, device=qx.device) if out is None else out
+    _check(load().w4a8_group_partials(_ptr(qx), _ptr(qweight), group, _ptr(out), M, N, K,
+                                      _stream(stream, qx.device)), "w4a8_group_partials")
+    return out
+
+
+def w4a16_gemm(x, qweight, w_scale, group: int, zeros=None, bias=None, y=None, stream=None):
+    """W4A16 linear: bf16 ``x [M, K]`` times GPTQ ``qweight [K/8, N]`` with fp16
+    or bf16 ``w_scale [G, N]`` and optional bf16 ``zeros [G, N]``."""
+    _cuda2d(x, "x", (torch.bfloat16,))
+    _cuda2d(qweight, "qweight", (torch.int32,))
+    M, K = x.shape
+    N = qweight.shape[1]
+    if qweight.shape[0] * 8 != K or w_scale.dim() != 2 or w_scale.shape[1] != N:
+        raise ValueError("inconsistent shapes for w4a16_gemm")
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device) if y is None else y
+    _check(load().w4a16_gemm(_ptr(x), _ptr(qweight), _ptr(w_scale), _scale_dtype(w_scale), _ptr(zeros), group,
+                             _ptr(bias), _ptr(y), M, N, K, _stream(stream, x.device)), "w4a16_gemm")
+    return y
+
+
+def w4afp8_moe_grouped_gemm(qx, x_scale, expert_offsets, qweight, w_scale, group: int, y=None, stream=None):
+    """Grouped expert linear: e4m3 ``qx [R, K]`` (rows grouped by expert, as
+    float8_e4m3fn or uint8 codes), fp32 ``x_scale [R]``, int32 device
+    ``expert_offsets [E+1]``, ``qweight [E, N, K/8]``, fp16 ``w_scale [E, N, G]``."""
+    _cuda2d(qx, "qx", (torch.float8_e4m3fn, torch.uint8))
+    R, K = qx.shape
+    if qweight.dim() != 3 or not qweight.is_contiguous() or qweight.dtype != torch.int32:
+        raise ValueError("qweight must be a contiguous int32 [E, N, K/8] tensor")
+    E, N = qweight.shape[0], qweight.shape[1]
+    if qweight.shape[2] * 8 != K or expert_offsets.shape != (E + 1,) or x_scale.shape != (R,) \
+            or w_scale.dim() != 3 or w_scale.shape[:2] != (E, N):
+        raise ValueError("inconsistent shapes for w4afp8_moe_grouped_gemm")
+    y = torch.empty((R, N), dtype=torch.bfloat16, device=qx.device) if y is None else y
+    _check(load().w4afp8_moe_grouped_gemm(_ptr(qx), _ptr(x_scale), _ptr(expert_offsets), E, _ptr(qweight),
+                                          _ptr(w_scale), _scale_dtype(w_scale), group, _ptr(y), R, N, K,
+                                          _stream(stream, qx.device)), "w4afp8_moe_grouped_gemm")
+    return y
+
+
+def w4_device_status(stream=None, device=None) -> int:
+    """Synchronize the stream and return (and clear) the kernels' status word."""
+    return int(load().w4_device_status(_stream(stream, device)))
+
+
+def w4_selftest_bounded_wait(spin_limit: int, stream=None, device=None):
+    _check(load().w4_selftest_bounded_wait(int(spin_limit), _stream(stream, device)), "w4_selftest_bounded_wait")

@@ -1,0 +1,224 @@
+// Public C entry points: host-side argument validation, then one launch.
+// Nothing is launched when validation fails; the status says why and
+// w4_last_error() holds a message for the calling thread.
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+w4_status fail(w4_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+w4_status ok() {
+  g_last_error[0] = '\0';
+  return W4_OK;
+}
+
+w4_status from_cuda(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return ok();
+  return fail(W4_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Device status word; bounded waits in the kernels record timeouts here.
+__device__ unsigned int g_device_status;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_status_mu;
+unsigned int* g_status_ptr[kMaxDevices] = {};
+
+// Address of this device's status word (looked up once per device).
+cudaError_t status_ptr(unsigned int** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_status_mu);
+  if (g_status_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_device_status);
+    if (e != cudaSuccess) return e;
+    g_status_ptr[dev] = static_cast<unsigned int*>(p);
+  }
+  *out = g_status_ptr[dev];
+  return cudaSuccess;
+}
+
+// Shared checks for the packed-weight GEMMs. On success *geff is the
+// effective group (K for -1).
+w4_status check_dims_group(int64_t M, int64_t N, int64_t K, int32_t group, int32_t* geff) {
+  if (M < 0 || N <= 0 || K <= 0) return fail(W4_ERR_SHAPE, "sizes must be M >= 0, N > 0, K > 0 (M=%lld N=%lld K=%lld)",
+                                             (long long)M, (long long)N, (long long)K);
+  if (N % 8 != 0 || K % 8 != 0)
+    return fail(W4_ERR_ALIGN, "N and K must be multiples of 8, got N=%lld K=%lld", (long long)N, (long long)K);
+  if (group == -1) {
+    if (K > INT32_MAX) return fail(W4_ERR_UNSUPPORTED, "K=%lld too large for one group", (long long)K);
+    *geff = static_cast<int32_t>(K);
+  } else {
+    if (group <= 0 || K % group != 0)
+      return fail(W4_ERR_GROUP, "group %d must be -1 or a positive divisor of K=%lld", group, (long long)K);
+    *geff = group;
+  }
+  return W4_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* w4_last_error(void) { return g_last_error; }
+
+const char* w4_status_string(int32_t st) {
+  switch (st) {
+    case W4_OK: return "W4_OK";
+    case W4_ERR_NULL: return "W4_ERR_NULL";
+    case W4_ERR_ALIGN: return "W4_ERR_ALIGN";
+    case W4_ERR_GROUP: return "W4_ERR_GROUP";
+    case W4_ERR_DTYPE: return "W4_ERR_DTYPE";
+    case W4_ERR_UNSUPPORTED: return "W4_ERR_UNSUPPORTED";
+    case W4_ERR_SHAPE: return "W4_ERR_SHAPE";
+    case W4_ERR_CUDA: return "W4_ERR_CUDA";
+    case W4_ERR_TIMEOUT: return "W4_ERR_TIMEOUT";
+    default: return "W4_ERR_UNKNOWN";
+  }
+}
+
+w4_status w4_quant_act_per_token(const void* x, int32_t x_dtype, int64_t M, int64_t K, int32_t q_dtype,
+                                 void* q, float* scale, void* stream) {
+  if (M < 0 || K <= 0) return fail(W4_ERR_SHAPE, "sizes must be M >= 0, K > 0 (M=%lld K=%lld)", (long long)M, (long long)K);
+  if (x_dtype != W4_BF16) return fail(W4_ERR_DTYPE, "x_dtype must be W4_BF16");
+  if (q_dtype != W4_INT8 && q_dtype != W4_FP8_E4M3) return fail(W4_ERR_DTYPE, "q_dtype must be W4_INT8 or W4_FP8_E4M3");
+  if (K % 8 != 0) return fail(W4_ERR_ALIGN, "K must be a multiple of 8, got %lld", (long long)K);
+  if (M == 0) return ok();
+  if (!x || !q || !scale) return fail(W4_ERR_NULL, "x, q and scale must be non-NULL");
+  if (!aligned(x, 16) || !aligned(q, 16) || !aligned(scale, 4))
+    return fail(W4_ERR_ALIGN, "x and q must be 16-byte aligned, scale 4-byte aligned");
+  if (M > INT32_MAX) return fail(W4_ERR_UNSUPPORTED, "M too large");
+  return from_cuda(w4::launch_quant_per_token(x, M, K, q_dtype == W4_FP8_E4M3, q, scale,
+                                              static_cast<cudaStream_t>(stream)),
+                   "w4_quant_act_per_token launch");
+}
+
+static w4_status w4a8_common(const void* qx, const float* x_scale, const void* qweight, const void* w_scale,
+                             int32_t w_scale_dtype, int32_t group, const void* bias, void* out,
+                             int64_t M, int64_t N, int64_t K, bool partials, void* stream) {
+  int32_t g = 0;
+  w4_status st = check_dims_group(M, N, K, group, &g);
+  if (st != W4_OK) return st;
+  if (!partials && w_scale_dtype != W4_FP16)
+    return fail(W4_ERR_DTYPE, "w4a8_gemm reads weight scales as fp16; pass fp16 scales (W4_FP16)");
+  if (K % 16 != 0 || g % 16 != 0)
+    return fail(W4_ERR_UNSUPPORTED, "w4a8 tiles need K and the group to be multiples of 16 (K=%lld group=%d)",
+                (long long)K, g);
+  if (partials && g > 16512) return fail(W4_ERR_UNSUPPORTED, "partials need group <= 16512 to stay exact");
+  if (M == 0) return ok();
+  if (!qx || !qweight || !out || (!partials && (!x_scale || !w_scale)))
+    return fail(W4_ERR_NULL, "required pointer is NULL");
+  if (!aligned(qx, 16) || !aligned(qweight, 16) || !aligned(out, 16) ||
+      (!partials && (!aligned(w_scale, 8) || !aligned(x_scale, 4))) || (bias && !aligned(bias, 8)))
+    return fail(W4_ERR_ALIGN, "matrices must be 16-byte aligned, vectors 8-byte aligned");
+  if (M > INT32_MAX || N > INT32_MAX) return fail(W4_ERR_UNSUPPORTED, "M or N too large");
+  unsigned int* status = nullptr;
+  cudaError_t e = status_ptr(&status);
+  if (e != cudaSuccess) return from_cuda(e, "device status word");
+  w4::W4A8Args a{qx, x_scale, qweight, w_scale, partials ? nullptr : bias, out, nullptr, 1, M, N, K, g, partials, status};
+  return from_cuda(w4::launch_w4a8_dense(a, static_cast<cudaStream_t>(stream)), "w4a8 launch");
+}
+
+w4_status w4a8_gemm(const void* qx, const float* x_scale, const void* qweight, const void* w_scale,
+                    int32_t w_scale_dtype, int32_t group, const void* bias, void* y,
+                    int64_t M, int64_t N, int64_t K, void* stream) {
+  return w4a8_common(qx, x_scale, qweight, w_scale, w_scale_dtype, group, bias, y, M, N, K, false, stream);
+}
+
+w4_status w4a8_group_partials(const void* qx, const void* qweight, int32_t group, int32_t* partials,
+                              int64_t M, int64_t N, int64_t K, void* stream) {
+  return w4a8_common(qx, nullptr, qweight, nullptr, W4_FP16, group, nullptr, partials, M, N, K, true, stream);
+}
+
+w4_status w4a16_gemm(const void* x, const void* qweight, const void* w_scale, int32_t w_scale_dtype,
+                     const void* zeros, int32_t group, const void* bias, void* y,
+                     int64_t M, int64_t N, int64_t K, void* stream) {
+  int32_t g = 0;
+  w4_status st = check_dims_group(M, N, K, group, &g);
+  if (st != W4_OK) return st;
+  if (w_scale_dtype != W4_FP16 && w_scale_dtype != W4_BF16)
+    return fail(W4_ERR_DTYPE, "w4a16_gemm scales must be W4_FP16 or W4_BF16");
+  if (K % 32 != 0 || g % 32 != 0)
+    return fail(W4_ERR_UNSUPPORTED, "w4a16 tiles need K and the group to be multiples of 32 (K=%lld group=%d)",
+                (long long)K, g);
+  if (M == 0) return ok();
+  if (!x || !qweight || !w_scale || !y) return fail(W4_ERR_NULL, "x, qweight, w_scale and y must be non-NULL");
+  if (!aligned(x, 16) || !aligned(qweight, 16) || !aligned(y, 8) || !aligned(w_scale, 8) ||
+      (zeros && !aligned(zeros, 8)) || (bias && !aligned(bias, 8)))
+    return fail(W4_ERR_ALIGN, "x and qweight must be 16-byte aligned; y, scales, zeros, bias 8-byte aligned");
+  if (M > INT32_MAX || N > INT32_MAX) return fail(W4_ERR_UNSUPPORTED, "M or N too large");
+  w4::W4A16Args a{x, qweight, w_scale, w_scale_dtype == W4_BF16, zeros, bias, y, M, N, K, g};
+  return from_cuda(w4::launch_w4a16(a, static_cast<cudaStream_t>(stream)), "w4a16 launch");
+}
+
+w4_status w4afp8_moe_grouped_gemm(const void* qx, const float* x_scale, const int32_t* expert_offsets, int32_t E,
+                                  const void* qweight, const void* w_scale, int32_t w_scale_dtype, int32_t group,
+                                  void* y, int64_t R, int64_t N, int64_t K, void* stream) {
+  int32_t g = 0;
+  w4_status st = check_dims_group(R, N, K, group, &g);
+  if (st != W4_OK) return st;
+  if (E <= 0) return fail(W4_ERR_SHAPE, "E must be positive, got %d", E);
+  if (w_scale_dtype != W4_FP16) return fail(W4_ERR_DTYPE, "expert weight scales must be fp16 (W4_FP16)");
+  if (K % 16 != 0 || g % 16 != 0)
+    return fail(W4_ERR_UNSUPPORTED, "expert tiles need K and the group to be multiples of 16 (K=%lld group=%d)",
+                (long long)K, g);
+  if (R == 0) return ok();
+  if (!qx || !x_scale || !expert_offsets || !qweight || !w_scale || !y)
+    return fail(W4_ERR_NULL, "required pointer is NULL");
+  if (!aligned(qx, 16) || !aligned(qweight, 16) || !aligned(y, 16) || !aligned(w_scale, 8) ||
+      !aligned(x_scale, 4) || !aligned(expert_offsets, 4))
+    return fail(W4_ERR_ALIGN, "matrices must be 16-byte aligned, vectors aligned to their element size");
+  if (R > INT32_MAX || N > INT32_MAX) return fail(W4_ERR_UNSUPPORTED, "R or N too large");
+  unsigned int* status = nullptr;
+  cudaError_t e = status_ptr(&status);
+  if (e != cudaSuccess) return from_cuda(e, "device status word");
+  w4::W4A8Args a{qx, x_scale, qweight, w_scale, nullptr, y, expert_offsets, E, R, N, K, g, false, status};
+  return from_cuda(w4::launch_w4afp8_experts(a, static_cast<cudaStream_t>(stream)), "w4afp8 experts launch");
+}
+
+w4_status w4_device_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return from_cuda(e, "cudaStreamSynchronize");
+  unsigned int* p = nullptr;
+  e = status_ptr(&p);
+  if (e != cudaSuccess) return from_cuda(e, "device status word");
+  unsigned int v = 0;
+  e = cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return from_cuda(e, "read device status");
+  if (v != 0) {
+    const unsigned int zero = 0;
+    e = cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return from_cuda(e, "clear device status");
+    return fail(static_cast<w4_status>(v), "a kernel recorded %s", w4_status_string(static_cast<int32_t>(v)));
+  }
+  return ok();
+}
+
+w4_status w4_selftest_bounded_wait(int64_t spin_limit, void* stream) {
+  if (spin_limit <= 0) return fail(W4_ERR_SHAPE, "spin_limit must be positive");
+  unsigned int* status = nullptr;
+  cudaError_t e = status_ptr(&status);
+  if (e != cudaSuccess) return from_cuda(e, "device status word");
+  return from_cuda(w4::launch_bounded_wait_selftest(spin_limit, status, static_cast<cudaStream_t>(stream)),
+                   "selftest launch");
+}
+
+}  // extern "C"

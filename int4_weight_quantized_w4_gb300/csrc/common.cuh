@@ -1,0 +1,137 @@
+// Device-side helpers shared by the kernels of the int4-weight linear layer.
+// sm_103a only: every helper is plain CUDA or inline PTX for that target.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "w4.h"
+
+#define W4_DEV __device__ __forceinline__
+
+namespace w4 {
+
+// ---------------------------------------------------------------------------
+// device status word (bounded waits record W4_ERR_TIMEOUT here)
+// ---------------------------------------------------------------------------
+
+// Sets *status to `code` once (the first error wins).
+W4_DEV void report(unsigned int* status, unsigned int code) {
+  if (status != nullptr) atomicCAS(status, 0u, code);
+}
+
+// ---------------------------------------------------------------------------
+// bit helpers
+// ---------------------------------------------------------------------------
+
+W4_DEV uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// (a & b) | c as one LOP3.
+W4_DEV uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// (a & b) ^ c as one LOP3.
+W4_DEV uint32_t and_xor(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+W4_DEV float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+W4_DEV float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// fp32 -> bf16 bits, round to nearest even (finite inputs).
+W4_DEV uint32_t f32_to_bf16_bits(float f) {
+  uint16_t h;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(f));
+  return h;
+}
+
+W4_DEV uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+W4_DEV float half_bits_to_f32(uint32_t h16) {
+  float f;
+  asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(static_cast<uint16_t>(h16)));
+  return f;
+}
+
+// ---------------------------------------------------------------------------
+// global memory access
+// ---------------------------------------------------------------------------
+
+// 16-byte streaming load that bypasses L1 (each weight byte is read once).
+W4_DEV uint4 ld_stream_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+W4_DEV uint4 ld_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+W4_DEV uint2 ld_nc_v2(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier with bounded waits
+// ---------------------------------------------------------------------------
+
+W4_DEV uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+W4_DEV void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_addr(bar)), "r"(count));
+}
+
+W4_DEV void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+W4_DEV void mbar_arrive(uint64_t* bar) {
+  asm volatile("{.reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0];}" :: "r"(smem_addr(bar)) : "memory");
+}
+
+W4_DEV void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("{.reg .b64 st; mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;}"
+               :: "r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+
+W4_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{.reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p;}"
+      : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
+
+// Waits for phase `parity` of `bar` to complete, polling at most `limit`
+// times. Returns false (after recording W4_ERR_TIMEOUT) if it never does.
+W4_DEV bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, long long limit, unsigned int* status) {
+  for (long long i = 0; i < limit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+  }
+  report(status, W4_ERR_TIMEOUT);
+  return false;
+}
+
+}  // namespace w4

@@ -1,0 +1,49 @@
+// Internal host-side launch functions, one per kernel family. The public
+// entry points in api.cu validate arguments and then call these; each returns
+// the cudaError_t of its launch.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace w4 {
+
+// Polls a bounded wait makes before it gives up (about a second of spinning).
+constexpr long long kWaitLimit = 1LL << 24;
+
+cudaError_t launch_quant_per_token(const void* x, int64_t M, int64_t K, bool fp8, void* q,
+                                   float* scale, cudaStream_t s);
+
+struct W4A16Args {
+  const void* x;
+  const void* qweight;
+  const void* w_scale;
+  bool scale_bf16;
+  const void* zeros;
+  const void* bias;
+  void* y;
+  int64_t M, N, K;
+  int32_t group;  // effective group (K when the caller passed -1)
+};
+cudaError_t launch_w4a16(const W4A16Args& a, cudaStream_t s);
+
+struct W4A8Args {
+  const void* act;        // int8 [M,K] (dense) or e4m3 [R,K] (experts)
+  const float* x_scale;   // [M] (ignored for partials)
+  const void* qweight;    // GPTQ [K/8,N] (dense) or CT [E,N,K/8] (experts)
+  const void* w_scale;    // fp16 [G,N] (dense) or [E,N,G] (experts)
+  const void* bias;       // bf16 [N] or nullptr
+  void* out;              // bf16 [M,N], or int32 [M,G,N] for partials
+  const int32_t* expert_offsets;  // device [E+1] (experts only)
+  int32_t E;
+  int64_t M, N, K;
+  int32_t group;          // effective group
+  bool partials;          // write int32 group partials instead of y
+  unsigned int* status;
+};
+cudaError_t launch_w4a8_dense(const W4A8Args& a, cudaStream_t s);
+cudaError_t launch_w4afp8_experts(const W4A8Args& a, cudaStream_t s);
+
+cudaError_t launch_bounded_wait_selftest(long long limit, unsigned int* status, cudaStream_t s);
+
+}  // namespace w4

@@ -1,0 +1,139 @@
+// Dynamic per-token symmetric activation quantization (int8 or e4m3).
+//
+// vLLM API docs, inc.schemes.inc_w4a8_linear, INCXPUW4A8LinearMethod.apply_weights:
+// activations are quantized per token, symmetric, to 8 bits right before the
+// W4A8 GEMM. vLLM API docs, quantization.w4afp8, W4AFP8Config.__init__: the
+// expert activations are 8-bit float, symmetric, per token, dynamic.
+//
+// Per row: amax = max |x|; s = amax / Q (IEEE fp32 divide; s = 1 if amax = 0);
+// int8: q = clamp(rne(x / s), -127, 127); e4m3: q = satfinite-rne(x / s).
+//
+// One CTA per row. Each thread keeps its 8-element chunks of the row in
+// registers (16-byte loads), the row maximum is a warp-shuffle butterfly plus
+// one shared-memory step, and the quantized chunks leave as 8-byte stores, so
+// HBM sees the row read once and the codes written once (3 bytes per element).
+#include "common.cuh"
+#include "launch.h"
+
+namespace w4 {
+namespace {
+
+constexpr int kMaxThreads = 256;
+
+W4_DEV float row_max(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  const int nw = (blockDim.x + 31) >> 5;
+  float m = 0.f;
+  for (int i = 0; i < nw; ++i) m = fmaxf(m, red[i]);
+  return m;
+}
+
+W4_DEV float chunk_absmax(const uint4& v) {
+  float m = fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x)));
+  m = fmaxf(m, fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y))));
+  m = fmaxf(m, fmaxf(fabsf(bf16_lo(v.z)), fabsf(bf16_hi(v.z))));
+  m = fmaxf(m, fmaxf(fabsf(bf16_lo(v.w)), fabsf(bf16_hi(v.w))));
+  return m;
+}
+
+W4_DEV uint32_t q_int8(float x, float s) {
+  int q = __float2int_rn(__fdiv_rn(x, s));
+  q = max(-127, min(127, q));
+  return static_cast<uint32_t>(q) & 0xFFu;
+}
+
+// Two int8 codes from one bf16x2 word, low element in the low byte.
+W4_DEV uint32_t q_int8_pair(uint32_t w, float s) {
+  return q_int8(bf16_lo(w), s) | (q_int8(bf16_hi(w), s) << 8);
+}
+
+// Two e4m3 codes from one bf16x2 word, low element in the low byte.
+W4_DEV uint32_t q_e4m3_pair(uint32_t w, float s) {
+  const float lo = __fdiv_rn(bf16_lo(w), s), hi = __fdiv_rn(bf16_hi(w), s);
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+template <bool FP8>
+W4_DEV uint2 quant_chunk(const uint4& v, float s) {
+  uint2 o;
+  if (FP8) {
+    o.x = q_e4m3_pair(v.x, s) | (q_e4m3_pair(v.y, s) << 16);
+    o.y = q_e4m3_pair(v.z, s) | (q_e4m3_pair(v.w, s) << 16);
+  } else {
+    o.x = q_int8_pair(v.x, s) | (q_int8_pair(v.y, s) << 16);
+    o.y = q_int8_pair(v.z, s) | (q_int8_pair(v.w, s) << 16);
+  }
+  return o;
+}
+
+// NCH > 0: the row fits in registers, NCH chunks per thread.
+// NCH == 0: long rows, read twice (the second read mostly hits L2).
+template <int NCH, bool FP8>
+__global__ void __launch_bounds__(kMaxThreads) quant_rows(const uint4* __restrict__ x, int K8,
+                                                          uint2* __restrict__ q, float* __restrict__ scale) {
+  __shared__ float red[kMaxThreads / 32];
+  const size_t row = blockIdx.x;
+  const uint4* xr = x + row * static_cast<size_t>(K8);
+  uint2* qr = q + row * static_cast<size_t>(K8);
+  constexpr float kQ = FP8 ? 448.f : 127.f;
+  if constexpr (NCH > 0) {
+    uint4 v[NCH];
+    float m = 0.f;
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+      const int i = threadIdx.x + c * blockDim.x;
+      v[c] = (i < K8) ? ld_stream_v4(xr + i) : make_uint4(0, 0, 0, 0);
+      m = fmaxf(m, chunk_absmax(v[c]));
+    }
+    const float amax = row_max(m, red);
+    const float s = (amax == 0.f) ? 1.f : __fdiv_rn(amax, kQ);
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+      const int i = threadIdx.x + c * blockDim.x;
+      if (i < K8) qr[i] = quant_chunk<FP8>(v[c], s);
+    }
+    if (threadIdx.x == 0) scale[row] = s;
+  } else {
+    float m = 0.f;
+    for (int i = threadIdx.x; i < K8; i += blockDim.x) m = fmaxf(m, chunk_absmax(ld_nc_v4(xr + i)));
+    const float amax = row_max(m, red);
+    const float s = (amax == 0.f) ? 1.f : __fdiv_rn(amax, kQ);
+    for (int i = threadIdx.x; i < K8; i += blockDim.x) qr[i] = quant_chunk<FP8>(ld_stream_v4(xr + i), s);
+    if (threadIdx.x == 0) scale[row] = s;
+  }
+}
+
+template <bool FP8>
+cudaError_t launch(const void* x, int64_t M, int64_t K, void* q, float* scale, cudaStream_t s) {
+  const int K8 = static_cast<int>(K / 8);
+  int threads = ((K8 + 31) / 32) * 32;
+  if (threads > kMaxThreads) threads = kMaxThreads;
+  const int nch = (K8 + threads - 1) / threads;
+  const dim3 grid(static_cast<unsigned>(M));
+  auto xp = static_cast<const uint4*>(x);
+  auto qp = static_cast<uint2*>(q);
+  switch (nch) {
+    case 1: quant_rows<1, FP8><<<grid, threads, 0, s>>>(xp, K8, qp, scale); break;
+    case 2: quant_rows<2, FP8><<<grid, threads, 0, s>>>(xp, K8, qp, scale); break;
+    case 3: quant_rows<3, FP8><<<grid, threads, 0, s>>>(xp, K8, qp, scale); break;
+    case 4: quant_rows<4, FP8><<<grid, threads, 0, s>>>(xp, K8, qp, scale); break;
+    default: quant_rows<0, FP8><<<grid, threads, 0, s>>>(xp, K8, qp, scale); break;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_quant_per_token(const void* x, int64_t M, int64_t K, bool fp8, void* q, float* scale,
+                                   cudaStream_t s) {
+  if (K / 8 > INT32_MAX) return cudaErrorInvalidValue;
+  return fp8 ? launch<true>(x, M, K, q, scale, s) : launch<false>(x, M, K, q, scale, s);
+}
+
+}  // namespace w4

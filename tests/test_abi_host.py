@@ -1,0 +1,125 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds, loads
+and exports every symbol include/w4.h declares, and argument validation
+returns its documented status before anything is launched."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import int4_weight_quantized_w4_gb300 as w4
+from int4_weight_quantized_w4_gb300 import _build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "w4.h")
+FAKE = ctypes.c_void_p(1 << 20)    # 16-byte aligned, never dereferenced: validation fails first
+ODD = ctypes.c_void_p((1 << 20) + 4)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return w4.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:w4_status|const char\*|void)\s+(w4\w*)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("w4_quant_act_per_token", "w4a8_gemm", "w4a16_gemm", "w4afp8_moe_grouped_gemm"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert names, "no declarations parsed"
+    for n in names:
+        assert hasattr(lib, n), f"libw4.so does not export {n}"
+    assert set(names) == set(w4.EXPORTED_SYMBOLS), "binding signatures out of sync with the header"
+
+
+def test_status_strings(lib):
+    assert lib.w4_status_string(0) == b"W4_OK"
+    assert lib.w4_status_string(4) == b"W4_ERR_DTYPE"
+    assert lib.w4_status_string(99) == b"W4_ERR_UNKNOWN"
+
+
+def gemm(lib, **kw):
+    a = dict(qx=FAKE, sx=FAKE, qw=FAKE, ws=FAKE, wdt=w4.W4_FP16, group=128, bias=None, y=FAKE,
+             M=16, N=256, K=256)
+    a.update(kw)
+    return lib.w4a8_gemm(a["qx"], a["sx"], a["qw"], a["ws"], a["wdt"], a["group"], a["bias"], a["y"],
+                         a["M"], a["N"], a["K"], None)
+
+
+def test_w4a8_validation(lib):
+    assert gemm(lib, wdt=w4.W4_BF16) == w4.W4_ERR_DTYPE          # the fp16-scale rule
+    assert b"fp16" in lib.w4_last_error()
+    assert gemm(lib, N=260) == w4.W4_ERR_ALIGN                    # N % 8
+    assert gemm(lib, K=252) == w4.W4_ERR_ALIGN                    # K % 8
+    assert gemm(lib, group=96) == w4.W4_ERR_GROUP                 # does not divide K
+    assert gemm(lib, group=0) == w4.W4_ERR_GROUP
+    assert gemm(lib, group=-2) == w4.W4_ERR_GROUP
+    assert gemm(lib, K=264, group=-1) == w4.W4_ERR_UNSUPPORTED    # K % 16 for the MMA tiles
+    assert gemm(lib, K=256, group=8) == w4.W4_ERR_UNSUPPORTED     # group % 16
+    assert gemm(lib, M=-1) == w4.W4_ERR_SHAPE
+    assert gemm(lib, qx=None) == w4.W4_ERR_NULL
+    assert gemm(lib, y=ODD) == w4.W4_ERR_ALIGN
+    assert gemm(lib, M=0) == w4.W4_OK                             # empty: no-op, no launch
+    assert lib.w4_last_error() == b""
+
+
+def test_w4a8_partials_validation(lib):
+    assert lib.w4a8_group_partials(FAKE, FAKE, 128, None, 16, 256, 256, None) == w4.W4_ERR_NULL
+    assert lib.w4a8_group_partials(FAKE, FAKE, 100, FAKE, 16, 256, 256, None) == w4.W4_ERR_GROUP
+
+
+def test_w4a16_validation(lib):
+    def call(**kw):
+        a = dict(x=FAKE, qw=FAKE, ws=FAKE, wdt=w4.W4_FP16, z=None, group=128, bias=None, y=FAKE,
+                 M=1, N=256, K=256)
+        a.update(kw)
+        return lib.w4a16_gemm(a["x"], a["qw"], a["ws"], a["wdt"], a["z"], a["group"], a["bias"], a["y"],
+                              a["M"], a["N"], a["K"], None)
+    assert call(wdt=w4.W4_INT8) == w4.W4_ERR_DTYPE
+    assert call(group=16) == w4.W4_ERR_UNSUPPORTED
+    assert call(N=12) == w4.W4_ERR_ALIGN
+    assert call(group=3) == w4.W4_ERR_GROUP
+    assert call(x=None) == w4.W4_ERR_NULL
+    assert call(qw=ODD) == w4.W4_ERR_ALIGN
+    assert call(M=0) == w4.W4_OK
+
+
+def test_quant_validation(lib):
+    def call(**kw):
+        a = dict(x=FAKE, xdt=w4.W4_BF16, M=4, K=256, qdt=w4.W4_INT8, q=FAKE, s=FAKE)
+        a.update(kw)
+        return lib.w4_quant_act_per_token(a["x"], a["xdt"], a["M"], a["K"], a["qdt"], a["q"], a["s"], None)
+    assert call(xdt=w4.W4_FP16) == w4.W4_ERR_DTYPE
+    assert call(qdt=w4.W4_BF16) == w4.W4_ERR_DTYPE
+    assert call(K=12) == w4.W4_ERR_ALIGN
+    assert call(K=0) == w4.W4_ERR_SHAPE
+    assert call(q=None) == w4.W4_ERR_NULL
+    assert call(x=ODD) == w4.W4_ERR_ALIGN
+    assert call(M=0) == w4.W4_OK
+
+
+def test_moe_validation(lib):
+    def call(**kw):
+        a = dict(qx=FAKE, sx=FAKE, off=FAKE, E=64, qw=FAKE, ws=FAKE, wdt=w4.W4_FP16, group=128, y=FAKE,
+                 R=32, N=256, K=256)
+        a.update(kw)
+        return lib.w4afp8_moe_grouped_gemm(a["qx"], a["sx"], a["off"], a["E"], a["qw"], a["ws"], a["wdt"],
+                                           a["group"], a["y"], a["R"], a["N"], a["K"], None)
+    assert call(E=0) == w4.W4_ERR_SHAPE
+    assert call(wdt=w4.W4_BF16) == w4.W4_ERR_DTYPE
+    assert call(off=None) == w4.W4_ERR_NULL
+    assert call(group=24) == w4.W4_ERR_GROUP
+    assert call(R=0) == w4.W4_OK
+
+
+def test_selftest_rejects_bad_limit(lib):
+    assert lib.w4_selftest_bounded_wait(0, None) == w4.W4_ERR_SHAPE

@@ -1,0 +1,66 @@
+"""Per-token activation quantization on the GPU against the oracle, bit-exact
+(codes and fp32 scales), through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import int4_weight_quantized_w4_gb300 as w4
+import oracle as O
+import synthetic as S
+from _gpu import bf16, requires_cuda
+
+pytestmark = [pytest.mark.gpu, requires_cuda]
+
+
+def _run(xb, kind):
+    q, s = w4.w4_quant_act_per_token(bf16(xb), kind)
+    torch.cuda.synchronize()
+    q = q.cpu()
+    q = q.view(torch.uint8).numpy() if kind == "fp8" else q.numpy()
+    return q, s.cpu().numpy()
+
+
+def _check(xb, kind):
+    q, s = _run(xb, kind)
+    qr, sr = (O.quant_fp8_per_token if kind == "fp8" else O.quant_int8_per_token)(xb)
+    np.testing.assert_array_equal(s.view(np.uint32), sr.view(np.uint32))
+    np.testing.assert_array_equal(q, qr)
+
+
+@pytest.mark.parametrize("kind", ["int8", "fp8"])
+@pytest.mark.parametrize("M,K", [(1, 8), (3, 256), (16, 256), (7, 1408), (33, 2048), (64, 3072),
+                                 (5, 4096), (9, 8200), (4, 16384), (2, 24)])
+def test_quant_parity(kind, M, K):
+    _check(S.activations_bf16(M, K, seed=M * 7 + K, outlier_frac=0.01), kind)
+
+
+@pytest.mark.parametrize("kind", ["int8", "fp8"])
+def test_quant_special_rows(kind):
+    """Zero rows (s = 1), rows whose amax is the code maximum (s = 1, ties at
+    x.5), tiny and huge magnitudes, and sign mixtures."""
+    K = 64
+    rows = []
+    rows.append(np.zeros(K))
+    t = np.zeros(K); t[:8] = [127, 2.5, 3.5, -2.5, 126.5, -127, 0.5, 1.5]; rows.append(t)
+    t = np.zeros(K); t[:6] = [448, 17, 19, -17, 0.0625, -448]; rows.append(t)
+    rows.append(np.full(K, -3.0e-30))
+    rows.append(np.linspace(-1e30, 1e30, K))
+    t = np.zeros(K); t[K - 1] = 1e-3; rows.append(t)
+    xb = S.to_bf16_bits(np.stack(rows))
+    _check(xb, kind)
+
+
+@pytest.mark.parametrize("kind", ["int8", "fp8"])
+def test_quant_full_size_prefill(kind):
+    """The prefill activations at full size: 4096 tokens x 4096, 1% outlier channels x20."""
+    _check(S.activations_bf16(4096, 4096, seed=0, outlier_frac=0.01), kind)
+
+
+def test_quant_moe_rows_full_size():
+    """The expert down-projection input at full size: 32768 rows x 1408, e4m3."""
+    _check(S.activations_bf16(32768, 1408, seed=3), "fp8")
+
+
+def test_quant_empty():
+    q, s = w4.w4_quant_act_per_token(torch.empty((0, 64), dtype=torch.bfloat16, device="cuda"), "int8")
+    assert q.shape == (0, 64) and s.shape == (0,)

@@ -1,0 +1,99 @@
+"""W4A16 decode GEMM on the GPU against the oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import int4_weight_quantized_w4_gb300 as w4
+import oracle as O
+import synthetic as S
+from _compare import check_bf16_output
+from _gpu import bf16, bits, requires_cuda, to_dev
+
+pytestmark = [pytest.mark.gpu, requires_cuda]
+
+
+def _case(M, N, K, group, scale_dtype="f16", zeros=False, bias=False, seed=0, cols=None):
+    g = K if group == -1 else group
+    xb = S.activations_bf16(M, K, seed=seed)
+    qw = S.random_words((K // 8, N), seed=seed + 1)
+    sw = S.scales_f16((K // g, N), seed=seed + 2) if scale_dtype == "f16" else S.scales_bf16((K // g, N), seed=seed + 2)
+    zb = S.zeros_bf16((K // g, N), seed=seed + 3) if zeros else None
+    bb = S.bias_bf16(N, seed=seed + 4) if bias else None
+    sw_t = to_dev(sw) if scale_dtype == "f16" else bf16(sw)
+    y = w4.w4a16_gemm(bf16(xb), to_dev(qw), sw_t, group, zeros=None if zb is None else bf16(zb),
+                      bias=None if bb is None else bf16(bb))
+    torch.cuda.synchronize()
+    yb = bits(y)
+    if cols is None:
+        cols = np.arange(N)
+    r = O.w4a16_linear(xb, qw[:, cols], sw[:, cols], group, zeros_bits=None if zb is None else zb[:, cols],
+                       bias_bits=None if bb is None else bb[cols], scale_dtype=scale_dtype)
+    check_bf16_output(yb[:, cols], r, f"w4a16 M={M} N={N} K={K} g={group}")
+    return yb
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 8])
+@pytest.mark.parametrize("group", [32, 64, 128, -1])
+def test_w4a16_small(M, group):
+    _case(M, 200, 256, group, seed=M)
+
+
+@pytest.mark.parametrize("scale_dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("zeros", [False, True])
+@pytest.mark.parametrize("bias", [False, True])
+def test_w4a16_variants(scale_dtype, zeros, bias):
+    _case(4, 328, 1024, 128, scale_dtype=scale_dtype, zeros=zeros, bias=bias, seed=11)
+
+
+@pytest.mark.parametrize("M", [9, 17, 40])
+def test_w4a16_more_than_8_tokens(M):
+    _case(M, 136, 512, 64, zeros=True, bias=True, seed=M)
+
+
+@pytest.mark.parametrize("M", [1, 4, 8])
+@pytest.mark.parametrize("zeros", [False, True])
+def test_w4a16_full_size_decode(M, zeros):
+    """K=4096, N=14336, group 128 (the decode GEMV), sampled output columns."""
+    cols = np.sort(np.random.default_rng(M).choice(14336, 700, replace=False))
+    cols = np.concatenate([cols, np.arange(14336 - 64, 14336)])
+    _case(M, 14336, 4096, 128, zeros=zeros, seed=100 + M, cols=cols)
+
+
+def test_w4a16_bf16_scales_full_size():
+    cols = np.arange(0, 14336, 37)
+    _case(1, 14336, 4096, 128, scale_dtype="bf16", seed=7, cols=cols)
+
+
+def test_w4a16_codes8_closed_form():
+    """All codes 8 and zeros z: y = sum_g z[g,n] * sum_{k in g} x + bias."""
+    M, N, K, g = 3, 64, 256, 64
+    xb = S.activations_bf16(M, K, seed=5)
+    qw = np.full((K // 8, N), 0x88888888, dtype=np.uint32).view(np.int32)
+    sw = S.scales_f16((K // g, N))
+    zb = S.zeros_bf16((K // g, N))
+    bb = S.bias_bf16(N)
+    y = w4.w4a16_gemm(bf16(xb), to_dev(qw), to_dev(sw), g, zeros=bf16(zb), bias=bf16(bb))
+    xs = O.bf16_to_f64(xb).reshape(M, K // g, g).sum(axis=2)
+    want = (xs @ O.bf16_to_f64(zb) + O.bf16_to_f64(bb)).astype(np.float32)
+    check_bf16_output(bits(y), want, "codes 8")
+
+
+def test_w4a16_shares_weights_with_w4a8_layout():
+    """The same qweight buffer is a valid input to both paths (bit-identical layout)."""
+    K, N = 256, 64
+    qw = to_dev(S.random_words((K // 8, N), seed=9))
+    before = qw.clone()
+    w4.w4a16_gemm(bf16(S.activations_bf16(1, K)), qw, to_dev(S.scales_f16((2, N))), 128)
+    torch.cuda.synchronize()
+    assert torch.equal(qw, before)
+
+
+def test_w4a16_output_guard():
+    """Writes stay inside y: a sentinel band around the output is untouched."""
+    M, N, K = 3, 72, 256
+    buf = torch.full((M * N + 256,), -7.0, dtype=torch.bfloat16, device="cuda")
+    y = buf[128:128 + M * N].view(M, N)
+    xb = S.activations_bf16(M, K)
+    w4.w4a16_gemm(bf16(xb), to_dev(S.random_words((K // 8, N))), to_dev(S.scales_f16((2, N))), 128, y=y)
+    torch.cuda.synchronize()
+    assert torch.all(buf[:128] == -7.0) and torch.all(buf[128 + M * N:] == -7.0)
