@@ -57,7 +57,8 @@ typedef enum {
   W4_ERR_UNSUPPORTED = 5, /* valid per the layer's rules but outside what the kernels tile */
   W4_ERR_SHAPE = 6,       /* negative or inconsistent sizes */
   W4_ERR_CUDA = 7,        /* a CUDA runtime call failed (message in w4_last_error) */
-  W4_ERR_TIMEOUT = 8      /* a bounded wait inside a kernel ran out */
+  W4_ERR_TIMEOUT = 8,     /* a bounded wait inside a kernel ran out */
+  W4_ERR_WORKSPACE = 9    /* workspace NULL, too small or misaligned */
 } w4_status;
 
 typedef enum {
@@ -66,6 +67,22 @@ typedef enum {
   W4_INT8 = 2,
   W4_FP8_E4M3 = 3
 } w4_dtype;
+
+/* Operations that take a workspace (see w4_workspace_bytes). */
+typedef enum {
+  W4_OP_W4A8 = 0,           /* w4a8_gemm and w4a8_group_partials */
+  W4_OP_W4AFP8_MOE = 1      /* w4afp8_moe_grouped_gemm (M = R, the row count) */
+} w4_op;
+
+/*
+ * Bytes of device workspace an operation needs for M activation rows of
+ * length K (N and group do not change it today but are part of the query).
+ * The tensor-core GEMMs first widen the 8-bit activations once into exact
+ * fp16 in this workspace, so that every output tile streams them with TMA
+ * instead of converting them again. The caller allocates it (16-byte
+ * aligned); its contents on entry do not matter and are overwritten.
+ */
+size_t w4_workspace_bytes(int32_t op, int64_t M, int64_t N, int64_t K, int32_t group);
 
 /*
  * Dynamic per-token symmetric activation quantization.
@@ -101,20 +118,24 @@ w4_status w4_quant_act_per_token(const void* x, int32_t x_dtype, int64_t M, int6
  * y[m,n] = bf16( x_scale[m] * sum_g w_scale[g,n] * P[m,g,n] + bias[n] ), with
  * P[m,g,n] = sum_{k in g} qx[m,k] * (q[k,n] - 8) formed exactly in integers
  * and the group scale applied in fp32. group: -1 or a multiple of 16 dividing
- * K (else UNSUPPORTED); K % 16 == 0.
+ * K (else UNSUPPORTED); K % 16 == 0. workspace: at least
+ * w4_workspace_bytes(W4_OP_W4A8, M, N, K, group) bytes (W4_ERR_WORKSPACE).
  */
 w4_status w4a8_gemm(const void* qx, const float* x_scale, const void* qweight,
                     const void* w_scale, int32_t w_scale_dtype, int32_t group,
-                    const void* bias, void* y, int64_t M, int64_t N, int64_t K, void* stream);
+                    const void* bias, void* y, int64_t M, int64_t N, int64_t K,
+                    void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * The integer group partials of w4a8_gemm, from the same tensor-core path:
  *   partials [M, G, N] int32, P[m,g,n] = sum_{k in g} qx[m,k] * (q[k,n] - 8).
- * Same argument rules as w4a8_gemm. Meant for verifying the integer core
- * (|P| <= 127 * 8 * group must stay below 2^24, so group <= 16512).
+ * Same argument rules as w4a8_gemm. Meant for verifying the integer core;
+ * group (or K for -1) must be at most 16384 so that |P| <= 127 * 8 * group
+ * stays below 2^24.
  */
 w4_status w4a8_group_partials(const void* qx, const void* qweight, int32_t group,
-                              int32_t* partials, int64_t M, int64_t N, int64_t K, void* stream);
+                              int32_t* partials, int64_t M, int64_t N, int64_t K,
+                              void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * W4A16 linear for decode: bf16 activations x the same GPTQ qweight
@@ -152,14 +173,16 @@ w4_status w4a16_gemm(const void* x, const void* qweight, const void* w_scale, in
  *   w_scale         [E, N, K/group] fp16 (w_scale_dtype W4_FP16)
  *   y               [R, N] bf16
  * y[r,n] = bf16( x_scale[r] * sum_g w_scale[e,n,g] * sum_{k in g} x[r,k] (q[e,n,k]-8) )
- * with e the expert owning row r. group: a multiple of 16 dividing K, or -1.
- * Offsets are not validated on the host (they live on the device); rows outside
- * [0, R) are never written.
+ * with e the expert owning row r. group: a multiple of 16 dividing K, or -1;
+ * K % 32 == 0. workspace: at least w4_workspace_bytes(W4_OP_W4AFP8_MOE, R, N, K,
+ * group) bytes. Offsets are not validated on the host (they live on the device);
+ * rows outside [0, R) are never written.
  */
 w4_status w4afp8_moe_grouped_gemm(const void* qx, const float* x_scale, const int32_t* expert_offsets,
                                   int32_t E, const void* qweight, const void* w_scale,
                                   int32_t w_scale_dtype, int32_t group, void* y,
-                                  int64_t R, int64_t N, int64_t K, void* stream);
+                                  int64_t R, int64_t N, int64_t K,
+                                  void* workspace, size_t workspace_bytes, void* stream);
 
 /* Message for the last non-OK status returned to the calling thread ("" if none). */
 const char* w4_last_error(void);

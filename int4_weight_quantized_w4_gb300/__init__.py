@@ -19,25 +19,27 @@ __all__ = [
     "w4_quant_act_per_token", "w4a8_gemm", "w4a8_group_partials", "w4a16_gemm",
     "w4afp8_moe_grouped_gemm", "w4_device_status", "w4_selftest_bounded_wait",
     "W4_OK", "W4_ERR_NULL", "W4_ERR_ALIGN", "W4_ERR_GROUP", "W4_ERR_DTYPE",
-    "W4_ERR_UNSUPPORTED", "W4_ERR_SHAPE", "W4_ERR_CUDA", "W4_ERR_TIMEOUT",
-    "EXPORTED_SYMBOLS",
+    "W4_ERR_UNSUPPORTED", "W4_ERR_SHAPE", "W4_ERR_CUDA", "W4_ERR_TIMEOUT", "W4_ERR_WORKSPACE",
+    "W4_OP_W4A8", "W4_OP_W4AFP8_MOE", "w4_workspace_bytes", "EXPORTED_SYMBOLS",
 ]
 
 (W4_OK, W4_ERR_NULL, W4_ERR_ALIGN, W4_ERR_GROUP, W4_ERR_DTYPE, W4_ERR_UNSUPPORTED,
- W4_ERR_SHAPE, W4_ERR_CUDA, W4_ERR_TIMEOUT) = range(9)
+ W4_ERR_SHAPE, W4_ERR_CUDA, W4_ERR_TIMEOUT, W4_ERR_WORKSPACE) = range(10)
 W4_BF16, W4_FP16, W4_INT8, W4_FP8_E4M3 = range(4)
+W4_OP_W4A8, W4_OP_W4AFP8_MOE = range(2)
 
 _DIR = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_DIR, "libw4.so")
 
-_P, _I32, _I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+_P, _I32, _I64, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
 # name -> (restype, argtypes); mirrors include/w4.h
 _SIGNATURES = {
     "w4_quant_act_per_token": (_I32, [_P, _I32, _I64, _I64, _I32, _P, _P, _P]),
-    "w4a8_gemm": (_I32, [_P, _P, _P, _P, _I32, _I32, _P, _P, _I64, _I64, _I64, _P]),
-    "w4a8_group_partials": (_I32, [_P, _P, _I32, _P, _I64, _I64, _I64, _P]),
+    "w4_workspace_bytes": (_SZ, [_I32, _I64, _I64, _I64, _I32]),
+    "w4a8_gemm": (_I32, [_P, _P, _P, _P, _I32, _I32, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
+    "w4a8_group_partials": (_I32, [_P, _P, _I32, _P, _I64, _I64, _I64, _P, _SZ, _P]),
     "w4a16_gemm": (_I32, [_P, _P, _P, _I32, _P, _I32, _P, _P, _I64, _I64, _I64, _P]),
-    "w4afp8_moe_grouped_gemm": (_I32, [_P, _P, _P, _I32, _P, _P, _I32, _I32, _P, _I64, _I64, _I64, _P]),
+    "w4afp8_moe_grouped_gemm": (_I32, [_P, _P, _P, _I32, _P, _P, _I32, _I32, _P, _I64, _I64, _I64, _P, _SZ, _P]),
     "w4_last_error": (ctypes.c_char_p, []),
     "w4_status_string": (ctypes.c_char_p, [_I32]),
     "w4_device_status": (_I32, [_P]),
@@ -97,6 +99,18 @@ def _scale_dtype(t):
     return {torch.float16: W4_FP16, torch.bfloat16: W4_BF16}.get(t.dtype, -1)
 
 
+def w4_workspace_bytes(op: int, M: int, N: int, K: int, group: int) -> int:
+    """Device workspace in bytes that ``op`` (W4_OP_W4A8 / W4_OP_W4AFP8_MOE) needs."""
+    return int(load().w4_workspace_bytes(op, M, N, K, group))
+
+
+def _workspace(ws, op, M, N, K, group, device):
+    need = w4_workspace_bytes(op, M, N, K, group)
+    if ws is None:
+        ws = torch.empty((max(need, 16),), dtype=torch.uint8, device=device)
+    return ws, ws.numel() * ws.element_size()
+
+
 def w4_quant_act_per_token(x, q_dtype: str = "int8", q=None, scale=None, stream=None):
     """Per-token symmetric quantization of bf16 ``x [M, K]``; returns ``(q, scale)``
     with q int8 (``q_dtype="int8"``) or float8_e4m3fn (``"fp8"``) and fp32 scales."""
@@ -117,9 +131,10 @@ def w4_quant_act_per_token(x, q_dtype: str = "int8", q=None, scale=None, stream=
     return q, scale
 
 
-def w4a8_gemm(qx, x_scale, qweight, w_scale, group: int, bias=None, y=None, stream=None):
+def w4a8_gemm(qx, x_scale, qweight, w_scale, group: int, bias=None, y=None, workspace=None, stream=None):
     """W4A8 linear: int8 ``qx [M, K]`` with fp32 ``x_scale [M]`` times GPTQ
-    ``qweight [K/8, N]`` with fp16 ``w_scale [G, N]``; returns bf16 ``y [M, N]``."""
+    ``qweight [K/8, N]`` with fp16 ``w_scale [G, N]``; returns bf16 ``y [M, N]``.
+    ``workspace`` (bytes from ``w4_workspace_bytes``) is allocated if not given."""
     _cuda2d(qx, "qx", (torch.int8,))
     _cuda2d(qweight, "qweight", (torch.int32,))
     M, K = qx.shape
@@ -127,12 +142,14 @@ def w4a8_gemm(qx, x_scale, qweight, w_scale, group: int, bias=None, y=None, stre
     if qweight.shape[0] * 8 != K or x_scale.shape != (M,) or w_scale.dim() != 2 or w_scale.shape[1] != N:
         raise ValueError("inconsistent shapes for w4a8_gemm")
     y = torch.empty((M, N), dtype=torch.bfloat16, device=qx.device) if y is None else y
+    ws, wsb = _workspace(workspace, W4_OP_W4A8, M, N, K, group, qx.device)
     _check(load().w4a8_gemm(_ptr(qx), _ptr(x_scale), _ptr(qweight), _ptr(w_scale), _scale_dtype(w_scale),
-                            group, _ptr(bias), _ptr(y), M, N, K, _stream(stream, qx.device)), "w4a8_gemm")
+                            group, _ptr(bias), _ptr(y), M, N, K, _ptr(ws), wsb, _stream(stream, qx.device)),
+           "w4a8_gemm")
     return y
 
 
-def w4a8_group_partials(qx, qweight, group: int, out=None, stream=None):
+def w4a8_group_partials(qx, qweight, group: int, out=None, workspace=None, stream=None):
     """Integer group partials ``P [M, G, N]`` (int32) of the W4A8 product."""
     _cuda2d(qx, "qx", (torch.int8,))
     _cuda2d(qweight, "qweight", (torch.int32,))
@@ -140,7 +157,8 @@ def w4a8_group_partials(qx, qweight, group: int, out=None, stream=None):
     N = qweight.shape[1]
     G = 1 if group == -1 else (K // group if group > 0 else 0)
     out = torch.empty((M, G, N), dtype=torch.int32, device=qx.device) if out is None else out
-    _check(load().w4a8_group_partials(_ptr(qx), _ptr(qweight), group, _ptr(out), M, N, K,
+    ws, wsb = _workspace(workspace, W4_OP_W4A8, M, N, K, group, qx.device)
+    _check(load().w4a8_group_partials(_ptr(qx), _ptr(qweight), group, _ptr(out), M, N, K, _ptr(ws), wsb,
                                       _stream(stream, qx.device)), "w4a8_group_partials")
     return out
 
@@ -160,7 +178,8 @@ def w4a16_gemm(x, qweight, w_scale, group: int, zeros=None, bias=None, y=None, s
     return y
 
 
-def w4afp8_moe_grouped_gemm(qx, x_scale, expert_offsets, qweight, w_scale, group: int, y=None, stream=None):
+def w4afp8_moe_grouped_gemm(qx, x_scale, expert_offsets, qweight, w_scale, group: int, y=None, workspace=None,
+                            stream=None):
     """Grouped expert linear: e4m3 ``qx [R, K]`` (rows grouped by expert, as
     float8_e4m3fn or uint8 codes), fp32 ``x_scale [R]``, int32 device
     ``expert_offsets [E+1]``, ``qweight [E, N, K/8]``, fp16 ``w_scale [E, N, G]``."""
@@ -173,9 +192,10 @@ def w4afp8_moe_grouped_gemm(qx, x_scale, expert_offsets, qweight, w_scale, group
             or w_scale.dim() != 3 or w_scale.shape[:2] != (E, N):
         raise ValueError("inconsistent shapes for w4afp8_moe_grouped_gemm")
     y = torch.empty((R, N), dtype=torch.bfloat16, device=qx.device) if y is None else y
+    ws, wsb = _workspace(workspace, W4_OP_W4AFP8_MOE, R, N, K, group, qx.device)
     _check(load().w4afp8_moe_grouped_gemm(_ptr(qx), _ptr(x_scale), _ptr(expert_offsets), E, _ptr(qweight),
                                           _ptr(w_scale), _scale_dtype(w_scale), group, _ptr(y), R, N, K,
-                                          _stream(stream, qx.device)), "w4afp8_moe_grouped_gemm")
+                                          _ptr(ws), wsb, _stream(stream, qx.device)), "w4afp8_moe_grouped_gemm")
     return y
 
 

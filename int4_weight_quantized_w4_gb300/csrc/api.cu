@@ -91,6 +91,7 @@ const char* w4_status_string(int32_t st) {
     case W4_ERR_SHAPE: return "W4_ERR_SHAPE";
     case W4_ERR_CUDA: return "W4_ERR_CUDA";
     case W4_ERR_TIMEOUT: return "W4_ERR_TIMEOUT";
+    case W4_ERR_WORKSPACE: return "W4_ERR_WORKSPACE";
     default: return "W4_ERR_UNKNOWN";
   }
 }
@@ -111,9 +112,25 @@ w4_status w4_quant_act_per_token(const void* x, int32_t x_dtype, int64_t M, int6
                    "w4_quant_act_per_token launch");
 }
 
+size_t w4_workspace_bytes(int32_t op, int64_t M, int64_t N, int64_t K, int32_t group) {
+  (void)N;
+  (void)group;
+  if (M <= 0 || K <= 0) return 0;
+  if (op == W4_OP_W4A8 || op == W4_OP_W4AFP8_MOE) return w4::w4a8_workspace_bytes(M, K);
+  return 0;
+}
+
+static w4_status check_workspace(void* ws, size_t bytes, int64_t rows, int64_t K) {
+  const size_t need = w4::w4a8_workspace_bytes(rows, K);
+  if (ws == nullptr || bytes < need || !aligned(ws, 16))
+    return fail(W4_ERR_WORKSPACE, "workspace must be 16-byte aligned and at least %zu bytes (got %zu)", need, bytes);
+  return W4_OK;
+}
+
 static w4_status w4a8_common(const void* qx, const float* x_scale, const void* qweight, const void* w_scale,
                              int32_t w_scale_dtype, int32_t group, const void* bias, void* out,
-                             int64_t M, int64_t N, int64_t K, bool partials, void* stream) {
+                             int64_t M, int64_t N, int64_t K, bool partials, void* workspace,
+                             size_t workspace_bytes, void* stream) {
   int32_t g = 0;
   w4_status st = check_dims_group(M, N, K, group, &g);
   if (st != W4_OK) return st;
@@ -122,7 +139,7 @@ static w4_status w4a8_common(const void* qx, const float* x_scale, const void* q
   if (K % 16 != 0 || g % 16 != 0)
     return fail(W4_ERR_UNSUPPORTED, "w4a8 tiles need K and the group to be multiples of 16 (K=%lld group=%d)",
                 (long long)K, g);
-  if (partials && g > 16512) return fail(W4_ERR_UNSUPPORTED, "partials need group <= 16512 to stay exact");
+  if (partials && g > 16384) return fail(W4_ERR_UNSUPPORTED, "partials need group <= 16384 to stay exact");
   if (M == 0) return ok();
   if (!qx || !qweight || !out || (!partials && (!x_scale || !w_scale)))
     return fail(W4_ERR_NULL, "required pointer is NULL");
@@ -130,22 +147,28 @@ static w4_status w4a8_common(const void* qx, const float* x_scale, const void* q
       (!partials && (!aligned(w_scale, 8) || !aligned(x_scale, 4))) || (bias && !aligned(bias, 8)))
     return fail(W4_ERR_ALIGN, "matrices must be 16-byte aligned, vectors 8-byte aligned");
   if (M > INT32_MAX || N > INT32_MAX) return fail(W4_ERR_UNSUPPORTED, "M or N too large");
+  st = check_workspace(workspace, workspace_bytes, M, K);
+  if (st != W4_OK) return st;
   unsigned int* status = nullptr;
   cudaError_t e = status_ptr(&status);
   if (e != cudaSuccess) return from_cuda(e, "device status word");
-  w4::W4A8Args a{qx, x_scale, qweight, w_scale, partials ? nullptr : bias, out, nullptr, 1, M, N, K, g, partials, status};
+  w4::W4A8Args a{qx, x_scale, qweight, w_scale, partials ? nullptr : bias, out, nullptr, 1, M, N, K, g, partials,
+                 status, workspace};
   return from_cuda(w4::launch_w4a8_dense(a, static_cast<cudaStream_t>(stream)), "w4a8 launch");
 }
 
 w4_status w4a8_gemm(const void* qx, const float* x_scale, const void* qweight, const void* w_scale,
                     int32_t w_scale_dtype, int32_t group, const void* bias, void* y,
-                    int64_t M, int64_t N, int64_t K, void* stream) {
-  return w4a8_common(qx, x_scale, qweight, w_scale, w_scale_dtype, group, bias, y, M, N, K, false, stream);
+                    int64_t M, int64_t N, int64_t K, void* workspace, size_t workspace_bytes, void* stream) {
+  return w4a8_common(qx, x_scale, qweight, w_scale, w_scale_dtype, group, bias, y, M, N, K, false, workspace,
+                     workspace_bytes, stream);
 }
 
 w4_status w4a8_group_partials(const void* qx, const void* qweight, int32_t group, int32_t* partials,
-                              int64_t M, int64_t N, int64_t K, void* stream) {
-  return w4a8_common(qx, nullptr, qweight, nullptr, W4_FP16, group, nullptr, partials, M, N, K, true, stream);
+                              int64_t M, int64_t N, int64_t K, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  return w4a8_common(qx, nullptr, qweight, nullptr, W4_FP16, group, nullptr, partials, M, N, K, true, workspace,
+                     workspace_bytes, stream);
 }
 
 w4_status w4a16_gemm(const void* x, const void* qweight, const void* w_scale, int32_t w_scale_dtype,
@@ -171,15 +194,17 @@ w4_status w4a16_gemm(const void* x, const void* qweight, const void* w_scale, in
 
 w4_status w4afp8_moe_grouped_gemm(const void* qx, const float* x_scale, const int32_t* expert_offsets, int32_t E,
                                   const void* qweight, const void* w_scale, int32_t w_scale_dtype, int32_t group,
-                                  void* y, int64_t R, int64_t N, int64_t K, void* stream) {
+                                  void* y, int64_t R, int64_t N, int64_t K, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
   int32_t g = 0;
   w4_status st = check_dims_group(R, N, K, group, &g);
   if (st != W4_OK) return st;
   if (E <= 0) return fail(W4_ERR_SHAPE, "E must be positive, got %d", E);
   if (w_scale_dtype != W4_FP16) return fail(W4_ERR_DTYPE, "expert weight scales must be fp16 (W4_FP16)");
-  if (K % 16 != 0 || g % 16 != 0)
-    return fail(W4_ERR_UNSUPPORTED, "expert tiles need K and the group to be multiples of 16 (K=%lld group=%d)",
+  if (K % 32 != 0 || g % 16 != 0)
+    return fail(W4_ERR_UNSUPPORTED, "expert tiles need K % 32 == 0 and the group a multiple of 16 (K=%lld group=%d)",
                 (long long)K, g);
+  if ((R + 127) / 128 + E > 65535) return fail(W4_ERR_UNSUPPORTED, "too many row tiles plus experts");
   if (R == 0) return ok();
   if (!qx || !x_scale || !expert_offsets || !qweight || !w_scale || !y)
     return fail(W4_ERR_NULL, "required pointer is NULL");
@@ -187,10 +212,12 @@ w4_status w4afp8_moe_grouped_gemm(const void* qx, const float* x_scale, const in
       !aligned(x_scale, 4) || !aligned(expert_offsets, 4))
     return fail(W4_ERR_ALIGN, "matrices must be 16-byte aligned, vectors aligned to their element size");
   if (R > INT32_MAX || N > INT32_MAX) return fail(W4_ERR_UNSUPPORTED, "R or N too large");
+  st = check_workspace(workspace, workspace_bytes, R, K);
+  if (st != W4_OK) return st;
   unsigned int* status = nullptr;
   cudaError_t e = status_ptr(&status);
   if (e != cudaSuccess) return from_cuda(e, "device status word");
-  w4::W4A8Args a{qx, x_scale, qweight, w_scale, nullptr, y, expert_offsets, E, R, N, K, g, false, status};
+  w4::W4A8Args a{qx, x_scale, qweight, w_scale, nullptr, y, expert_offsets, E, R, N, K, g, false, status, workspace};
   return from_cuda(w4::launch_w4afp8_experts(a, static_cast<cudaStream_t>(stream)), "w4afp8 experts launch");
 }
 

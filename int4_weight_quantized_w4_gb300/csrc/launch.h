@@ -40,7 +40,9 @@ struct W4A8Args {
   int32_t group;          // effective group
   bool partials;          // write int32 group partials instead of y
   unsigned int* status;
+  void* workspace;        // fp16 [rows, K]: the activations widened once per call
 };
+size_t w4a8_workspace_bytes(int64_t rows, int64_t K);
 cudaError_t launch_w4a8_dense(const W4A8Args& a, cudaStream_t s);
 cudaError_t launch_w4afp8_experts(const W4A8Args& a, cudaStream_t s);
 

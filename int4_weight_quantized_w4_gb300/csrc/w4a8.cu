@@ -1,7 +1,488 @@
-// placeholder until the tensor-core kernels land
+// W4A8 and W4AFP8 GEMMs on the 5th-generation tensor cores (tcgen05, sm_103a).
+//
+// vLLM API docs, inc.schemes.inc_w4a8_linear, INCXPUW4A8LinearMethod
+// (class docstring, apply_weights): int8 per-token activations times the GPTQ
+// int4 weight [K/8, N] with fp16 group scales, keeping the GEMM on an 8-bit
+// datapath for compute-bound token counts. vLLM API docs, quantization.w4afp8,
+// W4AFP8Config: int4 group-128 routed experts with fp8 per-token activations,
+// weights in the compressed-tensors layout [E, N, K/8].
+//
+// sm_103a has no integer tensor-core MMA, so the integer products run exactly
+// on the fp16 path: every int8 activation and every weight value q - 8 is an
+// exact fp16, every product is exact in fp32, and a group's partial sum
+// (|P| <= 127 * 8 * 16384 < 2^24) is an integer the fp32 accumulator holds
+// exactly. e4m3 activations are exact in fp16 too.
+//
+// Per output tile of 128 outputs (n) x 128 tokens:
+//  * swap-AB: the weights are the MMA's M operand (TMEM lane = output n),
+//    the tokens its N operand, so the per-group scale s[g, n] is one register
+//    per epilogue thread;
+//  * TMA streams the raw packed weight words into a ring in shared memory;
+//    converter warps turn each 32-bit word (8 nibbles) into 8 exact fp16
+//    values q - 8 with LOP3 + HSUB2/HFMA2 (the fp16 mantissa of 1024 + q) and
+//    write them into the 128-byte-swizzled K-major operand tile;
+//  * the activations were widened once per call to exact fp16 (see
+//    widen_kernel) and TMA loads them straight into the swizzled layout;
+//  * one thread issues tcgen05.mma (M=128, N=128, K=16) into a TMEM
+//    accumulator per group; the accumulator is double-buffered so the
+//    epilogue folds group g (T += s[g,n] * P) while group g+1 accumulates;
+//  * the epilogue finally writes y = bf16(s_x[m] * T + bias[n]).
+// Within every 8-wide chunk of k both operands use the order
+// (k0,k4,k1,k5,k2,k6,k3,k7), the order the nibble pairs come out in.
+#include <cuda.h>
+
 #include "common.cuh"
 #include "launch.h"
+#include "tc.cuh"
+
 namespace w4 {
-cudaError_t launch_w4a8_dense(const W4A8Args&, cudaStream_t) { return cudaErrorNotSupported; }
-cudaError_t launch_w4afp8_experts(const W4A8Args&, cudaStream_t) { return cudaErrorNotSupported; }
+namespace {
+
+constexpr int BM = 128;          // outputs per tile (MMA M, TMEM lanes)
+constexpr int BN = 128;          // tokens per tile (MMA N)
+constexpr int BK = 64;           // k per stage (one 128-byte fp16 swizzle row)
+constexpr int UMMA_K = 16;
+constexpr int OP_STAGES = 4;
+constexpr int RAW_STAGES = 8;
+constexpr int SEG_MAX = 16384;   // longest accumulation before a drain (exactness bound)
+
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int OP_BYTES = A_BYTES + B_BYTES;
+constexpr int RAW_BYTES = BM * BK / 2;
+
+constexpr int kEpiWarps = 4;
+constexpr int kConvWarps = 4;
+constexpr int kWarpConv0 = 4;
+constexpr int kWarpLoadW = 8;
+constexpr int kWarpLoadB = 9;
+constexpr int kWarpMma = 10;
+constexpr int kThreads = 11 * 32;
+constexpr uint32_t kTmemCols = 2 * BN;
+constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait
+
+constexpr int kSmemBytes = OP_STAGES * OP_BYTES + RAW_STAGES * RAW_BYTES + 1024 /*bars etc*/ + 1024 /*align*/;
+
+enum Mode : int { kDenseY = 0, kDensePartials = 1, kExperts = 2 };
+
+struct Params {
+  CUtensorMap tm_act;      // fp16 activations [rows, K], widened and permuted
+  CUtensorMap tm_w;        // raw weight words: GPTQ [K/8, N] or CT [E, N, K/8]
+  const uint16_t* w_scale; // fp16 [G, N] or [E, N, G]
+  const float* x_scale;    // [rows]
+  const uint16_t* bias;    // bf16 [N] or null
+  void* out;               // bf16 [rows, N] or int32 [rows, G, N]
+  const int32_t* offsets;  // [E + 1] (experts)
+  int E, M, N, K, group, mode;
+  unsigned int* status;
+};
+
+// 8 nibbles (k0..k7 of one output) -> 8 exact fp16 values q - 8 in the order
+// (k0,k4,k1,k5,k2,k6,k3,k7). 0x6400 | q is 1024 + q; 0x6400 | q << 4 is
+// 1024 + 16 q, which one fp16 FMA maps to q - 8 exactly.
+W4_DEV uint4 nibbles_to_f16(uint32_t w) {
+  const uint32_t w8 = w >> 8;
+  uint4 o;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(o.x) : "r"(and_or(w, 0x000F000Fu, 0x64006400u)), "r"(0x64086408u));
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(o.y) : "r"(and_or(w, 0x00F000F0u, 0x64006400u)), "r"(0x2C002C00u),
+      "r"(0xD480D480u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(o.z) : "r"(and_or(w8, 0x000F000Fu, 0x64006400u)), "r"(0x64086408u));
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(o.w) : "r"(and_or(w8, 0x00F000F0u, 0x64006400u)), "r"(0x2C002C00u),
+      "r"(0xD480D480u));
+  return o;
+}
+
+W4_DEV void bar_sync_epilogue() { asm volatile("bar.sync 1, %0;" :: "n"(kEpiWarps * 32) : "memory"); }
+
+__global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_constant__ Params p) {
+  extern __shared__ uint8_t smem_dyn[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+
+  // ---- which tile ----
+  const int n0 = blockIdx.x * BM;
+  int row0 = 0, row_end = 0, expert = 0;
+  if (p.mode == kExperts) {
+    int t = blockIdx.y;
+    for (int e = 0; e < p.E; ++e) {
+      const int a = p.offsets[e], b = p.offsets[e + 1];
+      const int nt = b > a ? (b - a + BN - 1) / BN : 0;
+      if (t < nt) {
+        expert = e;
+        row0 = a + t * BN;
+        row_end = min(row0 + BN, b);
+        break;
+      }
+      t -= nt;
+    }
+    row0 = max(row0, 0);
+    row_end = min(row_end, p.M);
+  } else {
+    row0 = blockIdx.y * BN;
+    row_end = min(row0 + BN, p.M);
+  }
+  if (row0 >= row_end) return;  // no tile for this CTA (uniform across the CTA)
+
+  uint8_t* op_base = smem;
+  uint8_t* raw_base = smem + OP_STAGES * OP_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(raw_base + RAW_STAGES * RAW_BYTES);
+  uint64_t* raw_full = bars;
+  uint64_t* raw_empty = raw_full + RAW_STAGES;
+  uint64_t* op_full = raw_empty + RAW_STAGES;
+  uint64_t* op_empty = op_full + OP_STAGES;
+  uint64_t* acc_full = op_empty + OP_STAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  float* xs_s = reinterpret_cast<float*>(tmem_holder + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < RAW_STAGES; ++i) {
+      mbar_init(&raw_full[i], 1);
+      mbar_init(&raw_empty[i], kConvWarps);
+    }
+    for (int i = 0; i < OP_STAGES; ++i) {
+      mbar_init(&op_full[i], 1 + kConvWarps);
+      mbar_init(&op_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], kEpiWarps);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) tc::tmem_alloc(tmem_holder, kTmemCols);
+  if (warp == kWarpLoadW && lane == 0) {
+    tc::prefetch_tmap(&p.tm_w);
+    tc::prefetch_tmap(&p.tm_act);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_holder;
+
+  const int K = p.K;
+  const int nst = (K + BK - 1) / BK;
+  const int group = p.group;
+
+  if (warp == kWarpLoadW) {
+    // ---- raw packed weight words -> ring ----
+    if (lane == 0) {
+      for (int s = 0; s < nst; ++s) {
+        const int r = s % RAW_STAGES;
+        if (!tc::wait(&raw_empty[r], ((s / RAW_STAGES) & 1) ^ 1, abort_flag, p.status, kWaitNs)) break;
+        mbar_arrive_expect_tx(&raw_full[r], RAW_BYTES);
+        if (p.mode == kExperts)
+          tc::tma_load_3d(raw_base + r * RAW_BYTES, &p.tm_w, &raw_full[r], s * (BK / 8), n0, expert);
+        else
+          tc::tma_load_2d(raw_base + r * RAW_BYTES, &p.tm_w, &raw_full[r], n0, s * (BK / 8));
+      }
+    }
+  } else if (warp == kWarpLoadB) {
+    // ---- widened activations -> operand B of each stage ----
+    if (lane == 0) {
+      for (int s = 0; s < nst; ++s) {
+        const int o = s % OP_STAGES;
+        if (!tc::wait(&op_empty[o], ((s / OP_STAGES) & 1) ^ 1, abort_flag, p.status, kWaitNs)) break;
+        mbar_arrive_expect_tx(&op_full[o], B_BYTES);
+        tc::tma_load_2d(op_base + o * OP_BYTES + A_BYTES, &p.tm_act, &op_full[o], s * BK, row0);
+      }
+    }
+  } else if (warp >= kWarpConv0 && warp < kWarpConv0 + kConvWarps) {
+    // ---- nibbles -> fp16 operand A ----
+    const int t = threadIdx.x - kWarpConv0 * 32;  // output row within the tile
+    for (int s = 0; s < nst; ++s) {
+      const int r = s % RAW_STAGES, o = s % OP_STAGES;
+      if (!tc::wait(&raw_full[r], (s / RAW_STAGES) & 1, abort_flag, p.status, kWaitNs)) break;
+      if (!tc::wait(&op_empty[o], ((s / OP_STAGES) & 1) ^ 1, abort_flag, p.status, kWaitNs)) break;
+      const uint32_t* raw = reinterpret_cast<const uint32_t*>(raw_base + r * RAW_BYTES);
+      uint32_t w[8];
+      if (p.mode == kExperts) {  // box [128 outputs][8 words]
+        const uint4 lo = *reinterpret_cast<const uint4*>(raw + t * 8);
+        const uint4 hi = *reinterpret_cast<const uint4*>(raw + t * 8 + 4);
+        w[0] = lo.x; w[1] = lo.y; w[2] = lo.z; w[3] = lo.w;
+        w[4] = hi.x; w[5] = hi.y; w[6] = hi.z; w[7] = hi.w;
+      } else {  // box [8 words][128 outputs]
+#pragma unroll
+        for (int kb = 0; kb < 8; ++kb) w[kb] = raw[kb * BM + t];
+      }
+      uint8_t* arow = op_base + o * OP_BYTES + t * 128;
+#pragma unroll
+      for (int kb = 0; kb < 8; ++kb)
+        *reinterpret_cast<uint4*>(arow + ((kb ^ (t & 7)) << 4)) = nibbles_to_f16(w[kb]);
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&op_full[o]);
+        mbar_arrive(&raw_empty[r]);
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // ---- one thread issues the MMAs ----
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::idesc_f16_f32(BM, BN);
+      const uint32_t op0 = smem_addr(op_base);
+      bool ok = true;
+      int seg = 0;
+      for (int k0 = 0; k0 < K && ok; ++seg) {
+        const int g = k0 / group;
+        const int kend = min(min((g + 1) * group, k0 + SEG_MAX), K);
+        const int buf = seg & 1;
+        if (!tc::wait(&acc_empty[buf], ((seg >> 1) & 1) ^ 1, abort_flag, p.status, kWaitNs)) break;
+        tc::fence_after_sync();
+        const uint32_t d = tmem + buf * BN;
+        for (int k = k0; k < kend; k += UMMA_K) {
+          const int s = k / BK, o = s % OP_STAGES;
+          if (k % BK == 0) {
+            if (!tc::wait(&op_full[o], (s / OP_STAGES) & 1, abort_flag, p.status, kWaitNs)) {
+              ok = false;
+              break;
+            }
+            tc::fence_after_sync();
+          }
+          const uint32_t a_addr = op0 + o * OP_BYTES + (k % BK) * 2;
+          tc::mma_f16(d, tc::sdesc_sw128(a_addr), tc::sdesc_sw128(a_addr + A_BYTES), idesc, k > k0 ? 1u : 0u);
+          if ((k + UMMA_K) % BK == 0 || k + UMMA_K >= K) tc::commit(&op_empty[o]);
+        }
+        if (!ok) break;
+        tc::commit(&acc_full[buf]);
+        k0 = kend;
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---- epilogue: warp e owns TMEM lanes 32e..32e+31 (outputs) ----
+    const int e = warp;
+    const int n = n0 + 32 * e + lane;
+    const bool n_ok = n < p.N;
+    const int N = p.N;
+    const int G = K / group;
+    const bool partials = p.mode == kDensePartials;
+    if (!partials)
+      for (int j = threadIdx.x; j < BN; j += kEpiWarps * 32)
+        xs_s[j] = (row0 + j < row_end) ? p.x_scale[row0 + j] : 0.f;
+    bar_sync_epilogue();
+
+    float T[BN];
+#pragma unroll
+    for (int j = 0; j < BN; ++j) T[j] = 0.f;
+
+    int seg = 0;
+    for (int k0 = 0; k0 < K; ++seg) {
+      const int g = k0 / group;
+      const int kend = min(min((g + 1) * group, k0 + SEG_MAX), K);
+      const int buf = seg & 1;
+      if (!tc::wait(&acc_full[buf], (seg >> 1) & 1, abort_flag, p.status, kWaitNs)) break;
+      tc::fence_after_sync();
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * e) << 16) + buf * BN;
+      if (partials) {
+        int32_t* out = static_cast<int32_t*>(p.out);
+#pragma unroll
+        for (int cc = 0; cc < BN / 32; ++cc) {
+          uint32_t v[32];
+          tc::tmem_ld32(taddr + cc * 32, v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int row = row0 + cc * 32 + j;
+            if (n_ok && row < row_end)
+              out[((size_t)row * G + g) * N + n] = __float2int_rn(__uint_as_float(v[j]));
+          }
+        }
+      } else {
+        float s = 0.f;
+        if (n_ok) {
+          const size_t si = (p.mode == kExperts) ? ((size_t)expert * N + n) * G + g : (size_t)g * N + n;
+          s = half_bits_to_f32(p.w_scale[si]);
+        }
+#pragma unroll
+        for (int cc = 0; cc < BN / 32; ++cc) {
+          uint32_t v[32];
+          tc::tmem_ld32(taddr + cc * 32, v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) T[cc * 32 + j] = fmaf(s, __uint_as_float(v[j]), T[cc * 32 + j]);
+        }
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+      k0 = kend;
+    }
+
+    if (!partials && !*abort_flag) {
+      const float b = (p.bias != nullptr && n_ok) ? __uint_as_float(static_cast<uint32_t>(p.bias[n]) << 16) : 0.f;
+      uint16_t* y = static_cast<uint16_t*>(p.out);
+#pragma unroll
+      for (int j = 0; j < BN; ++j) {
+        const int row = row0 + j;
+        if (n_ok && row < row_end) y[(size_t)row * N + n] = static_cast<uint16_t>(f32_to_bf16_bits(fmaf(xs_s[j], T[j], b)));
+      }
+    }
+  }
+
+  // ---- teardown: every warp arrives here; waits above are bounded ----
+  if (*abort_flag) {
+    // let copies and MMAs already issued land before the shared memory goes away
+    const uint64_t t0 = tc::globaltimer_ns();
+    while (tc::globaltimer_ns() - t0 < 1000000ull) {
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// widening pass: 8-bit activations -> exact fp16, k permuted per 8-chunk
+// ---------------------------------------------------------------------------
+
+// int8 bytes b0..b7 -> fp16 (b0,b4,b1,b5,b2,b6,b3,b7). (b ^ 0x80) in the low
+// mantissa byte of 1024 is 1152 + b; subtracting 1152 leaves b exactly.
+W4_DEV uint32_t i8pair(uint32_t u0, uint32_t u1, uint32_t sel) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(and_xor(prmt(u0, u1, sel), 0x00FF00FFu, 0x64806480u)),
+      "r"(0x64806480u));
+  return d;
+}
+
+W4_DEV uint4 widen_i8(uint32_t u0, uint32_t u1) {
+  return make_uint4(i8pair(u0, u1, 0x0400u), i8pair(u0, u1, 0x0501u), i8pair(u0, u1, 0x0602u),
+                    i8pair(u0, u1, 0x0703u));
+}
+
+W4_DEV uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+  uint32_t d;
+  asm("{.reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t;}" : "=r"(d) : "r"(two_codes));
+  return d;
+}
+
+// e4m3 codes b0..b7 -> fp16 (b0,b4,b1,b5,b2,b6,b3,b7), exactly.
+W4_DEV uint4 widen_e4m3(uint32_t u0, uint32_t u1) {
+  const uint32_t a = prmt(u0, u1, 0x5140u), b = prmt(u0, u1, 0x7362u);
+  return make_uint4(e4m3x2_to_f16x2(a & 0xFFFFu), e4m3x2_to_f16x2(a >> 16), e4m3x2_to_f16x2(b & 0xFFFFu),
+                    e4m3x2_to_f16x2(b >> 16));
+}
+
+template <bool FP8>
+__global__ void __launch_bounds__(256) widen_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                    size_t n16) {
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) {
+    const uint4 v = ld_stream_v4(src + i);
+    dst[2 * i] = FP8 ? widen_e4m3(v.x, v.y) : widen_i8(v.x, v.y);
+    dst[2 * i + 1] = FP8 ? widen_e4m3(v.z, v.w) : widen_i8(v.z, v.w);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+cudaError_t get_encoder(EncodeTiled* fn) {
+  static EncodeTiled cached = nullptr;
+  if (cached == nullptr) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || f == nullptr) return cudaErrorNotSupported;
+    cached = reinterpret_cast<EncodeTiled>(f);
+  }
+  *fn = cached;
+  return cudaSuccess;
+}
+
+cudaError_t encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const cuuint64_t* dims,
+                   const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle sw) {
+  EncodeTiled fn = nullptr;
+  cudaError_t e = get_encoder(&fn);
+  if (e != cudaSuccess) return e;
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, dt, rank, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t widen(const void* src, void* dst, int64_t rows, int64_t K, bool fp8, cudaStream_t s) {
+  const size_t n16 = (size_t)rows * (size_t)K / 16;
+  if (n16 == 0) return cudaSuccess;
+  const size_t want = (n16 + 255) / 256;
+  const unsigned blocks = static_cast<unsigned>(want < 152 * 16 ? want : 152 * 16);
+  if (fp8)
+    widen_kernel<true><<<blocks, 256, 0, s>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst), n16);
+  else
+    widen_kernel<false><<<blocks, 256, 0, s>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst), n16);
+  return cudaGetLastError();
+}
+
+cudaError_t run(const W4A8Args& a, int mode, cudaStream_t s) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(w4a8_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const bool experts = mode == kExperts;
+  cudaError_t e = widen(a.act, a.workspace, a.M, a.K, experts, s);
+  if (e != cudaSuccess) return e;
+
+  Params p;
+  memset(&p, 0, sizeof(p));
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.M};
+    const cuuint64_t strides[1] = {(cuuint64_t)a.K * 2};
+    const cuuint32_t box[2] = {BK, BN};
+    e = encode(&p.tm_act, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.workspace, dims, strides, box,
+               CU_TENSOR_MAP_SWIZZLE_128B);
+    if (e != cudaSuccess) return e;
+  }
+  if (experts) {
+    const cuuint64_t dims[3] = {(cuuint64_t)a.K / 8, (cuuint64_t)a.N, (cuuint64_t)a.E};
+    const cuuint64_t strides[2] = {(cuuint64_t)a.K / 8 * 4, (cuuint64_t)a.N * (a.K / 8) * 4};
+    const cuuint32_t box[3] = {BK / 8, BM, 1};
+    e = encode(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_INT32, 3, a.qweight, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+  } else {
+    const cuuint64_t dims[2] = {(cuuint64_t)a.N, (cuuint64_t)a.K / 8};
+    const cuuint64_t strides[1] = {(cuuint64_t)a.N * 4};
+    const cuuint32_t box[2] = {BM, BK / 8};
+    e = encode(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, a.qweight, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+  }
+  if (e != cudaSuccess) return e;
+  p.w_scale = static_cast<const uint16_t*>(a.w_scale);
+  p.x_scale = a.x_scale;
+  p.bias = static_cast<const uint16_t*>(a.bias);
+  p.out = a.out;
+  p.offsets = a.expert_offsets;
+  p.E = a.E;
+  p.M = static_cast<int>(a.M);
+  p.N = static_cast<int>(a.N);
+  p.K = static_cast<int>(a.K);
+  p.group = a.group;
+  p.mode = mode;
+  p.status = a.status;
+
+  const unsigned gx = static_cast<unsigned>((a.N + BM - 1) / BM);
+  const long long gy = experts ? (a.M + BN - 1) / BN + a.E : (a.M + BN - 1) / BN;
+  if (gy > 65535) return cudaErrorInvalidConfiguration;
+  w4a8_tc_kernel<<<dim3(gx, static_cast<unsigned>(gy)), kThreads, kSmemBytes, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t w4a8_workspace_bytes(int64_t rows, int64_t K) { return static_cast<size_t>(rows) * static_cast<size_t>(K) * 2; }
+
+cudaError_t launch_w4a8_dense(const W4A8Args& a, cudaStream_t s) {
+  return run(a, a.partials ? kDensePartials : kDenseY, s);
+}
+
+cudaError_t launch_w4afp8_experts(const W4A8Args& a, cudaStream_t s) { return run(a, kExperts, s); }
+
 }  // namespace w4

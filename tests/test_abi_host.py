@@ -24,7 +24,7 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:w4_status|const char\*|void)\s+(w4\w*)\s*\(", text, flags=re.M)))
+    return sorted(set(re.findall(r"^\s*(?:w4_status|const char\*|void|size_t)\s+(w4\w*)\s*\(", text, flags=re.M)))
 
 
 def test_header_declares_the_entry_points():
@@ -49,10 +49,10 @@ def test_status_strings(lib):
 
 def gemm(lib, **kw):
     a = dict(qx=FAKE, sx=FAKE, qw=FAKE, ws=FAKE, wdt=w4.W4_FP16, group=128, bias=None, y=FAKE,
-             M=16, N=256, K=256)
+             M=16, N=256, K=256, work=None, work_bytes=0)
     a.update(kw)
     return lib.w4a8_gemm(a["qx"], a["sx"], a["qw"], a["ws"], a["wdt"], a["group"], a["bias"], a["y"],
-                         a["M"], a["N"], a["K"], None)
+                         a["M"], a["N"], a["K"], a["work"], a["work_bytes"], None)
 
 
 def test_w4a8_validation(lib):
@@ -70,11 +70,18 @@ def test_w4a8_validation(lib):
     assert gemm(lib, y=ODD) == w4.W4_ERR_ALIGN
     assert gemm(lib, M=0) == w4.W4_OK                             # empty: no-op, no launch
     assert lib.w4_last_error() == b""
+    # workspace: missing, too small, misaligned
+    need = lib.w4_workspace_bytes(w4.W4_OP_W4A8, 16, 256, 256, 128)
+    assert need == 16 * 256 * 2
+    assert gemm(lib) == w4.W4_ERR_WORKSPACE
+    assert gemm(lib, work=FAKE, work_bytes=need - 1) == w4.W4_ERR_WORKSPACE
+    assert gemm(lib, work=ODD, work_bytes=need) == w4.W4_ERR_WORKSPACE
 
 
 def test_w4a8_partials_validation(lib):
-    assert lib.w4a8_group_partials(FAKE, FAKE, 128, None, 16, 256, 256, None) == w4.W4_ERR_NULL
-    assert lib.w4a8_group_partials(FAKE, FAKE, 100, FAKE, 16, 256, 256, None) == w4.W4_ERR_GROUP
+    assert lib.w4a8_group_partials(FAKE, FAKE, 128, None, 16, 256, 256, FAKE, 1 << 20, None) == w4.W4_ERR_NULL
+    assert lib.w4a8_group_partials(FAKE, FAKE, 100, FAKE, 16, 256, 256, FAKE, 1 << 20, None) == w4.W4_ERR_GROUP
+    assert lib.w4a8_group_partials(FAKE, FAKE, -1, FAKE, 16, 256, 32768, FAKE, 1 << 30, None) == w4.W4_ERR_UNSUPPORTED
 
 
 def test_w4a16_validation(lib):
@@ -110,14 +117,17 @@ def test_quant_validation(lib):
 def test_moe_validation(lib):
     def call(**kw):
         a = dict(qx=FAKE, sx=FAKE, off=FAKE, E=64, qw=FAKE, ws=FAKE, wdt=w4.W4_FP16, group=128, y=FAKE,
-                 R=32, N=256, K=256)
+                 R=32, N=256, K=256, work=FAKE, work_bytes=1 << 20)
         a.update(kw)
         return lib.w4afp8_moe_grouped_gemm(a["qx"], a["sx"], a["off"], a["E"], a["qw"], a["ws"], a["wdt"],
-                                           a["group"], a["y"], a["R"], a["N"], a["K"], None)
+                                           a["group"], a["y"], a["R"], a["N"], a["K"], a["work"], a["work_bytes"],
+                                           None)
     assert call(E=0) == w4.W4_ERR_SHAPE
     assert call(wdt=w4.W4_BF16) == w4.W4_ERR_DTYPE
     assert call(off=None) == w4.W4_ERR_NULL
     assert call(group=24) == w4.W4_ERR_GROUP
+    assert call(K=272, group=16) == w4.W4_ERR_UNSUPPORTED        # K % 32 for the 3-D weight map
+    assert call(work=None) == w4.W4_ERR_WORKSPACE
     assert call(R=0) == w4.W4_OK
 
 
