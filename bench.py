@@ -251,8 +251,139 @@ def run_ours(args, rank, world, local_rank):
                 "how": "per step: pinned H2D of x, w4a16_gemm, D2H of y; host wall clock"},
         "gpu_launches": steps,
         "clocks": clk.summary(),
+        "sm_count": torch.cuda.get_device_properties(dev).multi_processor_count,
     }
+    if not args.no_rows:
+        line["rows"] = bench_rows(dev, stream, bf16_tf, peak_kind)
     return line
+
+
+# ---------------------------------------------------------------------------
+# the other rows of the hot path (same run, own timing)
+# ---------------------------------------------------------------------------
+
+def _time_graph(torch, stream, fn, calls, replays, warmup=3):
+    """Capture `calls` invocations of fn into a graph; return ms per invocation."""
+    with torch.cuda.stream(stream):
+        fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(calls):
+            fn()
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(replays):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / (calls * replays)
+
+
+def bench_rows(dev, stream, bf16_tf, peak_kind):
+    import torch
+    import int4_weight_quantized_w4_gb300 as w4
+
+    def bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    def on(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    rows = {}
+
+    def dense(name, M, N, K, group, outliers):
+        g = K if group == -1 else group
+        x = bf16(S.activations_bf16(M, K, seed=0, outlier_frac=outliers))
+        qw = on(S.random_words((K // 8, N), seed=1))
+        sw = on(S.scales_f16((K // g, N), seed=2))
+        q = torch.empty((M, K), dtype=torch.int8, device=dev)
+        s = torch.empty((M,), dtype=torch.float32, device=dev)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty((w4.w4_workspace_bytes(w4.W4_OP_W4A8, M, N, K, group),), dtype=torch.uint8, device=dev)
+
+        def step():
+            w4.w4_quant_act_per_token(x, "int8", q=q, scale=s, stream=stream)
+            w4.w4a8_gemm(q, s, qw, sw, group, y=y, workspace=ws, stream=stream)
+
+        def gemm():
+            w4.w4a8_gemm(q, s, qw, sw, group, y=y, workspace=ws, stream=stream)
+
+        def quant():
+            w4.w4_quant_act_per_token(x, "int8", q=q, scale=s, stream=stream)
+
+        t_step = _time_graph(torch, stream, step, 5, 10)
+        t_gemm = _time_graph(torch, stream, gemm, 5, 10)
+        t_quant = _time_graph(torch, stream, quant, 5, 10)
+        ops = 2.0 * M * N * K
+        tops_gemm = ops / (t_gemm * 1e-3) / 1e12
+        rows[name] = {
+            "config": {"M": M, "N": N, "K": K, "group": group, "outlier_channels": outliers},
+            "value": round(ops / (t_step * 1e-3) / 1e12, 1), "unit": "TOPS",
+            "ms_per_step": t_step, "step": "per-token int8 quantization + w4a8_gemm",
+            "gemm_ms": t_gemm, "gemm_tops": round(tops_gemm, 1),
+            "quant_ms": t_quant, "quant_gbs": round(3.0 * M * K / (t_quant * 1e-3) / 1e9, 1),
+            "roofline": {"bound": "tensor", "achieved": round(tops_gemm, 1), "peak": bf16_tf, "unit": "TFLOP/s",
+                         "frac": round(tops_gemm / bf16_tf, 4), "traffic": None,
+                         "peak_source": f"{peak_kind} bf16_tflops (the exact int8 x int4 products run on the "
+                                        "fp16 tensor datapath; sm_103a has no int8 tcgen05 MMA)",
+                         "kernel": "w4a8_gemm call = widen_kernel + w4a8_tc_kernel"},
+            "l2": "inputs + outputs per step larger than L2",
+        }
+
+    dense("w4a8_prefill", 4096, 11008, 4096, 128, 0.01)
+    dense("w4a8_diffusion", 16384, 3072, 3072, -1, 0.0)
+
+    # grouped experts: 4096 tokens, 64 experts, top-8
+    T, E, top, g = 4096, 64, 8, 128
+    tok, exp, off = S.moe_routing(T, E, top, seed=5)
+    R = T * top
+    off_d = on(off)
+    shapes = {"gate_up": (2048, 2816), "down": (1408, 2048)}
+    bufs = {}
+    for nm, (K, N) in shapes.items():
+        x = bf16(S.activations_bf16(R, K, seed=3 if nm == "down" else 0))
+        bufs[nm] = dict(
+            K=K, N=N, x=x,
+            qw=on(S.random_words((E, N, K // 8), seed=1)), sw=on(S.scales_f16((E, N, K // g), seed=2)),
+            q=torch.empty((R, K), dtype=torch.float8_e4m3fn, device=dev), s=torch.empty((R,), dtype=torch.float32, device=dev),
+            y=torch.empty((R, N), dtype=torch.bfloat16, device=dev),
+            ws=torch.empty((w4.w4_workspace_bytes(w4.W4_OP_W4AFP8_MOE, R, N, K, g),), dtype=torch.uint8, device=dev))
+
+    def moe_step():
+        for nm in ("gate_up", "down"):
+            b = bufs[nm]
+            w4.w4_quant_act_per_token(b["x"], "fp8", q=b["q"], scale=b["s"], stream=stream)
+            w4.w4afp8_moe_grouped_gemm(b["q"], b["s"], off_d, b["qw"], b["sw"], g, y=b["y"], workspace=b["ws"],
+                                       stream=stream)
+
+    def moe_gemms():
+        for nm in ("gate_up", "down"):
+            b = bufs[nm]
+            w4.w4afp8_moe_grouped_gemm(b["q"], b["s"], off_d, b["qw"], b["sw"], g, y=b["y"], workspace=b["ws"],
+                                       stream=stream)
+
+    t_step = _time_graph(torch, stream, moe_step, 3, 10)
+    t_gemm = _time_graph(torch, stream, moe_gemms, 3, 10)
+    flops = sum(2.0 * R * N * K for K, N in shapes.values())
+    tf_gemm = flops / (t_gemm * 1e-3) / 1e12
+    rows["w4afp8_moe"] = {
+        "config": {"tokens": T, "experts": E, "top_k": top, "rows": R, "gate_up": [2048, 2816], "down": [1408, 2048],
+                   "group": g},
+        "value": round(flops / (t_step * 1e-3) / 1e12, 1), "unit": "TFLOP/s", "ms_per_step": t_step,
+        "step": "fp8 quantization + grouped GEMM, gate_up then down",
+        "gemm_ms": t_gemm, "gemm_tflops": round(tf_gemm, 1),
+        "roofline": {"bound": "tensor", "achieved": round(tf_gemm, 1), "peak": bf16_tf, "unit": "TFLOP/s",
+                     "frac": round(tf_gemm / bf16_tf, 4), "traffic": None,
+                     "peak_source": f"{peak_kind} bf16_tflops (e4m3 activations widened to exact fp16; "
+                                    "fp16 tensor datapath)",
+                     "kernel": "w4afp8_moe_grouped_gemm call = widen_kernel + w4a8_tc_kernel"},
+    }
+    return rows
 
 
 # ---------------------------------------------------------------------------
@@ -326,6 +457,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-rows", action="store_true", help="time only the headline workload")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))

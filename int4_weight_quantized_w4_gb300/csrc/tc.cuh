@@ -20,14 +20,25 @@ W4_DEV uint64_t globaltimer_ns() {
 // or as soon as another thread of the CTA has raised *abort; on its own
 // timeout it records W4_ERR_TIMEOUT and raises *abort. Returns true when the
 // phase completed.
+// One poll that lets the hardware suspend the thread for up to `hint_ns`
+// (it resumes as soon as the phase completes), so waiting warps do not take
+// issue slots from the warps that do the work.
+W4_DEV bool try_wait_suspend(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{.reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p;}"
+      : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns) : "memory");
+  return ok != 0;
+}
+
 W4_DEV bool wait(uint64_t* bar, uint32_t parity, volatile int* abort, unsigned int* status,
-                 uint64_t limit_ns) {
+                 uint64_t limit_ns, uint32_t hint_ns = 1000) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
 #pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    for (int i = 0; i < 8; ++i)
+      if (try_wait_suspend(bar, parity, hint_ns)) return true;
     if (*abort) return false;
     if (globaltimer_ns() - t0 > limit_ns) {
       report(status, W4_ERR_TIMEOUT);
@@ -55,6 +66,26 @@ W4_DEV void tma_load_3d(void* smem_dst, const void* tmap, uint64_t* bar, int c0,
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];"
       :: "r"(smem_addr(smem_dst)), "l"(tmap), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "r"(c2) : "memory");
+}
+
+// The same tile slice lands at the same shared-memory offset in every CTA of
+// the cluster named in `cta_mask`, and completes tx bytes on the mbarrier at
+// `bar`'s offset in each of them.
+W4_DEV void tma_load_2d_multicast(void* smem_dst, const void* tmap, uint64_t* bar, int c0, int c1, uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster "
+      "[%0], [%1, {%3, %4}], [%2], %5;"
+      :: "r"(smem_addr(smem_dst)), "l"(tmap), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "h"(cta_mask) : "memory");
+}
+
+W4_DEV uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+W4_DEV void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // Makes this thread's generic-proxy shared-memory writes visible to the async
@@ -115,6 +146,13 @@ W4_DEV void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t 
 W4_DEV void commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                :: "r"(smem_addr(bar)) : "memory");
+}
+
+// Arrive (once) on the mbarrier at `bar`'s offset in every CTA of `cta_mask`
+// when every tcgen05 op this thread issued so far is done.
+W4_DEV void commit_multicast(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+               :: "r"(smem_addr(bar)), "h"(cta_mask) : "memory");
 }
 
 // Warp-wide: 32 lanes x 32 consecutive 32-bit columns from TMEM. The wait is

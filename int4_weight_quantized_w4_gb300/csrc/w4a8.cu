@@ -13,7 +13,7 @@
 // (|P| <= 127 * 8 * 16384 < 2^24) is an integer the fp32 accumulator holds
 // exactly. e4m3 activations are exact in fp16 too.
 //
-// Per output tile of 128 outputs (n) x 128 tokens:
+// Per output tile of 128 outputs (n) x 256 tokens:
 //  * swap-AB: the weights are the MMA's M operand (TMEM lane = output n),
 //    the tokens its N operand, so the per-group scale s[g, n] is one register
 //    per epilogue thread;
@@ -23,7 +23,7 @@
 //    write them into the 128-byte-swizzled K-major operand tile;
 //  * the activations were widened once per call to exact fp16 (see
 //    widen_kernel) and TMA loads them straight into the swizzled layout;
-//  * one thread issues tcgen05.mma (M=128, N=128, K=16) into a TMEM
+//  * one thread issues tcgen05.mma (M=128, N=256, K=16) into a TMEM
 //    accumulator per group; the accumulator is double-buffered so the
 //    epilogue folds group g (T += s[g,n] * P) while group g+1 accumulates;
 //  * the epilogue finally writes y = bf16(s_x[m] * T + bias[n]).
@@ -39,29 +39,33 @@ namespace w4 {
 namespace {
 
 constexpr int BM = 128;          // outputs per tile (MMA M, TMEM lanes)
-constexpr int BN = 128;          // tokens per tile (MMA N)
+constexpr int BN = 256;          // tokens per tile (MMA N)
 constexpr int BK = 64;           // k per stage (one 128-byte fp16 swizzle row)
 constexpr int UMMA_K = 16;
-constexpr int OP_STAGES = 4;
-constexpr int RAW_STAGES = 8;
+constexpr int A_STAGES = 3;      // converted weight tiles
+constexpr int B_STAGES = 4;      // activation tiles (TMA)
+constexpr int RAW_STAGES = 8;    // packed weight words (TMA)
 constexpr int SEG_MAX = 16384;   // longest accumulation before a drain (exactness bound)
 
-constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BN * BK * 2;
-constexpr int OP_BYTES = A_BYTES + B_BYTES;
-constexpr int RAW_BYTES = BM * BK / 2;
+constexpr int A_BYTES = BM * BK * 2;    // 16 KB
+constexpr int B_BYTES = BN * BK * 2;    // 32 KB
+constexpr int RAW_BYTES = BM * BK / 2;  // 4 KB
 
-constexpr int kEpiWarps = 4;
+// Warp roles, four warpgroups: 0-7 epilogue (warp w reads TMEM lane quadrant
+// w % 4, token half w / 4), 8-11 converters, 12 weight-word TMA, 13
+// activation TMA, 14 MMA issuer (and TMEM owner), 15 idle.
+constexpr int kEpiWarps = 8;
 constexpr int kConvWarps = 4;
-constexpr int kWarpConv0 = 4;
-constexpr int kWarpLoadW = 8;
-constexpr int kWarpLoadB = 9;
-constexpr int kWarpMma = 10;
-constexpr int kThreads = 11 * 32;
-constexpr uint32_t kTmemCols = 2 * BN;
+constexpr int kWarpConv0 = 8;
+constexpr int kWarpLoadW = 12;
+constexpr int kWarpLoadB = 13;
+constexpr int kWarpMma = 14;
+constexpr int kThreads = 16 * 32;
+constexpr uint32_t kTmemCols = 2 * BN;        // double-buffered accumulator
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait
+constexpr int kEpiCols = BN / 2;              // token columns per epilogue thread
 
-constexpr int kSmemBytes = OP_STAGES * OP_BYTES + RAW_STAGES * RAW_BYTES + 1024 /*bars etc*/ + 1024 /*align*/;
+constexpr int kSmemBytes = B_STAGES * B_BYTES + A_STAGES * A_BYTES + RAW_STAGES * RAW_BYTES + 2048 + 1024;
 
 enum Mode : int { kDenseY = 0, kDensePartials = 1, kExperts = 2 };
 
@@ -74,6 +78,7 @@ struct Params {
   void* out;               // bf16 [rows, N] or int32 [rows, G, N]
   const int32_t* offsets;  // [E + 1] (experts)
   int E, M, N, K, group, mode;
+  int cl;                  // CTAs per cluster along N; they share each activation tile
   unsigned int* status;
 };
 
@@ -122,14 +127,17 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
   }
   if (row0 >= row_end) return;  // no tile for this CTA (uniform across the CTA)
 
-  uint8_t* op_base = smem;
-  uint8_t* raw_base = smem + OP_STAGES * OP_BYTES;
+  uint8_t* b_base = smem;                                  // 1024-aligned
+  uint8_t* a_base = b_base + B_STAGES * B_BYTES;           // 1024-aligned
+  uint8_t* raw_base = a_base + A_STAGES * A_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(raw_base + RAW_STAGES * RAW_BYTES);
   uint64_t* raw_full = bars;
   uint64_t* raw_empty = raw_full + RAW_STAGES;
-  uint64_t* op_full = raw_empty + RAW_STAGES;
-  uint64_t* op_empty = op_full + OP_STAGES;
-  uint64_t* acc_full = op_empty + OP_STAGES;
+  uint64_t* a_full = raw_empty + RAW_STAGES;
+  uint64_t* a_empty = a_full + A_STAGES;
+  uint64_t* b_full = a_empty + A_STAGES;
+  uint64_t* b_empty = b_full + B_STAGES;
+  uint64_t* acc_full = b_empty + B_STAGES;
   uint64_t* acc_empty = acc_full + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
@@ -141,9 +149,13 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
       mbar_init(&raw_full[i], 1);
       mbar_init(&raw_empty[i], kConvWarps);
     }
-    for (int i = 0; i < OP_STAGES; ++i) {
-      mbar_init(&op_full[i], 1 + kConvWarps);
-      mbar_init(&op_empty[i], 1);
+    for (int i = 0; i < A_STAGES; ++i) {
+      mbar_init(&a_full[i], kConvWarps);
+      mbar_init(&a_empty[i], 1);
+    }
+    for (int i = 0; i < B_STAGES; ++i) {
+      mbar_init(&b_full[i], 1);
+      mbar_init(&b_empty[i], p.cl);   // every CTA of the cluster must be done with the slot
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
@@ -161,11 +173,18 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_holder;
+  // peers multicast into this CTA's shared memory: their barriers must be live
+  const uint32_t crank = p.cl > 1 ? tc::cluster_ctarank() : 0;
+  const uint16_t cmask = static_cast<uint16_t>((1u << p.cl) - 1u);
+  if (p.cl > 1) tc::cluster_sync();
 
   const int K = p.K;
   const int nst = (K + BK - 1) / BK;
   const int group = p.group;
 
+  if (warp >= kEpiWarps) {
+  // producer warpgroups give registers to the epilogue warpgroups
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 80;");
   if (warp == kWarpLoadW) {
     // ---- raw packed weight words -> ring ----
     if (lane == 0) {
@@ -180,22 +199,37 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
       }
     }
   } else if (warp == kWarpLoadB) {
-    // ---- widened activations -> operand B of each stage ----
+    // ---- widened activations -> ring; with a cluster, each CTA loads 1/cl of
+    // the rows and multicasts them to every CTA of the cluster ----
     if (lane == 0) {
+      const int rows = BN / p.cl;
+      bool ok = true;
       for (int s = 0; s < nst; ++s) {
-        const int o = s % OP_STAGES;
-        if (!tc::wait(&op_empty[o], ((s / OP_STAGES) & 1) ^ 1, abort_flag, p.status, kWaitNs)) break;
-        mbar_arrive_expect_tx(&op_full[o], B_BYTES);
-        tc::tma_load_2d(op_base + o * OP_BYTES + A_BYTES, &p.tm_act, &op_full[o], s * BK, row0);
+        const int b = s % B_STAGES;
+        if (!tc::wait(&b_empty[b], ((s / B_STAGES) & 1) ^ 1, abort_flag, p.status, kWaitNs)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&b_full[b], B_BYTES);
+        if (p.cl > 1)
+          tc::tma_load_2d_multicast(b_base + b * B_BYTES + crank * rows * 128, &p.tm_act, &b_full[b], s * BK,
+                                    row0 + crank * rows, cmask);
+        else
+          tc::tma_load_2d(b_base + b * B_BYTES, &p.tm_act, &b_full[b], s * BK, row0);
+      }
+      // every CTA of the cluster releases every slot before anyone leaves:
+      // no peer commit may still be on its way to this CTA's barriers
+      for (int b = 0; ok && b < B_STAGES && b < nst; ++b) {
+        const int uses = (nst - b + B_STAGES - 1) / B_STAGES;
+        ok = tc::wait(&b_empty[b], (uses - 1) & 1, abort_flag, p.status, kWaitNs);
       }
     }
   } else if (warp >= kWarpConv0 && warp < kWarpConv0 + kConvWarps) {
     // ---- nibbles -> fp16 operand A ----
     const int t = threadIdx.x - kWarpConv0 * 32;  // output row within the tile
     for (int s = 0; s < nst; ++s) {
-      const int r = s % RAW_STAGES, o = s % OP_STAGES;
+      const int r = s % RAW_STAGES, a = s % A_STAGES;
       if (!tc::wait(&raw_full[r], (s / RAW_STAGES) & 1, abort_flag, p.status, kWaitNs)) break;
-      if (!tc::wait(&op_empty[o], ((s / OP_STAGES) & 1) ^ 1, abort_flag, p.status, kWaitNs)) break;
       const uint32_t* raw = reinterpret_cast<const uint32_t*>(raw_base + r * RAW_BYTES);
       uint32_t w[8];
       if (p.mode == kExperts) {  // box [128 outputs][8 words]
@@ -207,66 +241,94 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
 #pragma unroll
         for (int kb = 0; kb < 8; ++kb) w[kb] = raw[kb * BM + t];
       }
-      uint8_t* arow = op_base + o * OP_BYTES + t * 128;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&raw_empty[r]);   // words are in registers
+      if (!tc::wait(&a_empty[a], ((s / A_STAGES) & 1) ^ 1, abort_flag, p.status, kWaitNs)) break;
+      uint8_t* arow = a_base + a * A_BYTES + t * 128;
 #pragma unroll
       for (int kb = 0; kb < 8; ++kb)
         *reinterpret_cast<uint4*>(arow + ((kb ^ (t & 7)) << 4)) = nibbles_to_f16(w[kb]);
       tc::fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&op_full[o]);
-        mbar_arrive(&raw_empty[r]);
-      }
+      if (lane == 0) mbar_arrive(&a_full[a]);
     }
   } else if (warp == kWarpMma) {
     // ---- one thread issues the MMAs ----
+    // Lean issue loop: one wait pair and two descriptors per stage, four MMAs
+    // per stage from constant offsets; group boundaries (multiples of 16)
+    // may fall inside a stage.
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_f16_f32(BM, BN);
-      const uint32_t op0 = smem_addr(op_base);
-      bool ok = true;
-      int seg = 0;
-      for (int k0 = 0; k0 < K && ok; ++seg) {
-        const int g = k0 / group;
-        const int kend = min(min((g + 1) * group, k0 + SEG_MAX), K);
-        const int buf = seg & 1;
-        if (!tc::wait(&acc_empty[buf], ((seg >> 1) & 1) ^ 1, abort_flag, p.status, kWaitNs)) break;
+      const uint64_t adesc0 = tc::sdesc_sw128(smem_addr(a_base));
+      const uint64_t bdesc0 = tc::sdesc_sw128(smem_addr(b_base));
+      int seg = 0, buf = 0;
+      int seg_end = min(min(group, SEG_MAX), K);
+      uint32_t acc = 0;
+      bool ok = tc::wait(&acc_empty[0], 1, abort_flag, p.status, kWaitNs);
+      tc::fence_after_sync();
+      int a = 0, b = 0, a_phase = 0, b_phase = 0;
+      for (int s = 0; s < nst && ok; ++s) {
+        if (!tc::wait(&b_full[b], b_phase, abort_flag, p.status, kWaitNs, 200) ||
+            !tc::wait(&a_full[a], a_phase, abort_flag, p.status, kWaitNs, 200)) {
+          ok = false;
+          break;
+        }
         tc::fence_after_sync();
-        const uint32_t d = tmem + buf * BN;
-        for (int k = k0; k < kend; k += UMMA_K) {
-          const int s = k / BK, o = s % OP_STAGES;
-          if (k % BK == 0) {
-            if (!tc::wait(&op_full[o], (s / OP_STAGES) & 1, abort_flag, p.status, kWaitNs)) {
-              ok = false;
-              break;
+        const uint64_t ad = adesc0 + static_cast<uint64_t>((a * A_BYTES) >> 4);
+        const uint64_t bd = bdesc0 + static_cast<uint64_t>((b * B_BYTES) >> 4);
+        const int kbase = s * BK;
+#pragma unroll
+        for (int j = 0; j < BK / UMMA_K; ++j) {
+          const int k = kbase + j * UMMA_K;
+          if (k < K) {
+            if (k == seg_end) {  // close this accumulation, open the next buffer
+              tc::commit(&acc_full[buf]);
+              ++seg;
+              buf = seg & 1;
+              const int g = k / group;
+              seg_end = min(min((g + 1) * group, k + SEG_MAX), K);
+              if (!tc::wait(&acc_empty[buf], ((seg >> 1) & 1) ^ 1, abort_flag, p.status, kWaitNs)) {
+                ok = false;
+                break;
+              }
+              tc::fence_after_sync();
+              acc = 0;
             }
-            tc::fence_after_sync();
+            tc::mma_f16(tmem + buf * BN, ad + 2 * j, bd + 2 * j, idesc, acc);
+            acc = 1;
           }
-          const uint32_t a_addr = op0 + o * OP_BYTES + (k % BK) * 2;
-          tc::mma_f16(d, tc::sdesc_sw128(a_addr), tc::sdesc_sw128(a_addr + A_BYTES), idesc, k > k0 ? 1u : 0u);
-          if ((k + UMMA_K) % BK == 0 || k + UMMA_K >= K) tc::commit(&op_empty[o]);
         }
         if (!ok) break;
-        tc::commit(&acc_full[buf]);
-        k0 = kend;
+        tc::commit(&a_empty[a]);
+        if (p.cl > 1)
+          tc::commit_multicast(&b_empty[b], cmask);
+        else
+          tc::commit(&b_empty[b]);
+        if (++a == A_STAGES) { a = 0; a_phase ^= 1; }
+        if (++b == B_STAGES) { b = 0; b_phase ^= 1; }
       }
+      if (ok) tc::commit(&acc_full[buf]);
     }
     __syncwarp();
+  }
   } else {
-    // ---- epilogue: warp e owns TMEM lanes 32e..32e+31 (outputs) ----
-    const int e = warp;
-    const int n = n0 + 32 * e + lane;
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 176;");
+    // ---- epilogue: warp w owns TMEM lanes 32(w%4).. (outputs), token half w/4 ----
+    const int q = warp & 3, half = warp >> 2;
+    const int n = n0 + 32 * q + lane;
     const bool n_ok = n < p.N;
     const int N = p.N;
     const int G = K / group;
     const bool partials = p.mode == kDensePartials;
+    const int c0 = half * kEpiCols;
     if (!partials)
       for (int j = threadIdx.x; j < BN; j += kEpiWarps * 32)
         xs_s[j] = (row0 + j < row_end) ? p.x_scale[row0 + j] : 0.f;
     bar_sync_epilogue();
 
-    float T[BN];
+    float T[kEpiCols];
 #pragma unroll
-    for (int j = 0; j < BN; ++j) T[j] = 0.f;
+    for (int j = 0; j < kEpiCols; ++j) T[j] = 0.f;
 
     int seg = 0;
     for (int k0 = 0; k0 < K; ++seg) {
@@ -275,16 +337,16 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
       const int buf = seg & 1;
       if (!tc::wait(&acc_full[buf], (seg >> 1) & 1, abort_flag, p.status, kWaitNs)) break;
       tc::fence_after_sync();
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * e) << 16) + buf * BN;
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + buf * BN + c0;
       if (partials) {
         int32_t* out = static_cast<int32_t*>(p.out);
-#pragma unroll
-        for (int cc = 0; cc < BN / 32; ++cc) {
+#pragma unroll 1
+        for (int cc = 0; cc < kEpiCols / 32; ++cc) {
           uint32_t v[32];
           tc::tmem_ld32(taddr + cc * 32, v);
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const int row = row0 + cc * 32 + j;
+            const int row = row0 + c0 + cc * 32 + j;
             if (n_ok && row < row_end)
               out[((size_t)row * G + g) * N + n] = __float2int_rn(__uint_as_float(v[j]));
           }
@@ -296,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
           s = half_bits_to_f32(p.w_scale[si]);
         }
 #pragma unroll
-        for (int cc = 0; cc < BN / 32; ++cc) {
+        for (int cc = 0; cc < kEpiCols / 32; ++cc) {
           uint32_t v[32];
           tc::tmem_ld32(taddr + cc * 32, v);
 #pragma unroll
@@ -310,12 +372,13 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
     }
 
     if (!partials && !*abort_flag) {
-      const float b = (p.bias != nullptr && n_ok) ? __uint_as_float(static_cast<uint32_t>(p.bias[n]) << 16) : 0.f;
+      const float bsv = (p.bias != nullptr && n_ok) ? __uint_as_float(static_cast<uint32_t>(p.bias[n]) << 16) : 0.f;
       uint16_t* y = static_cast<uint16_t*>(p.out);
 #pragma unroll
-      for (int j = 0; j < BN; ++j) {
-        const int row = row0 + j;
-        if (n_ok && row < row_end) y[(size_t)row * N + n] = static_cast<uint16_t>(f32_to_bf16_bits(fmaf(xs_s[j], T[j], b)));
+      for (int j = 0; j < kEpiCols; ++j) {
+        const int row = row0 + c0 + j;
+        if (n_ok && row < row_end)
+          y[(size_t)row * N + n] = static_cast<uint16_t>(f32_to_bf16_bits(fmaf(xs_s[c0 + j], T[j], bsv)));
       }
     }
   }
@@ -329,6 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
   }
   tc::fence_before_sync();
   __syncthreads();
+  if (p.cl > 1) tc::cluster_sync();
   if (warp == kWarpMma) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
@@ -433,12 +497,20 @@ cudaError_t run(const W4A8Args& a, int mode, cudaStream_t s) {
   cudaError_t e = widen(a.act, a.workspace, a.M, a.K, experts, s);
   if (e != cudaSuccess) return e;
 
+  // Optional cluster along N: the CTAs of a cluster share one activation
+  // tile, each loading 1/cl of it and multicasting it to the others. Measured
+  // on GB300 this did not beat one CTA per tile (the activation stream is not
+  // limited by L2 bandwidth), so the launcher uses cl = 1; the multicast path
+  // stays for shapes that are.
+  const int n_tiles = static_cast<int>((a.N + BM - 1) / BM);
+  const int cl = 1;
+
   Params p;
   memset(&p, 0, sizeof(p));
   {
     const cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.M};
     const cuuint64_t strides[1] = {(cuuint64_t)a.K * 2};
-    const cuuint32_t box[2] = {BK, BN};
+    const cuuint32_t box[2] = {BK, static_cast<cuuint32_t>(BN / cl)};   // one CTA's slice of the tile
     e = encode(&p.tm_act, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.workspace, dims, strides, box,
                CU_TENSOR_MAP_SWIZZLE_128B);
     if (e != cudaSuccess) return e;
@@ -468,11 +540,23 @@ cudaError_t run(const W4A8Args& a, int mode, cudaStream_t s) {
   p.mode = mode;
   p.status = a.status;
 
-  const unsigned gx = static_cast<unsigned>((a.N + BM - 1) / BM);
+  p.cl = cl;
+  const unsigned gx = static_cast<unsigned>((n_tiles + cl - 1) / cl * cl);
   const long long gy = experts ? (a.M + BN - 1) / BN + a.E : (a.M + BN - 1) / BN;
   if (gy > 65535) return cudaErrorInvalidConfiguration;
-  w4a8_tc_kernel<<<dim3(gx, static_cast<unsigned>(gy)), kThreads, kSmemBytes, s>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(gx, static_cast<unsigned>(gy));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, w4a8_tc_kernel, p);
 }
 
 }  // namespace
