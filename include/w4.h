@@ -152,7 +152,17 @@ w4_status w4a8_group_partials(const void* qx, const void* qweight, int32_t group
  * y[m,n] = bf16( sum_g [ s[g,n] * sum_{k in g} x[m,k] (q[k,n]-8)
  *                        + z[g,n] * sum_{k in g} x[m,k] ] + bias[n] ),
  * products exact, sums in fp32. Built for small M (tokens are processed in
- * blocks of 8); group: -1 or a multiple of 32 dividing K; K % 32 == 0.
+ * blocks of up to 8, each block one pass over the weights, its x held in
+ * shared memory); group: -1 or a multiple of 64 dividing K; K % 64 == 0 and
+ * one token row of x must fit in shared memory (K up to about 64000), else
+ * W4_ERR_UNSUPPORTED.
+ * Launched with programmatic dependent launch: the kernel may start, and
+ * start streaming qweight, while the kernel before it on `stream` is still
+ * finishing (it waits for that kernel before it reads x, the scales, the
+ * zeros or the bias, or writes y). So qweight must not be written by a kernel
+ * that runs immediately before on the same stream and signals its dependents
+ * early; kernels that do not (every kernel of this library except this one,
+ * and ordinary library kernels) are waited for in full.
  */
 w4_status w4a16_gemm(const void* x, const void* qweight, const void* w_scale, int32_t w_scale_dtype,
                      const void* zeros, int32_t group, const void* bias, void* y,

@@ -179,16 +179,21 @@ w4_status w4a16_gemm(const void* x, const void* qweight, const void* w_scale, in
   if (st != W4_OK) return st;
   if (w_scale_dtype != W4_FP16 && w_scale_dtype != W4_BF16)
     return fail(W4_ERR_DTYPE, "w4a16_gemm scales must be W4_FP16 or W4_BF16");
-  if (K % 32 != 0 || g % 32 != 0)
-    return fail(W4_ERR_UNSUPPORTED, "w4a16 tiles need K and the group to be multiples of 32 (K=%lld group=%d)",
+  if (K % 64 != 0 || g % 64 != 0)
+    return fail(W4_ERR_UNSUPPORTED, "w4a16 tiles need K and the group to be multiples of 64 (K=%lld group=%d)",
                 (long long)K, g);
+  if (w4::w4a16_smem_bytes(K, g) > 227 * 1024)
+    return fail(W4_ERR_UNSUPPORTED, "w4a16 keeps a token row of x in shared memory: K=%lld is too long", (long long)K);
   if (M == 0) return ok();
   if (!x || !qweight || !w_scale || !y) return fail(W4_ERR_NULL, "x, qweight, w_scale and y must be non-NULL");
   if (!aligned(x, 16) || !aligned(qweight, 16) || !aligned(y, 8) || !aligned(w_scale, 8) ||
       (zeros && !aligned(zeros, 8)) || (bias && !aligned(bias, 8)))
     return fail(W4_ERR_ALIGN, "x and qweight must be 16-byte aligned; y, scales, zeros, bias 8-byte aligned");
   if (M > INT32_MAX || N > INT32_MAX) return fail(W4_ERR_UNSUPPORTED, "M or N too large");
-  w4::W4A16Args a{x, qweight, w_scale, w_scale_dtype == W4_BF16, zeros, bias, y, M, N, K, g};
+  unsigned int* status = nullptr;
+  cudaError_t e = status_ptr(&status);
+  if (e != cudaSuccess) return from_cuda(e, "device status word");
+  w4::W4A16Args a{x, qweight, w_scale, w_scale_dtype == W4_BF16, zeros, bias, y, M, N, K, g, status};
   return from_cuda(w4::launch_w4a16(a, static_cast<cudaStream_t>(stream)), "w4a16 launch");
 }
 

@@ -24,8 +24,11 @@ struct W4A16Args {
   void* y;
   int64_t M, N, K;
   int32_t group;  // effective group (K when the caller passed -1)
+  unsigned int* status;
 };
 cudaError_t launch_w4a16(const W4A16Args& a, cudaStream_t s);
+// Shared memory the decode kernel needs for one token row beside a minimal ring.
+size_t w4a16_smem_bytes(int64_t K, int32_t group);
 
 struct W4A8Args {
   const void* act;        // int8 [M,K] (dense) or e4m3 [R,K] (experts)

@@ -93,6 +93,9 @@ def test_w4a16_validation(lib):
                               a["M"], a["N"], a["K"], None)
     assert call(wdt=w4.W4_INT8) == w4.W4_ERR_DTYPE
     assert call(group=16) == w4.W4_ERR_UNSUPPORTED
+    assert call(group=32) == w4.W4_ERR_UNSUPPORTED
+    assert call(K=288, group=-1) == w4.W4_ERR_UNSUPPORTED         # K % 64
+    assert call(K=131072, group=128) == w4.W4_ERR_UNSUPPORTED     # a row of x does not fit in shared memory
     assert call(N=12) == w4.W4_ERR_ALIGN
     assert call(group=3) == w4.W4_ERR_GROUP
     assert call(x=None) == w4.W4_ERR_NULL
