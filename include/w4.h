@@ -127,6 +127,25 @@ w4_status w4a8_gemm(const void* qx, const float* x_scale, const void* qweight,
                     void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * w4a8_gemm for callers that cannot allocate device memory (no counterpart on
+ * the source pages: a service of this library). Same arguments and results as
+ * w4a8_gemm, minus the workspace: it uses a 32 MiB workspace built into the
+ * library, a device array that every GPU which loads the library holds until
+ * the process exits. It allocates nothing itself.
+ *   - M * K must be at most 16,777,216 (2 bytes of workspace per activation),
+ *     else W4_ERR_UNSUPPORTED with a message in w4_last_error().
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call shares the one array and overwrites it: calls whose kernels
+ *     may overlap on the GPU (other streams, other host threads) race and
+ *     must be serialized by the caller. Nothing in the array needs to start
+ *     at zero; it keeps the last call's contents.
+ */
+w4_status w4a8_gemm_noalloc(const void* qx, const float* x_scale, const void* qweight,
+                            const void* w_scale, int32_t w_scale_dtype, int32_t group,
+                            const void* bias, void* y, int64_t M, int64_t N, int64_t K, void* stream);
+
+/*
  * The integer group partials of w4a8_gemm, from the same tensor-core path:
  *   partials [M, G, N] int32, P[m,g,n] = sum_{k in g} qx[m,k] * (q[k,n] - 8).
  * Same argument rules as w4a8_gemm. Meant for verifying the integer core;

@@ -16,7 +16,7 @@ import torch
 
 __all__ = [
     "W4Error", "load", "library_path",
-    "w4_quant_act_per_token", "w4a8_gemm", "w4a8_group_partials", "w4a16_gemm",
+    "w4_quant_act_per_token", "w4a8_gemm", "w4a8_gemm_noalloc", "w4a8_group_partials", "w4a16_gemm",
     "w4afp8_moe_grouped_gemm", "w4_device_status", "w4_selftest_bounded_wait",
     "W4_OK", "W4_ERR_NULL", "W4_ERR_ALIGN", "W4_ERR_GROUP", "W4_ERR_DTYPE",
     "W4_ERR_UNSUPPORTED", "W4_ERR_SHAPE", "W4_ERR_CUDA", "W4_ERR_TIMEOUT", "W4_ERR_WORKSPACE",
@@ -38,6 +38,7 @@ _SIGNATURES = {
     "w4_workspace_bytes": (_SZ, [_I32, _I64, _I64, _I64, _I32]),
     "w4a8_gemm": (_I32, [_P, _P, _P, _P, _I32, _I32, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
     "w4a8_group_partials": (_I32, [_P, _P, _I32, _P, _I64, _I64, _I64, _P, _SZ, _P]),
+    "w4a8_gemm_noalloc": (_I32, [_P, _P, _P, _P, _I32, _I32, _P, _P, _I64, _I64, _I64, _P]),
     "w4a16_gemm": (_I32, [_P, _P, _P, _I32, _P, _I32, _P, _P, _I64, _I64, _I64, _P]),
     "w4afp8_moe_grouped_gemm": (_I32, [_P, _P, _P, _I32, _P, _P, _I32, _I32, _P, _I64, _I64, _I64, _P, _SZ, _P]),
     "w4_last_error": (ctypes.c_char_p, []),
@@ -146,6 +147,24 @@ def w4a8_gemm(qx, x_scale, qweight, w_scale, group: int, bias=None, y=None, work
     _check(load().w4a8_gemm(_ptr(qx), _ptr(x_scale), _ptr(qweight), _ptr(w_scale), _scale_dtype(w_scale),
                             group, _ptr(bias), _ptr(y), M, N, K, _ptr(ws), wsb, _stream(stream, qx.device)),
            "w4a8_gemm")
+    return y
+
+
+def w4a8_gemm_noalloc(qx, x_scale, qweight, w_scale, group: int, bias=None, y=None, stream=None):
+    """``w4a8_gemm`` without a workspace argument: for callers that cannot
+    allocate device memory, it uses the library's built-in 32 MiB workspace
+    (M * K <= 16,777,216). Calls that may overlap on the GPU share that
+    workspace and must be serialized by the caller."""
+    _cuda2d(qx, "qx", (torch.int8,))
+    _cuda2d(qweight, "qweight", (torch.int32,))
+    M, K = qx.shape
+    N = qweight.shape[1]
+    if qweight.shape[0] * 8 != K or x_scale.shape != (M,) or w_scale.dim() != 2 or w_scale.shape[1] != N:
+        raise ValueError("inconsistent shapes for w4a8_gemm_noalloc")
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=qx.device) if y is None else y
+    _check(load().w4a8_gemm_noalloc(_ptr(qx), _ptr(x_scale), _ptr(qweight), _ptr(w_scale), _scale_dtype(w_scale),
+                                    group, _ptr(bias), _ptr(y), M, N, K, _stream(stream, qx.device)),
+           "w4a8_gemm_noalloc")
     return y
 
 

@@ -76,6 +76,11 @@ w4_status check_dims_group(int64_t M, int64_t N, int64_t K, int32_t group, int32
 
 }  // namespace
 
+namespace w4 {
+// Lets other translation units report a status with a message for w4_last_error().
+w4_status report_error(w4_status st, const char* msg) { return fail(st, "%s", msg); }
+}  // namespace w4
+
 extern "C" {
 
 const char* w4_last_error(void) { return g_last_error; }

@@ -6,6 +6,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "w4.h"
+
 namespace w4 {
 
 // Polls a bounded wait makes before it gives up (about a second of spinning).
@@ -46,6 +48,8 @@ struct W4A8Args {
   void* workspace;        // fp16 [rows, K]: the activations widened once per call
 };
 size_t w4a8_workspace_bytes(int64_t rows, int64_t K);
+// Sets the calling thread's w4_last_error() message and returns `st`.
+w4_status report_error(w4_status st, const char* msg);
 cudaError_t launch_w4a8_dense(const W4A8Args& a, cudaStream_t s);
 cudaError_t launch_w4afp8_experts(const W4A8Args& a, cudaStream_t s);
 
