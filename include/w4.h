@@ -164,8 +164,8 @@ w4_status w4a8_group_partials(const void* qx, const void* qweight, int32_t group
  *
  *   x        [M, K] bf16
  *   qweight  [K/8, N] int32 GPTQ (as in w4a8_gemm)
- *   w_scale  [G, N], w_scale_dtype W4_FP16 or W4_BF16
- *   zeros    [G, N] bf16 or NULL (symmetric)
+ *   w_scale  [G, N], w_scale_dtype W4_FP16 or W4_BF16, 16-byte aligned
+ *   zeros    [G, N] bf16 or NULL (symmetric), 16-byte aligned
  *   bias     [N] bf16 or NULL
  *   y        [M, N] bf16
  * y[m,n] = bf16( sum_g [ s[g,n] * sum_{k in g} x[m,k] (q[k,n]-8)
@@ -176,12 +176,13 @@ w4_status w4a8_group_partials(const void* qx, const void* qweight, int32_t group
  * one token row of x must fit in shared memory (K up to about 64000), else
  * W4_ERR_UNSUPPORTED.
  * Launched with programmatic dependent launch: the kernel may start, and
- * start streaming qweight, while the kernel before it on `stream` is still
- * finishing (it waits for that kernel before it reads x, the scales, the
- * zeros or the bias, or writes y). So qweight must not be written by a kernel
- * that runs immediately before on the same stream and signals its dependents
- * early; kernels that do not (every kernel of this library except this one,
- * and ordinary library kernels) are waited for in full.
+ * start streaming qweight with its scales and zeros, while the kernel before
+ * it on `stream` is still finishing (it waits for that kernel before it reads
+ * x or the bias, or writes y). So qweight, w_scale and zeros must not be
+ * written by a kernel that runs immediately before on the same stream and
+ * signals its dependents early; kernels that do not (every kernel of this
+ * library except this one, and ordinary library kernels) are waited for in
+ * full.
  */
 w4_status w4a16_gemm(const void* x, const void* qweight, const void* w_scale, int32_t w_scale_dtype,
                      const void* zeros, int32_t group, const void* bias, void* y,

@@ -187,13 +187,13 @@ w4_status w4a16_gemm(const void* x, const void* qweight, const void* w_scale, in
   if (K % 64 != 0 || g % 64 != 0)
     return fail(W4_ERR_UNSUPPORTED, "w4a16 tiles need K and the group to be multiples of 64 (K=%lld group=%d)",
                 (long long)K, g);
-  if (w4::w4a16_smem_bytes(K, g) > 227 * 1024)
+  if (w4::w4a16_smem_bytes(N, K, g) > 227 * 1024)
     return fail(W4_ERR_UNSUPPORTED, "w4a16 keeps a token row of x in shared memory: K=%lld is too long", (long long)K);
   if (M == 0) return ok();
   if (!x || !qweight || !w_scale || !y) return fail(W4_ERR_NULL, "x, qweight, w_scale and y must be non-NULL");
-  if (!aligned(x, 16) || !aligned(qweight, 16) || !aligned(y, 8) || !aligned(w_scale, 8) ||
-      (zeros && !aligned(zeros, 8)) || (bias && !aligned(bias, 8)))
-    return fail(W4_ERR_ALIGN, "x and qweight must be 16-byte aligned; y, scales, zeros, bias 8-byte aligned");
+  if (!aligned(x, 16) || !aligned(qweight, 16) || !aligned(y, 8) || !aligned(w_scale, 16) ||
+      (zeros && !aligned(zeros, 16)) || (bias && !aligned(bias, 8)))
+    return fail(W4_ERR_ALIGN, "x, qweight, scales and zeros must be 16-byte aligned; y and bias 8-byte aligned");
   if (M > INT32_MAX || N > INT32_MAX) return fail(W4_ERR_UNSUPPORTED, "M or N too large");
   unsigned int* status = nullptr;
   cudaError_t e = status_ptr(&status);

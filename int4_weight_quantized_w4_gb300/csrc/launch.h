@@ -30,7 +30,7 @@ struct W4A16Args {
 };
 cudaError_t launch_w4a16(const W4A16Args& a, cudaStream_t s);
 // Shared memory the decode kernel needs for one token row beside a minimal ring.
-size_t w4a16_smem_bytes(int64_t K, int32_t group);
+size_t w4a16_smem_bytes(int64_t N, int64_t K, int32_t group);
 
 struct W4A8Args {
   const void* act;        // int8 [M,K] (dense) or e4m3 [R,K] (experts)

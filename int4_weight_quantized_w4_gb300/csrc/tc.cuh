@@ -68,6 +68,21 @@ W4_DEV void tma_load_3d(void* smem_dst, const void* tmap, uint64_t* bar, int c0,
       :: "r"(smem_addr(smem_dst)), "l"(tmap), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "r"(c2) : "memory");
 }
 
+// Contiguous global -> shared copy of `bytes` (a multiple of 16; both
+// addresses 16-byte aligned), completion counted on `bar`.
+W4_DEV void bulk_load(void* smem_dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      :: "r"(smem_addr(smem_dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)) : "memory");
+}
+
+// Starts moving a tile into L2 without a shared-memory destination or a
+// completion to wait for (a later tma_load_2d of it then hits in L2).
+W4_DEV void tma_prefetch_l2_2d(const void* tmap, int c0, int c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+               :: "l"(tmap), "r"(c0), "r"(c1) : "memory");
+}
+
 // The same tile slice lands at the same shared-memory offset in every CTA of
 // the cluster named in `cta_mask`, and completes tx bytes on the mbarrier at
 // `bar`'s offset in each of them.

@@ -7,42 +7,57 @@
 // the token rate -- and the weight is w = (q - 8) * scale + zero.
 //
 // Design (GB300):
-//  * Persistent CTAs, at most one per SM. The output columns are cut into
-//    strips of 32; a CTA owns whole strips across all of K, dealt round-robin,
-//    so there is no cross-CTA reduction and the work per SM is within one
-//    strip of even.
-//  * One producer thread streams each strip as 16 KB TMA tiles (32 columns x
-//    1024 k, 128-byte swizzle) through an up-to-8-deep shared-memory ring:
-//    128 KB of weights in flight per SM, independent of registers. (Measured
-//    on GB300: TMA streams at HBM rate from 16 KB tiles but only ~2.4 TB/s
-//    from 8 KB and ~1.6 TB/s from 4 KB ones.)
-//  * Programmatic dependent launch: the weights never depend on the previous
-//    kernel, so the grid starts streaming them while the previous call on the
-//    stream drains, and waits for it only before reading x and writing y.
-//    A standalone 30 MB stream pays a ~4 us fixed cost per launch on GB300;
-//    back-to-back decode calls hide most of it this way.
-//  * Sixteen consumer warps, four per tile, each take 256 k of a tile, with
-//    four independent MMA accumulator chains each. Swap-AB on the warp-level
-//    tensor core (m16n8k16, fp16 in, fp32 accumulate): 16 output columns are
-//    the MMA's rows, up to 8 tokens its columns.
-//  * Nibbles enter the MMA with one AND per pair and no convert: a nibble in
-//    bits 0-3 of an fp16 is the exact subnormal q * 2^-24, one in bits 4-7 is
-//    16 q * 2^-24 (fp16 subnormal operands multiply exactly on the tensor
-//    core). Nibbles i and i+4 of a word share one register. The activations
-//    are staged once per CTA as fp16 2^e x, with 2^e a per-token power of two
-//    that puts the token's largest |x| in [2^14, 2^15) so every 2^e x is an
-//    exact fp16 (except ones below 2^-14 relative to that maximum, whose
-//    rounding is far below the fp32 sums); the activations paired with the
-//    16 q nibbles carry an extra 1/16.
-//  * Per scale group the exact-product fp32 partial becomes
-//    sum x (q - 8) = 2^24 acc - 8 sum(x), folded as
-//    tot += s (2^24 acc - 8 sum x) + z sum x, with the token sums over 64-k
-//    blocks computed once; the result is scaled back by 2^-e.
+//  * Two kernels per call, both with programmatic dependent launch. A one-warp
+//    prefetch grid starts beside the previous call's GEMV (it needs no shared
+//    memory), pulls this call's weights, scales and zeros into L2, and waits
+//    for the previous kernel before it exits. The GEMV grid that follows
+//    therefore streams its weights from L2 while HBM already serves the next
+//    call's prefetch: back-to-back decode calls keep HBM busy across the call
+//    boundary, and the conversion work per weight (~1.8 us a call at
+//    4096 x 14336 on 152 SMs) hides under it.
+//  * GEMV: persistent CTAs, one per SM. The output columns are cut into
+//    strips of 32; a CTA owns whole strips across all of K, dealt
+//    round-robin, so there is no cross-CTA reduction.
+//  * Each strip moves as 16 KB TMA tiles (32 columns x 1024 k, 128-byte
+//    swizzle) with the scale (and zero) rows the tile's k range meets, all on
+//    one mbarrier, through a ring of up to 8 stages. (A plain global load from
+//    an SM with that much streaming in flight waits ~2 us on GB300, so the
+//    consumer loop touches no global memory.) There is no producer warp: one
+//    thread fills the ring at the start, and the warp that finishes the last
+//    unit of a stage refills its slot with the stage R later (a per-slot
+//    shared counter elects it). Sixteen warps, four per SM sub-partition, get
+//    120 registers each.
+//  * The warps take 256-k units of a strip (four per stage): warp w gets
+//    units w, w + 16, ..., so the four units of stage i always go to warp
+//    group i % 4. The ring depth is a multiple of 4, so each warp sees every
+//    phase of the slots it reads and the parity waits stay exact.
+//  * Swap-AB on the warp-level tensor core (m16n8k16, fp16 in, fp32
+//    accumulate): 16 output columns are the MMA rows, up to 8 tokens its
+//    columns. Nibbles enter the MMA with one AND per pair and no convert: a
+//    nibble in bits 0-3 of an fp16 is the exact subnormal q 2^-24, one in
+//    bits 4-7 is 16 q 2^-24 (fp16 subnormal operands multiply exactly on the
+//    tensor core, at full rate). Nibbles i and i+4 of a word share one
+//    register. Each 256-k segment of a token's x is staged as fp16 2^e x, with
+//    2^e a power of two per (token, segment) that puts the segment's largest
+//    |x| in [2^14, 2^15), so every 2^e x is an exact fp16 (except ones below
+//    2^-24 of that maximum, whose rounding is far below the fp32 sums); the
+//    ones paired with the 16 q nibbles carry an extra 1/16.
+//  * x segments have owner warps (segment u: warp u % 16): the owner
+//    bulk-copies its segments right after the dependency wait, converts them
+//    in place and signals a per-segment mbarrier, so no block-wide barrier
+//    sits between the wait and the first MMA. At the common K = 4096 each
+//    warp only ever reads its own segment.
+//  * Per scale group the partial is folded as
+//    tot += s 2^-e acc + (z - 8 s) X, X = 2^-24 sum x over the group's k
+//    (since sum x (q - 8) = 2^24 2^-e acc - 8 sum x); tot is scaled by 2^24
+//    at the end (exact). Fold points are compile-time for groups of 64, 128
+//    and multiples of 256.
 //  * The k order inside each 32-wide step is permuted consistently for both
-//    operands; the word-row order (2c + step parity) makes the 16-byte
-//    shared loads of a quarter-warp land in 8 distinct swizzled chunks.
-//  * Partials of a strip are reduced across the consumer warps in shared
-//    memory in a fixed order; the bias is added and y written once in bf16.
+//    operands; word rows 2c + (step parity) make the 16-byte shared loads of
+//    a quarter-warp land in 8 distinct swizzled chunks.
+//  * Each warp keeps its strip partial in registers and stores it once per
+//    strip; after the last unit the block sums the partials in a fixed order,
+//    adds the bias and writes y once in bf16.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -56,26 +71,33 @@ constexpr int kStrip = 32;          // output columns per strip
 constexpr int kStageRows = 128;     // word rows per stage (1024 k)
 constexpr int kStageK = kStageRows * 8;
 constexpr int kStageBytes = kStrip * kStageRows * 4;   // 16 KB
-constexpr int kRingMax = 8;         // up to 128 KB of weights in flight
+constexpr int kRingMax = 8;
 constexpr int kConsumers = 16;
-constexpr int kPerStage = 4;        // consumer warps per stage, 32 word rows (256 k) each
-constexpr int kQuarterRows = kStageRows / kPerStage;
-constexpr int kProducerWarp = kConsumers;
-constexpr int kThreads = (kConsumers + 1) * 32;
+constexpr int kUnitRows = 32;       // word rows per consumer unit (256 k, 8 steps)
+constexpr int kUnitK = kUnitRows * 8;
+constexpr int kUnitsPerStage = kStageRows / kUnitRows;
+constexpr int kSegChunks = kUnitK / 8;   // 16-byte x chunks per 256-k segment (one per lane)
+constexpr int kThreads = kConsumers * 32;
 constexpr int kTok = 8;             // tokens per MMA column block
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 struct Params {
   CUtensorMap tm_w;      // GPTQ words [K/8, N], box 32 x 128, 128-byte swizzle
+  CUtensorMap tm_s;      // scales, fp16 or bf16 [G, N], box 32 x gh
+  CUtensorMap tm_z;      // zeros, bf16 [G, N], box 32 x gh (when present)
   const uint16_t* x;     // bf16 [M, K]
-  const uint16_t* sc;    // fp16 or bf16 [G, N]
-  const uint16_t* zr;    // bf16 [G, N] or null
   const uint16_t* bias;  // bf16 [N] or null
   uint16_t* y;           // bf16 [M, N]
   int M, N, K, group;    // M <= 8 here
   int strips, stages;    // per strip: stages = ceil(K / 1024)
   int xstride;           // shared-memory row stride of x, in fp16 elements
-  int ring;              // stages in the ring (<= kRingMax)
+  int ring;              // stages in the ring: 4 or 8
+  int gh;                // scale rows per stage tile: most groups one stage's k range meets
+  int zoff;              // byte offset of the zero rows inside a slot's scale area
+  int scb;               // bytes of one slot's scale area (scales, then zeros)
+  int pstrips;           // most strips one CTA owns
+  int ring_shift;        // log2(ring)
+  int group_shift;       // log2(group) when the group is a power of two, else -1
   unsigned int* status;
 };
 
@@ -88,12 +110,15 @@ W4_DEV void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-template <bool kScaleBf16>
-W4_DEV float scale_at(uint32_t bits16) {
-  return kScaleBf16 ? __uint_as_float(bits16 << 16) : half_bits_to_f32(bits16);
+// One m16n8k16 MMA that starts from zero instead of accumulating.
+W4_DEV void mma_f16_first(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                          uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
 }
-
-W4_DEV uint2 ld4x16(const uint16_t* p, bool in) { return in ? ld_nc_v2(p) : make_uint2(0, 0); }
 
 W4_DEV uint32_t pack_f16x2(float lo, float hi) {
   uint32_t d;
@@ -103,51 +128,84 @@ W4_DEV uint32_t pack_f16x2(float lo, float hi) {
 
 // Shared-memory carve-up (byte offsets from the 1024-aligned base).
 struct Layout {
-  int red, bars, ex, xsum, xs, total;
-  __host__ __device__ Layout(int nb64, int xchunks, int rows, int ring) {
-    red = ring * kStageBytes;
-    bars = red + 2 * kConsumers * kStrip * rows * 4;   // [2][kConsumers][rows * kStrip]
-    ex = bars + 256;                      // 2 * kRingMax + 4 mbarriers + the abort flag
-    xsum = ex + 2 * kTok * 4;             // per token: 2^e and 2^-e
-    xs = (xsum + rows * nb64 * 4 + 15) & ~15;
-    total = xs + rows * xchunks * 16;
+  int scl, red, bars, xrdy, exs, xsum, xs, total;
+  __host__ __device__ Layout(int nseg, int xchunks, int rows, int ring, int scb, int pstrips) {
+    scl = ring * kStageBytes;             // ring x scb: scale (and zero) rows per slot
+    red = scl + ring * scb;               // [pstrips][kConsumers][rows][kStrip] strip partials
+    bars = red + pstrips * kConsumers * rows * kStrip * 4;   // full, per-warp x, slot counters, abort flag
+    xrdy = bars + 512;                    // [nseg] mbarriers: x segment converted
+    exs = xrdy + nseg * 8;                // [nseg][kTok] 2^-e per segment and token
+    xsum = exs + nseg * kTok * 4;         // [nseg * 4][kTok] 2^-24 sums of x over 64-k blocks
+    xs = (xsum + nseg * 4 * kTok * 4 + 15) & ~15;
+    total = xs + rows * xchunks * 16;     // [rows][xchunks] x, converted in place
   }
 };
 
-template <bool kScaleBf16, bool kZero, bool kBias>
-__global__ void __launch_bounds__(kThreads, 1) w4a16_kernel(const __grid_constant__ Params p) {
+// Pulls [base, base + bytes) into L2, this block's share of it, 16 KB at a
+// time (base 16-byte aligned, bytes a multiple of 16).
+W4_DEV void prefetch_share(const uint8_t* base, size_t bytes) {
+  if (base == nullptr || bytes == 0) return;
+  const size_t share = ((bytes + gridDim.x - 1) / gridDim.x + 15) & ~size_t(15);
+  const size_t lo = blockIdx.x * share;
+  const size_t hi = lo + share < bytes ? lo + share : bytes;
+  for (size_t o = lo; o < hi; o += 16384) {
+    const uint32_t n = static_cast<uint32_t>(hi - o < 16384 ? hi - o : 16384);
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(base + o), "r"(n) : "memory");
+  }
+}
+
+// The L2 prefetch grid: one warp per SM, no shared memory, so it runs beside
+// the previous call's GEMV. It lets its dependent (this call's GEMV) launch at
+// once, and it completes only after the kernel before it on the stream, so the
+// GEMV's dependency wait still covers that kernel.
+__global__ void __launch_bounds__(32) w4a16_prefetch_kernel(const uint8_t* w, size_t wb, const uint8_t* s,
+                                                            size_t sb, const uint8_t* z, size_t zb) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (threadIdx.x == 0) {
+    prefetch_share(w, wb);
+    prefetch_share(s, sb);
+    prefetch_share(z, zb);
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// kSPF: steps (32 k each) per scale group inside a 256-k unit when the fold
+// points are fixed -- 2 for group 64, 4 for group 128, 8 for groups that are
+// multiples of 256 -- or 0 for any other group, whose fold points are found
+// per unit.
+// 120 registers a thread, not the 128 that 512 threads could have: a
+// sub-partition then keeps room for the one-warp prefetch grid of the next
+// call (4 x 32 x 120 + 768 <= 16384), which must run beside this grid.
+template <bool kScaleBf16, bool kZero, int kSPF>
+__global__ void __maxnreg__(120) w4a16_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   const int S = p.stages;
   const int R = p.ring;
-  const int nb64 = S * (kStageK / 64);       // 64-wide k blocks (padded to whole stages)
+  const int M = p.M;
+  const int nseg = S * (kStageK / kUnitK);   // 256-k x segments (padded to whole stages)
   const int xch = p.xstride / 8;             // 16-byte chunks per token row
-  const Layout L(nb64, xch, p.M, R);
-  const int red_n = p.M * kStrip;            // partial outputs per warp
+  const Layout L(nseg, xch, M, R, p.scb, p.pstrips);
   uint8_t* ring = smem;                                      // R x 16 KB, 1024-aligned
-  float* red = reinterpret_cast<float*>(smem + L.red);       // [2][kConsumers][red_n]
+  const uint8_t* scl = smem + L.scl;                         // R x scb
+  float* red = reinterpret_cast<float*>(smem + L.red);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
-  uint64_t* empty = full + kRingMax;
-  uint64_t* red_full = empty + kRingMax;
-  uint64_t* red_empty = red_full + 2;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(red_empty + 2);
-  float* ex = reinterpret_cast<float*>(smem + L.ex);         // [kTok] 2^e, then [kTok] 2^-e
-  float* xsum = reinterpret_cast<float*>(smem + L.xsum);     // [M][nb64]: sum of 2^e x over 64-k blocks
-  uint4* xs = reinterpret_cast<uint4*>(smem + L.xs);         // [M][xch]: 2^e x as fp16, permuted
+  uint64_t* xbar = full + kRingMax;                          // [kConsumers] a warp's x copies landed
+  unsigned int* done = reinterpret_cast<unsigned int*>(xbar + kConsumers);   // [kRingMax] units finished per slot
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(done + kRingMax);
+  uint64_t* xrdy = reinterpret_cast<uint64_t*>(smem + L.xrdy);
+  float* exs = reinterpret_cast<float*>(smem + L.exs);
+  float* xsum = reinterpret_cast<float*>(smem + L.xsum);
+  uint4* xs = reinterpret_cast<uint4*>(smem + L.xs);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // consumer warp w works on word rows [32 (w % 4), +32) of stages w / 4, w / 4 + 4, ...
-  const int groups = kConsumers / kPerStage;
-  const int act = (S < groups ? S : groups) * kPerStage;   // consumer warps with work in every strip
   if (threadIdx.x == 0) {
     for (int i = 0; i < R; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kPerStage);
+      done[i] = 0u;
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&red_full[i], act);
-      mbar_init(&red_empty[i], 1);
-    }
+    for (int i = 0; i < kConsumers; ++i) mbar_init(&xbar[i], 1);
+    for (int i = 0; i < nseg; ++i) mbar_init(&xrdy[i], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -155,160 +213,99 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_kernel(const __grid_constan
 
   const int my_strips = p.strips > (int)blockIdx.x ? (p.strips - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
 
-  // the next call on the stream may start now: its weight stream does not
-  // depend on this call (it waits for this grid before touching x and y)
+  // the next call on the stream may start now: its grids do not touch this
+  // call's x or y before they wait for it
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-  if (warp == kProducerWarp) {
-    // ---- stream this CTA's strips, stage by stage, through the ring; the
-    // weights never depend on the previous kernel, so this starts at once ----
-    if (lane == 0) {
-      tc::prefetch_tmap(&p.tm_w);
-      const int total = my_strips * S;
-      for (int i = 0; i < total; ++i) {
-        const int slot = i % R;
-        if (!tc::wait(&empty[slot], ((i / R) & 1) ^ 1, abort_flag, p.status, kWaitNs)) break;
-        const int strip = blockIdx.x + (i / S) * gridDim.x, st = i % S;
-        mbar_arrive_expect_tx(&full[slot], kStageBytes);
-        tc::tma_load_2d(ring + slot * kStageBytes, &p.tm_w, &full[slot], strip * kStrip, st * kStageRows);
+  const int total = my_strips * S;            // stages this CTA streams
+  const uint32_t tx = kStageBytes + (kZero ? 2 : 1) * p.gh * kStrip * 2;
+  // stage i -> its ring slot (the weights never depend on the previous kernel)
+  auto issue = [&](int i) {
+    const int slot = i & (R - 1);
+    const int col = (blockIdx.x + (i / S) * gridDim.x) * kStrip, st = i % S;
+    const int gst = st * kStageK / p.group;   // first scale row the stage meets
+    uint8_t* sdst = smem + L.scl + slot * p.scb;
+    mbar_arrive_expect_tx(&full[slot], tx);
+    tc::tma_load_2d(ring + slot * kStageBytes, &p.tm_w, &full[slot], col, st * kStageRows);
+    tc::tma_load_2d(sdst, &p.tm_s, &full[slot], col, gst);
+    if (kZero) tc::tma_load_2d(sdst + p.zoff, &p.tm_z, &full[slot], col, gst);
+  };
+  if (threadIdx.x == 0) {
+    tc::prefetch_tmap(&p.tm_w);
+    tc::prefetch_tmap(&p.tm_s);
+    if (kZero) tc::prefetch_tmap(&p.tm_z);
+    for (int i = 0; i < R && i < total; ++i) issue(i);
+  }
+  {
+    const int K = p.K, group = p.group;
+    // ---- prologue, per warp over the x segments it owns (u = warp, warp + 16,
+    // ...): zero what lies past K (nothing here depends on x), then after the
+    // dependency wait copy the segments in, find each token's largest
+    // exponent field E in the segment, which fixes 2^e, e = 14 - (E - 127),
+    // and convert in place ----
+    for (int u = warp; u < nseg; u += kConsumers)
+      for (int m = 0; m < M; ++m) {
+        const int cc = u * kSegChunks + lane;
+        if (cc * 8 >= K) xs[m * xch + cc] = make_uint4(0, 0, 0, 0);
       }
-    }
-  } else {
-    const int M = p.M, K = p.K, N = p.N;
     // x (and y) may belong to the previous kernel on the stream
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    // ---- prologue 1: per-token power-of-two scale 2^e with amax * 2^e in [2^14, 2^15),
-    // so every 2^e x (and 2^e x / 16) below is an exact fp16 except negligibly small ones ----
-    if (warp < M) {
-      float a = 0.f;
-      for (int k8 = lane * 8; k8 < K; k8 += 256) {
-        const uint4 v = ld_nc_v4(p.x + (size_t)warp * K + k8);
-        a = fmaxf(a, fmaxf(fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x))), fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y)))));
-        a = fmaxf(a, fmaxf(fmaxf(fabsf(bf16_lo(v.z)), fabsf(bf16_hi(v.z))), fmaxf(fabsf(bf16_lo(v.w)), fabsf(bf16_hi(v.w)))));
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-      if (lane == 0) {
-        int e = 0;
-        if (a > 0.f) {
-          int E;
-          frexpf(a, &E);               // a = f * 2^E, f in [0.5, 1)
-          e = min(max(15 - E, -100), 100);
-        }
-        ex[warp] = __int_as_float((e + 127) << 23);          // 2^e, exactly
-        ex[kTok + warp] = __int_as_float((127 - e) << 23);   // 2^-e
+    if (lane == 0) {
+      uint32_t bytes = 0;
+      for (int u = warp; u < nseg && u * kUnitK < K; u += kConsumers)
+        bytes += M * 2 * min(kUnitK, K - u * kUnitK);
+      if (bytes > 0) {
+        mbar_arrive_expect_tx(&xbar[warp], bytes);
+        for (int u = warp; u < nseg && u * kUnitK < K; u += kConsumers)
+          for (int m = 0; m < M; ++m)
+            tc::bulk_load(xs + m * xch + u * kSegChunks, p.x + (size_t)m * K + u * kUnitK,
+                          2 * min(kUnitK, K - u * kUnitK), &xbar[warp]);
+      } else {
+        mbar_arrive(&xbar[warp]);
       }
     }
-    asm volatile("bar.sync 1, %0;" :: "n"(kConsumers * 32) : "memory");
-    // ---- prologue 2: tokens to shared memory as fp16 2^e x, each 8-chunk in the order
-    // (x0,x4) (x1/16,x5/16) (x2,x6) (x3/16,x7/16) that matches the nibble pairs; zero past K ----
-    for (int i = threadIdx.x; i < M * xch; i += kConsumers * 32) {
-      const int m = i / xch, k8 = (i % xch) * 8;
-      uint4 o = make_uint4(0, 0, 0, 0);
-      if (k8 < K) {
-        const uint4 v = ld_nc_v4(p.x + (size_t)m * K + k8);
-        const float sc = ex[m], sc16 = sc * 0.0625f;
-        o.x = pack_f16x2(bf16_lo(v.x) * sc, bf16_lo(v.z) * sc);       // (x0, x4)
-        o.y = pack_f16x2(bf16_hi(v.x) * sc16, bf16_hi(v.z) * sc16);   // (x1, x5) / 16
-        o.z = pack_f16x2(bf16_lo(v.y) * sc, bf16_lo(v.w) * sc);       // (x2, x6)
-        o.w = pack_f16x2(bf16_hi(v.y) * sc16, bf16_hi(v.w) * sc16);   // (x3, x7) / 16
+    const bool x_ok = __all_sync(0xffffffffu, tc::wait(&xbar[warp], 0, abort_flag, p.status, kWaitNs));
+    for (int u = warp; u < nseg && x_ok; u += kConsumers) {
+      const int cc = u * kSegChunks + lane;
+      for (int m = 0; m < M; ++m) {
+        const uint4 v = xs[m * xch + cc];
+        const uint32_t h = __vmaxu2(__vmaxu2(v.x & 0x7F807F80u, v.y & 0x7F807F80u),
+                                    __vmaxu2(v.z & 0x7F807F80u, v.w & 0x7F807F80u));
+        const uint32_t ef = __reduce_max_sync(0xffffffffu, max(h & 0xFFFFu, h >> 16));
+        const int e = min(max(141 - static_cast<int>(ef >> 7), -120), 100);
+        const float sc = __int_as_float((127 + e) << 23), sc16 = sc * 0.0625f;
+        uint4 o;   // (x0,x4) (x1/16,x5/16) (x2,x6) (x3/16,x7/16): the nibble pair order
+        o.x = pack_f16x2(bf16_lo(v.x) * sc, bf16_lo(v.z) * sc);
+        o.y = pack_f16x2(bf16_hi(v.x) * sc16, bf16_hi(v.z) * sc16);
+        o.z = pack_f16x2(bf16_lo(v.y) * sc, bf16_lo(v.w) * sc);
+        o.w = pack_f16x2(bf16_hi(v.y) * sc16, bf16_hi(v.w) * sc16);
+        xs[m * xch + cc] = o;
+        // 2^-24 sums of x over 64-k blocks (8 neighbouring lanes)
+        float sum = ((bf16_lo(v.x) + bf16_hi(v.x)) + (bf16_lo(v.y) + bf16_hi(v.y))) +
+                    ((bf16_lo(v.z) + bf16_hi(v.z)) + (bf16_lo(v.w) + bf16_hi(v.w)));
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+        if ((lane & 7) == 0) xsum[(u * 4 + lane / 8) * kTok + m] = sum * 5.9604644775390625e-8f;
+        if (lane == 0) exs[u * kTok + m] = __int_as_float((127 - e) << 23);   // 2^-e, exactly
       }
-      xs[i] = o;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&xrdy[u]);   // releases this warp's writes of the segment
     }
-    // ---- prologue 3: sums of 2^e x over 64-k blocks (for the -8 offset and the zeros) ----
-    for (int i = threadIdx.x; i < M * nb64; i += kConsumers * 32) {
-      const int m = i / nb64, k0 = (i % nb64) * 64;
-      float sum = 0.f;
-      for (int k8 = k0; k8 < k0 + 64 && k8 < K; k8 += 8) {
-        const uint4 v = ld_nc_v4(p.x + (size_t)m * K + k8);
-        sum += (bf16_lo(v.x) + bf16_hi(v.x)) + (bf16_lo(v.y) + bf16_hi(v.y)) + (bf16_lo(v.z) + bf16_hi(v.z)) +
-               (bf16_lo(v.w) + bf16_hi(v.w));
-      }
-      xsum[i] = sum * ex[m];
-    }
-    asm volatile("bar.sync 1, %0;" :: "n"(kConsumers * 32) : "memory");
 
+    // ---- main loop over this warp's 256-k units ----
     const int r = lane >> 2, c = lane & 3;
-    const int group = p.group;
-    for (int su = 0; su < my_strips && !*abort_flag; ++su) {
-      const int strip = blockIdx.x + su * gridDim.x;
-      const int n0 = strip * kStrip + 4 * r;   // this lane's 4 columns n0..n0+3
-      const bool n_in = n0 < N;
-      float tot[2][4];
-#pragma unroll
-      for (int j = 0; j < 2; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) tot[j][e] = 0.f;
-      bool ok = true;
-      // this warp's quarter of stages warp / 4, warp / 4 + groups, ... of the strip
-      for (int st = warp / kPerStage; st < S; st += groups) {
-        const int i = su * S + st, slot = i % R;
-        if (!tc::wait(&full[slot], (i / R) & 1, abort_flag, p.status, kWaitNs, 500)) {
-          ok = false;
-          break;
-        }
-        const uint8_t* tile = ring + slot * kStageBytes + (warp % kPerStage) * kQuarterRows * 128;
-        const int kst = st * kStageK + (warp % kPerStage) * kQuarterRows * 8;
-        const int nsteps = max(0, min(kQuarterRows / 4, (K - kst) / 32));
-        const uint4* xrow = xs + r * xch + kst / 8;
-        // segments: the part of one scale group inside this quarter (even step counts)
-        for (int t0 = 0; t0 < nsteps;) {
-          const int g = (kst + t0 * 32) / group;
-          const int t1 = min(nsteps, ((g + 1) * group - kst) / 32);
-          float acc[4][4];   // [tile * 2 + k half]: four independent MMA chains
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
-          const uint2 sv = ld4x16(p.sc + (size_t)g * N + n0, n_in);
-          uint2 zv = make_uint2(0, 0);
-          if (kZero) zv = ld4x16(p.zr + (size_t)g * N + n0, n_in);
-          for (int t = t0; t < t1; ++t) {
-            const int kb = 8 * (t >> 1) + 2 * c + (t & 1);      // word row inside the quarter
-            const uint4 w = *reinterpret_cast<const uint4*>(tile + kb * 128 + ((r ^ (kb & 7)) << 4));
-            const uint4 xv = (r < M) ? xrow[kb] : make_uint4(0, 0, 0, 0);
-            // nibble pairs as fp16 subnormals: (i, i+4) at bits 0-3 -> q 2^-24,
-            // at bits 4-7 -> 16 q 2^-24 (its activations carry the 1/16)
-            const uint32_t xh = w.x >> 8, yh = w.y >> 8, zh = w.z >> 8, wh = w.w >> 8;
-            // tile 0: rows r <-> n0, r+8 <-> n0+1; tile 1: rows r <-> n0+2, r+8 <-> n0+3
-            mma_f16(acc[0], w.x & 0x000F000Fu, w.y & 0x000F000Fu, w.x & 0x00F000F0u, w.y & 0x00F000F0u, xv.x, xv.y);
-            mma_f16(acc[1], xh & 0x000F000Fu, yh & 0x000F000Fu, xh & 0x00F000F0u, yh & 0x00F000F0u, xv.z, xv.w);
-            mma_f16(acc[2], w.z & 0x000F000Fu, w.w & 0x000F000Fu, w.z & 0x00F000F0u, w.w & 0x00F000F0u, xv.x, xv.y);
-            mma_f16(acc[3], zh & 0x000F000Fu, wh & 0x000F000Fu, zh & 0x00F000F0u, wh & 0x00F000F0u, xv.z, xv.w);
-          }
-          // fold: sum_k x (q - 8) = 2^24 acc - 8 sum(x) (all in units of 2^e x);
-          // tot += s * that + z * sum(x)
-          float x0 = 0.f, x1 = 0.f;
-          for (int b = (kst + t0 * 32) / 64; b < (kst + t1 * 32) / 64; ++b) {
-            if (2 * c < M) x0 += xsum[(2 * c) * nb64 + b];
-            if (2 * c + 1 < M) x1 += xsum[(2 * c + 1) * nb64 + b];
-          }
-          const uint32_t sb[4] = {sv.x & 0xFFFFu, sv.x >> 16, sv.y & 0xFFFFu, sv.y >> 16};
-          const uint32_t zb[4] = {zv.x & 0xFFFFu, zv.x >> 16, zv.y & 0xFFFFu, zv.y >> 16};
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const float s_lo = scale_at<kScaleBf16>(sb[2 * j]), s_hi = scale_at<kScaleBf16>(sb[2 * j + 1]);
-            const float z_lo = kZero ? __uint_as_float(zb[2 * j] << 16) : 0.f;
-            const float z_hi = kZero ? __uint_as_float(zb[2 * j + 1] << 16) : 0.f;
-            const float a_lo = s_lo * 16777216.f, a_hi = s_hi * 16777216.f;   // s * 2^24
-            const float b_lo = fmaf(-8.f, s_lo, z_lo), b_hi = fmaf(-8.f, s_hi, z_hi);
-            const float* p0 = acc[2 * j];
-            const float* p1 = acc[2 * j + 1];
-            tot[j][0] = fmaf(a_lo, p0[0] + p1[0], fmaf(b_lo, x0, tot[j][0]));
-            tot[j][1] = fmaf(a_lo, p0[1] + p1[1], fmaf(b_lo, x1, tot[j][1]));
-            tot[j][2] = fmaf(a_hi, p0[2] + p1[2], fmaf(b_hi, x0, tot[j][2]));
-            tot[j][3] = fmaf(a_hi, p0[3] + p1[3], fmaf(b_hi, x1, tot[j][3]));
-          }
-          t0 = t1;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);   // this quarter of the tile consumed
-      }
-      if (!ok || warp >= act) continue;
-      // hand the partial to the reduction; warp 0 finishes the strip
-      const int rb = su & 1;
-      if (!tc::wait(&red_empty[rb], ((su >> 1) & 1) ^ 1, abort_flag, p.status, kWaitNs)) break;
-      float* dst = red + (rb * kConsumers + warp) * red_n;
+    const int units = kUnitsPerStage * S;                // per strip
+    const int total_units = x_ok ? my_strips * units : 0;
+    // lane offsets of the two word rows a step reads (even / odd step), swizzled
+    const int w_off_e = (2 * c) * 128 + ((r ^ (2 * c)) << 4);
+    const int w_off_o = (2 * c + 1) * 128 + ((r ^ (2 * c + 1)) << 4);
+    const uint4* xrow = xs + min(r, M - 1) * xch;        // tokens past M: any finite data, discarded
+    float tot[2][4];
+    int cur = -1;                                        // strip whose partial tot holds
+    bool ok = true;
+    auto flush = [&](int su) {
+      float* dst = red + (su * kConsumers + warp) * M * kStrip;
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         const int nl = 4 * r + 2 * j;
@@ -321,23 +318,156 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_kernel(const __grid_constan
           dst[(2 * c + 1) * kStrip + nl + 1] = tot[j][3];
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&red_full[rb]);
-      if (warp == 0) {
-        if (!tc::wait(&red_full[rb], (su >> 1) & 1, abort_flag, p.status, kWaitNs)) break;
-        const float* src = red + rb * kConsumers * red_n;
-        for (int o = lane; o < red_n; o += 32) {
-          const int m = o / kStrip, n = strip * kStrip + o % kStrip;
-          float v = 0.f;
-          for (int w = 0; w < act; ++w) v += src[w * red_n + o];   // fixed order
-          if (n < N) {
-            v *= ex[kTok + m];                                     // undo 2^e (exact)
-            if (kBias) v += __uint_as_float(static_cast<uint32_t>(p.bias[n]) << 16);
-            p.y[(size_t)m * N + n] = static_cast<uint16_t>(f32_to_bf16_bits(v));
+    };
+    // unit v is unit u of strip su (v = su * units + u); kept incrementally
+    int su = warp / units, u = warp % units;
+    for (int v = warp; v < total_units; v += kConsumers, u += kConsumers) {
+      while (u >= units) {
+        u -= units;
+        ++su;
+      }
+      const int st = u / kUnitsPerStage, qu = u % kUnitsPerStage;
+      if (su != cur) {
+        if (cur >= 0) flush(cur);
+        cur = su;
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) tot[j][e] = 0.f;
+      }
+      const int i = su * S + st, slot = i & (R - 1), phase = (i >> p.ring_shift) & 1;
+      const int kunit = st * kStageK + qu * kUnitK;
+      const int seg = u;                                   // kunit / 256
+      const int nsteps = min(kUnitRows / 4, max(0, (K - kunit) / 32));   // even: K % 64 == 0
+      if (!tc::wait(&xrdy[seg], 0, abort_flag, p.status, kWaitNs) ||
+          !tc::wait(&full[slot], phase, abort_flag, p.status, kWaitNs, 500)) {
+        ok = false;
+        break;
+      }
+      if (nsteps > 0) {
+        const uint8_t* wbase = ring + slot * kStageBytes + qu * (kUnitRows * 128);
+        const uint8_t* we = wbase + w_off_e;
+        const uint8_t* wo = wbase + w_off_o;
+        const uint4* xe = xrow + kunit / 8 + 2 * c;
+        const uint4* xo = xe + 1;
+        const float* xb = xsum + (kunit / 64) * kTok + 2 * c;
+        const float2 f = *reinterpret_cast<const float2*>(exs + seg * kTok + 2 * c);   // 2^-e, tokens 2c, 2c+1
+        // scale rows of the slot: this unit's first group is row kunit / group - gst
+        const uint8_t* sbase = scl + slot * p.scb + 8 * r;
+        const int row0 = kSPF == 2   ? 4 * qu
+                         : kSPF == 4 ? 2 * qu
+                         : p.group_shift >= 0 ? (kunit >> p.group_shift) - ((st * kStageK) >> p.group_shift)
+                                              : kunit / group - st * kStageK / group;
+        // steps that end a scale group (or the unit's k range) fold the partial
+        uint32_t fold_mask = 0;
+        if (kSPF == 0) {
+          fold_mask = 1u << (nsteps - 1);
+          for (int t = (group - kunit % group) / 32 - 1; t < nsteps - 1; t += group / 32) fold_mask |= 1u << t;
+        }
+        float acc[4][4];   // [tile * 2 + nibble half]: four independent MMA chains
+        if (kSPF == 0) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
+        }
+        float X0 = 0.f, X1 = 0.f;
+        int gseg = 0;
+        // tot += s 2^-e acc + (z - 8 s) X for the scale group that just ended;
+        // with fixed fold points the row is clamped into the slot's scale area
+        // (past K it meets only zero products)
+        auto fold = [&](int row) {
+          const uint2 sv = *reinterpret_cast<const uint2*>(sbase + row * (kStrip * 2));
+          const uint2 zv = kZero ? *reinterpret_cast<const uint2*>(sbase + p.zoff + row * (kStrip * 2))
+                                 : make_uint2(0, 0);
+          const uint32_t sb[4] = {sv.x & 0xFFFFu, sv.x >> 16, sv.y & 0xFFFFu, sv.y >> 16};
+          const uint32_t zb[4] = {zv.x & 0xFFFFu, zv.x >> 16, zv.y & 0xFFFFu, zv.y >> 16};
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const float s_lo = kScaleBf16 ? __uint_as_float(sb[2 * j] << 16) : half_bits_to_f32(sb[2 * j]);
+            const float s_hi = kScaleBf16 ? __uint_as_float(sb[2 * j + 1] << 16) : half_bits_to_f32(sb[2 * j + 1]);
+            const float z_lo = kZero ? __uint_as_float(zb[2 * j] << 16) : 0.f;
+            const float z_hi = kZero ? __uint_as_float(zb[2 * j + 1] << 16) : 0.f;
+            const float b_lo = fmaf(-8.f, s_lo, z_lo), b_hi = fmaf(-8.f, s_hi, z_hi);
+            const float s0 = s_lo * f.x, s1 = s_lo * f.y, s2 = s_hi * f.x, s3 = s_hi * f.y;
+            const float* p0 = acc[2 * j];
+            const float* p1 = acc[2 * j + 1];
+            tot[j][0] = fmaf(s0, p0[0], fmaf(s0, p1[0], fmaf(b_lo, X0, tot[j][0])));
+            tot[j][1] = fmaf(s1, p0[1], fmaf(s1, p1[1], fmaf(b_lo, X1, tot[j][1])));
+            tot[j][2] = fmaf(s2, p0[2], fmaf(s2, p1[2], fmaf(b_hi, X0, tot[j][2])));
+            tot[j][3] = fmaf(s3, p0[3], fmaf(s3, p1[3], fmaf(b_hi, X1, tot[j][3])));
+          }
+          X0 = X1 = 0.f;
+        };
+#pragma unroll
+        for (int t = 0; t < kUnitRows / 4; ++t) {
+          const uint4 w = *reinterpret_cast<const uint4*>((t & 1 ? wo : we) + (t >> 1) * 1024);
+          const uint4 xv = (t & 1 ? xo : xe)[(t >> 1) * 8];
+          // nibble pairs as fp16 subnormals: (i, i+4) at bits 0-3 -> q 2^-24,
+          // at bits 4-7 -> 16 q 2^-24 (its activations carry the 1/16)
+          const uint32_t xh = w.x >> 8, yh = w.y >> 8, zh = w.z >> 8, wh = w.w >> 8;
+          // tile 0: rows r <-> n0, r+8 <-> n0+1; tile 1: rows r <-> n0+2, r+8 <-> n0+3
+          if (kSPF != 0 && t % (kSPF > 0 ? kSPF : 1) == 0) {   // a scale group starts: fresh accumulators
+            mma_f16_first(acc[0], w.x & 0x000F000Fu, w.y & 0x000F000Fu, w.x & 0x00F000F0u, w.y & 0x00F000F0u, xv.x, xv.y);
+            mma_f16_first(acc[1], xh & 0x000F000Fu, yh & 0x000F000Fu, xh & 0x00F000F0u, yh & 0x00F000F0u, xv.z, xv.w);
+            mma_f16_first(acc[2], w.z & 0x000F000Fu, w.w & 0x000F000Fu, w.z & 0x00F000F0u, w.w & 0x00F000F0u, xv.x, xv.y);
+            mma_f16_first(acc[3], zh & 0x000F000Fu, wh & 0x000F000Fu, zh & 0x00F000F0u, wh & 0x00F000F0u, xv.z, xv.w);
+          } else {
+            mma_f16(acc[0], w.x & 0x000F000Fu, w.y & 0x000F000Fu, w.x & 0x00F000F0u, w.y & 0x00F000F0u, xv.x, xv.y);
+            mma_f16(acc[1], xh & 0x000F000Fu, yh & 0x000F000Fu, xh & 0x00F000F0u, yh & 0x00F000F0u, xv.z, xv.w);
+            mma_f16(acc[2], w.z & 0x000F000Fu, w.w & 0x000F000Fu, w.z & 0x00F000F0u, w.w & 0x00F000F0u, xv.x, xv.y);
+            mma_f16(acc[3], zh & 0x000F000Fu, wh & 0x000F000Fu, zh & 0x00F000F0u, wh & 0x00F000F0u, xv.z, xv.w);
+          }
+          if (t & 1) {
+            // a 64-k block ends: add its x sums (tokens 2c, 2c+1)
+            const float2 bs = *reinterpret_cast<const float2*>(xb + (t >> 1) * kTok);
+            X0 += bs.x;
+            X1 += bs.y;
+            if (kSPF != 0) {
+              if (t % (kSPF > 0 ? kSPF : 1) == kSPF - 1) fold(min(row0 + t / (kSPF > 0 ? kSPF : 1), p.gh - 1));
+            } else if (fold_mask & (1u << t)) {
+              fold(row0 + gseg);
+              ++gseg;
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
+            }
           }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&red_empty[rb]);
+      }
+      // this unit of the tile is consumed; the warp that finishes the stage's
+      // last unit refills the slot with stage i + R (the counter only grows:
+      // the last of the four units of round i / R reads 4 (i / R) + 3)
+      __syncwarp();
+      if (lane == 0) {
+        asm volatile("fence.acq_rel.cta;" ::: "memory");
+        const unsigned int before = atomicAdd(&done[slot], 1u);
+        if (before == kUnitsPerStage * static_cast<unsigned int>(i >> p.ring_shift) + kUnitsPerStage - 1 &&
+            i + R < total) {
+          asm volatile("fence.acq_rel.cta;" ::: "memory");
+          tc::fence_proxy_async_smem();   // the warps' reads of the slot before the copy that overwrites it
+          issue(i + R);
+        }
+      }
+    }
+    if (ok && cur >= 0) flush(cur);
+    __syncthreads();
+    if (!*abort_flag) {
+      // ---- sum the strip partials of the warps that worked on each strip in
+      // a fixed order, scale back, add the bias, write y ----
+      const int nout = my_strips * M * kStrip;
+      for (int o = threadIdx.x; o < nout; o += kConsumers * 32) {
+        const int su = o / (M * kStrip), m = (o / kStrip) % M, nl = o % kStrip;
+        const int n = (blockIdx.x + su * gridDim.x) * kStrip + nl;
+        const int v0 = su * units, v1 = v0 + min(units, kConsumers);
+        float s = 0.f;
+        for (int vv = v0; vv < v1; ++vv) s += red[((su * kConsumers + vv % kConsumers) * M + m) * kStrip + nl];
+        if (n < p.N) {
+          s *= 16777216.f;                                       // undo 2^-24 (exact)
+          if (p.bias != nullptr) s += __uint_as_float(static_cast<uint32_t>(p.bias[n]) << 16);
+          p.y[(size_t)m * p.N + n] = static_cast<uint16_t>(f32_to_bf16_bits(s));
+        }
       }
     }
   }
@@ -363,24 +493,56 @@ using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, 
                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-cudaError_t encode_weights(CUtensorMap* m, const void* qweight, int64_t N, int64_t K) {
+EncodeTiled encoder(cudaError_t* err) {
   static EncodeTiled fn = nullptr;
   if (fn == nullptr) {
     void* f = nullptr;
     cudaDriverEntryPointQueryResult q;
-    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q);
-    if (e != cudaSuccess) return e;
-    if (q != cudaDriverEntryPointSuccess || f == nullptr) return cudaErrorNotSupported;
+    *err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q);
+    if (*err != cudaSuccess) return nullptr;
+    if (q != cudaDriverEntryPointSuccess || f == nullptr) {
+      *err = cudaErrorNotSupported;
+      return nullptr;
+    }
     fn = reinterpret_cast<EncodeTiled>(f);
   }
-  const cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)(K / 8)};
-  const cuuint64_t strides[1] = {(cuuint64_t)N * 4};
-  const cuuint32_t box[2] = {kStrip, kStageRows};
+  *err = cudaSuccess;
+  return fn;
+}
+
+// A row-major [rows, N] matrix of `esize`-byte elements, read as tiles of
+// 32 columns x box_rows rows (swizzled for the weight words).
+cudaError_t encode_rows(CUtensorMap* m, const void* base, int64_t N, int64_t rows, int esize, int box_rows,
+                        bool swizzle) {
+  cudaError_t e;
+  EncodeTiled fn = encoder(&e);
+  if (fn == nullptr) return e;
+  const cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)N * esize};
+  const cuuint32_t box[2] = {kStrip, (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, const_cast<void*>(qweight), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = fn(m, esize == 4 ? CU_TENSOR_MAP_DATA_TYPE_INT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// The most scale groups the k range of one stage meets.
+int group_rows(int K, int group) {
+  int h = 1;
+  for (int k0 = 0; k0 < K; k0 += kStageK) {
+    const int k1 = (k0 + kStageK < K ? k0 + kStageK : K) - 1;
+    if (k1 / group - k0 / group + 1 > h) h = k1 / group - k0 / group + 1;
+  }
+  return h;
+}
+
+// Bytes of one slot's scale area: gh rows of 32 scales, then as many zeros.
+int scale_area(int gh, bool zeros, int* zoff) {
+  const int rows = (gh * kStrip * 2 + 127) & ~127;
+  *zoff = rows;
+  return zeros ? 2 * rows : rows;
 }
 
 int x_stride(int K) {
@@ -388,46 +550,69 @@ int x_stride(int K) {
   return stages * kStageK + 8;   // +16 bytes: token rows start in different banks
 }
 
-size_t smem_bytes(int K, int rows, int ring) {
+size_t smem_bytes(int K, int rows, int ring, int scb, int pstrips) {
   const int stages = (K + kStageK - 1) / kStageK;
-  return 1024 + static_cast<size_t>(Layout(stages * (kStageK / 64), x_stride(K) / 8, rows, ring).total);
+  return 1024 + static_cast<size_t>(
+                    Layout(stages * (kStageK / kUnitK), x_stride(K) / 8, rows, ring, scb, pstrips).total);
 }
 constexpr size_t kSmemMax = 227 * 1024;
 
-template <bool kScaleBf16, bool kZero, bool kBias>
-cudaError_t launch_t(const Params& p, int grid, size_t smem, cudaStream_t s) {
-  auto k = w4a16_kernel<kScaleBf16, kZero, kBias>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  // programmatic dependent launch: this grid may start while the previous
-  // kernel on the stream finishes; it waits for it before reading x
+cudaLaunchConfig_t pdl_config(int grid, int block, size_t smem, cudaStream_t s, cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(block);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  // programmatic dependent launch: the grid may start while the previous
+  // kernel on the stream finishes; it waits for it before reading x
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  return cfg;
+}
+
+template <bool kScaleBf16, bool kZero, int kSPF>
+cudaError_t launch_t(const Params& p, int grid, size_t smem, cudaStream_t s) {
+  auto k = w4a16_kernel<kScaleBf16, kZero, kSPF>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg = pdl_config(grid, kThreads, smem, s, attr);
   return cudaLaunchKernelEx(&cfg, k, p);
+}
+
+template <bool kScaleBf16>
+cudaError_t launch_spf(const Params& p, bool z, int spf, int grid, size_t smem, cudaStream_t s) {
+  switch (spf) {
+    case 2: return z ? launch_t<kScaleBf16, true, 2>(p, grid, smem, s) : launch_t<kScaleBf16, false, 2>(p, grid, smem, s);
+    case 4: return z ? launch_t<kScaleBf16, true, 4>(p, grid, smem, s) : launch_t<kScaleBf16, false, 4>(p, grid, smem, s);
+    case 8: return z ? launch_t<kScaleBf16, true, 8>(p, grid, smem, s) : launch_t<kScaleBf16, false, 8>(p, grid, smem, s);
+    default: return z ? launch_t<kScaleBf16, true, 0>(p, grid, smem, s) : launch_t<kScaleBf16, false, 0>(p, grid, smem, s);
+  }
 }
 
 }  // namespace
 
-size_t w4a16_smem_bytes(int64_t K, int32_t group) {
-  (void)group;
-  return smem_bytes(static_cast<int>(K), 1, 2);
+size_t w4a16_smem_bytes(int64_t N, int64_t K, int32_t group) {
+  int zoff;
+  const int scb = scale_area(group_rows(static_cast<int>(K), group), true, &zoff);
+  const int64_t strips = (N + kStrip - 1) / kStrip;
+  const int64_t grid = strips < sm_count() ? strips : sm_count();
+  const int pstrips = static_cast<int>((strips + grid - 1) / (grid > 0 ? grid : 1));
+  return smem_bytes(static_cast<int>(K), 1, 4, scb, pstrips);
 }
 
 cudaError_t launch_w4a16(const W4A16Args& a, cudaStream_t s) {
   Params p;
   memset(&p, 0, sizeof(p));
-  cudaError_t e = encode_weights(&p.tm_w, a.qweight, a.N, a.K);
+  const int G = static_cast<int>(a.K / a.group);
+  p.gh = group_rows(static_cast<int>(a.K), a.group);
+  p.scb = scale_area(p.gh, a.zeros != nullptr, &p.zoff);
+  cudaError_t e = encode_rows(&p.tm_w, a.qweight, a.N, a.K / 8, 4, kStageRows, true);
+  if (e == cudaSuccess) e = encode_rows(&p.tm_s, a.w_scale, a.N, G, 2, p.gh, false);
+  if (e == cudaSuccess && a.zeros != nullptr) e = encode_rows(&p.tm_z, a.zeros, a.N, G, 2, p.gh, false);
   if (e != cudaSuccess) return e;
-  p.sc = static_cast<const uint16_t*>(a.w_scale);
-  p.zr = static_cast<const uint16_t*>(a.zeros);
   p.bias = static_cast<const uint16_t*>(a.bias);
   p.N = static_cast<int>(a.N);
   p.K = static_cast<int>(a.K);
@@ -435,28 +620,40 @@ cudaError_t launch_w4a16(const W4A16Args& a, cudaStream_t s) {
   p.strips = (p.N + kStrip - 1) / kStrip;
   p.stages = (p.K + kStageK - 1) / kStageK;
   p.xstride = x_stride(p.K);
+  p.group_shift = -1;
+  for (int sh = 0; sh < 31; ++sh)
+    if (p.group == (1 << sh)) p.group_shift = sh;
   p.status = a.status;
-  // tokens in blocks of up to 8 beside a ring of at least 4 stages (deeper
-  // when it fits); each block is one pass over the weights
-  int block = kTok;
-  while (block > 1 && smem_bytes(p.K, block, 4) > kSmemMax) --block;
-  if (smem_bytes(p.K, block, 2) > kSmemMax) return cudaErrorInvalidValue;
   const int grid = p.strips < sm_count() ? p.strips : sm_count();
-  const bool bf = a.scale_bf16, z = a.zeros != nullptr, b = a.bias != nullptr;
+  p.pstrips = (p.strips + grid - 1) / grid;
+  auto bytes = [&](int rows, int ring) { return smem_bytes(p.K, rows, ring, p.scb, p.pstrips); };
+  // Tokens go in blocks of up to 8, each block one pass over the weights,
+  // beside a ring of 8 stages when it fits, else 4.
+  int block = kTok;
+  while (block > 1 && bytes(block, 4) > kSmemMax) --block;
+  if (bytes(block, 4) > kSmemMax) return cudaErrorInvalidValue;
+  const bool z = a.zeros != nullptr;
+  // fixed fold points for the common group sizes
+  const int spf = p.group == 64 ? 2 : p.group == 128 ? 4 : p.group % 256 == 0 ? 8 : 0;
+  {
+    // this call's weights, scales and zeros on their way into L2 while the
+    // kernel before it on the stream still runs
+    const size_t wb = static_cast<size_t>(a.K / 8) * a.N * 4, sb = static_cast<size_t>(G) * a.N * 2;
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = pdl_config(sm_count(), 32, 0, s, attr);
+    e = cudaLaunchKernelEx(&cfg, w4a16_prefetch_kernel, static_cast<const uint8_t*>(a.qweight), wb,
+                           static_cast<const uint8_t*>(a.w_scale), sb, static_cast<const uint8_t*>(a.zeros),
+                           z ? sb : size_t(0));
+    if (e != cudaSuccess) return e;
+  }
   for (int64_t m0 = 0; m0 < a.M; m0 += block) {
     p.x = static_cast<const uint16_t*>(a.x) + m0 * a.K;
     p.y = static_cast<uint16_t*>(a.y) + m0 * a.N;
     p.M = static_cast<int>(a.M - m0 < block ? a.M - m0 : block);
-    p.ring = kRingMax;
-    while (p.ring > 2 && smem_bytes(p.K, p.M, p.ring) > kSmemMax) --p.ring;
-    const size_t smem = smem_bytes(p.K, p.M, p.ring);
-    if (bf) {
-      if (z) e = b ? launch_t<true, true, true>(p, grid, smem, s) : launch_t<true, true, false>(p, grid, smem, s);
-      else e = b ? launch_t<true, false, true>(p, grid, smem, s) : launch_t<true, false, false>(p, grid, smem, s);
-    } else {
-      if (z) e = b ? launch_t<false, true, true>(p, grid, smem, s) : launch_t<false, true, false>(p, grid, smem, s);
-      else e = b ? launch_t<false, false, true>(p, grid, smem, s) : launch_t<false, false, false>(p, grid, smem, s);
-    }
+    p.ring = bytes(p.M, 8) <= kSmemMax ? 8 : 4;
+    p.ring_shift = p.ring == 8 ? 3 : 2;
+    const size_t smem = bytes(p.M, p.ring);
+    e = a.scale_bf16 ? launch_spf<true>(p, z, spf, grid, smem, s) : launch_spf<false>(p, z, spf, grid, smem, s);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

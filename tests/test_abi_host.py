@@ -100,6 +100,8 @@ def test_w4a16_validation(lib):
     assert call(group=3) == w4.W4_ERR_GROUP
     assert call(x=None) == w4.W4_ERR_NULL
     assert call(qw=ODD) == w4.W4_ERR_ALIGN
+    assert call(ws=ctypes.c_void_p((1 << 20) + 8)) == w4.W4_ERR_ALIGN   # scales and zeros arrive by TMA
+    assert call(z=ctypes.c_void_p((1 << 20) + 8)) == w4.W4_ERR_ALIGN
     assert call(M=0) == w4.W4_OK
 
 
