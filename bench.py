@@ -52,7 +52,11 @@ GRAPH_CALLS = 200
 
 # DRAM bytes (read + write) per launch from ncu, keyed by the SHA-256 of the
 # kernel's source file at capture time; reported only while the source matches.
-TRAFFIC = {}
+TRAFFIC = {
+    # w4a16_kernel, M=1 K=4096 N=14336 g128: dram__bytes_read.sum + dram__bytes_write.sum
+    # (30,337,280 + 0), profiles/w4a16_kernel_m1_k4096_n14336_full.md
+    "w4a16": (30337280, "c7e94205b1369c60"),
+}
 
 
 def _sha(path):
@@ -249,7 +253,7 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": DEC_M * DEC_K * 2,
                 "d2h_bytes_per_step": DEC_M * DEC_N * 2, "steps": e2e_steps,
                 "how": "per step: pinned H2D of x, w4a16_gemm, D2H of y; host wall clock"},
-        "gpu_launches": steps,
+        "gpu_launches": 2 * steps,   # per call: the L2 prefetch grid and the GEMV grid
         "clocks": clk.summary(),
         "sm_count": torch.cuda.get_device_properties(dev).multi_processor_count,
     }
