@@ -106,3 +106,37 @@ def test_w4a16_output_guard():
     w4.w4a16_gemm(bf16(xb), to_dev(S.random_words((K // 8, N))), to_dev(S.scales_f16((2, N))), 128, y=y)
     torch.cuda.synchronize()
     assert torch.all(buf[:128] == -7.0) and torch.all(buf[128 + M * N:] == -7.0)
+
+
+def test_w4a16_back_to_back_chain_reads_previous_output():
+    """Back-to-back calls on one stream where each call's x is the previous
+    call's y (K == N): every call must read the finished output of the call
+    before it, although the calls overlap through programmatic dependent
+    launch. Each y_i is checked against the oracle applied to the GPU's
+    y_{i-1}; the output buffers start out holding a constant, so a call that
+    read its input early would disagree."""
+    M, K, g, steps = 2, 4096, 128, 6
+    N = K
+    x0 = S.activations_bf16(M, K, seed=21)
+    qws = [S.random_words((K // 8, N), seed=40 + i) for i in range(steps)]
+    # scales chosen so the activations keep a similar magnitude from call to call
+    sws = [S.scales_f16((K // g, N), lo=0.003, hi=0.004, seed=60 + i) for i in range(steps)]
+    ys = [torch.full((M, N), 3.0, dtype=torch.bfloat16, device="cuda") for _ in range(steps)]
+    qws_d = [to_dev(q) for q in qws]
+    sws_d = [to_dev(s_) for s_ in sws]
+    x_d = bf16(x0)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        inp = x_d
+        for i in range(steps):
+            w4.w4a16_gemm(inp, qws_d[i], sws_d[i], g, y=ys[i], stream=s)
+            inp = ys[i]
+    s.synchronize()
+    prev = x0
+    for i in range(steps):
+        yb = bits(ys[i])
+        r = np.concatenate([O.w4a16_linear(prev, qws[i][:, c:c + 1024], sws[i][:, c:c + 1024], g)
+                            for c in range(0, N, 1024)], axis=1)
+        check_bf16_output(yb, r, f"chain step {i}")
+        prev = yb
