@@ -258,7 +258,7 @@ def run_ours(args, rank, world, local_rank):
         "sm_count": torch.cuda.get_device_properties(dev).multi_processor_count,
     }
     if not args.no_rows:
-        line["rows"] = bench_rows(dev, stream, bf16_tf, peak_kind)
+        line["rows"] = bench_rows(dev, stream, bf16_tf, peak_kind, hbm)
     return line
 
 
@@ -288,7 +288,7 @@ def _time_graph(torch, stream, fn, calls, replays, warmup=3):
     return e0.elapsed_time(e1) / (calls * replays)
 
 
-def bench_rows(dev, stream, bf16_tf, peak_kind):
+def bench_rows(dev, stream, bf16_tf, peak_kind, hbm_peak):
     import torch
     import int4_weight_quantized_w4_gb300 as w4
 
@@ -386,6 +386,34 @@ def bench_rows(dev, stream, bf16_tf, peak_kind):
                      "peak_source": f"{peak_kind} bf16_tflops (e4m3 activations widened to exact fp16; "
                                     "fp16 tensor datapath)",
                      "kernel": "w4afp8_moe_grouped_gemm call = widen_kernel + w4a8_tc_kernel"},
+    }
+    # weight-side tools (load time): the group quantizer on a 14336 x 4096 bf16
+    # weight, and the XOR 0x88 repack of a 64-expert [E, N, K/2] int4 tensor
+    Nq, Kq, gq = 14336, 4096, 128
+    blk = S.to_bf16_bits(S.normal(0, 90, 1024 * Kq).reshape(1024, Kq) * 0.05)
+    wq = bf16(np.tile(blk, (Nq // 1024, 1)))
+    pk = torch.empty((Nq, Kq // 2), dtype=torch.uint8, device=dev)
+    sq = torch.empty((Nq, Kq // gq), dtype=torch.float32, device=dev)
+    zq = torch.empty((Nq, Kq // gq), dtype=torch.float32, device=dev)
+    t_q = _time_graph(torch, stream, lambda: w4.w4_quantize_groupwise(wq, gq, pk, sq, zq, stream=stream), 5, 10)
+    qbytes = Nq * Kq * 2 + Nq * Kq // 2 + 2 * Nq * (Kq // gq) * 4
+    rows["weight_quantize_groupwise"] = {
+        "config": {"N": Nq, "K": Kq, "group": gq, "w": "bf16"}, "value": round(qbytes / (t_q * 1e-3) / 1e9, 1),
+        "unit": "GB/s", "ms_per_step": t_q,
+        "roofline": {"bound": "hbm", "achieved": round(qbytes / (t_q * 1e-3) / 1e9, 1), "peak": hbm_peak,
+                     "unit": "GB/s", "frac": round(qbytes / (t_q * 1e-3) / 1e9 / hbm_peak, 4), "traffic": None,
+                     "kernel": "quantize_groupwise_kernel", "algorithmic_bytes_per_launch": qbytes},
+    }
+    rb = 64 * 2816 * 1024
+    s4 = on((S.raw_u64(8, 80, rb // 8).view(np.uint8)))
+    s4o = torch.empty_like(s4)
+    t_r = _time_graph(torch, stream, lambda: w4.w4_repack_s4_to_uint4b8(s4, s4o, stream=stream), 5, 10)
+    rows["s4_repack_uint4b8"] = {
+        "config": {"bytes": rb, "layout": "[64, 2816, 1024] int8 -> int32 [64, 2816, 256]"},
+        "value": round(2 * rb / (t_r * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": t_r,
+        "roofline": {"bound": "hbm", "achieved": round(2 * rb / (t_r * 1e-3) / 1e9, 1), "peak": hbm_peak,
+                     "unit": "GB/s", "frac": round(2 * rb / (t_r * 1e-3) / 1e9 / hbm_peak, 4), "traffic": None,
+                     "kernel": "xor88_kernel", "algorithmic_bytes_per_launch": 2 * rb},
     }
     return rows
 

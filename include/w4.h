@@ -214,6 +214,39 @@ w4_status w4afp8_moe_grouped_gemm(const void* qx, const float* x_scale, const in
                                   int64_t R, int64_t N, int64_t K,
                                   void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Weight-side tools (load time, not on the per-token path).
+ *
+ * w4_quantize_groupwise: the asymmetric min/max 4-bit group quantizer of
+ * [OMNI] quantize_groupwise. For each row n of w [N, K] (bf16 or fp16,
+ * w_dtype W4_BF16 / W4_FP16) and each group of `group` consecutive columns
+ * (group -1 = K), in fp32 with IEEE rounding at every step:
+ *     scale = max(max - min, 1e-9) / 15,   zero = min + 8 * scale,
+ *     q = clamp(round_half_even((w - min) / scale), 0, 15),
+ * so that (q - 8) * scale + zero reproduces the group's extremes. Outputs, all
+ * caller-owned device memory:
+ *     packed [N, K/2] uint8, two codes per byte, low nibble first
+ *            ([OMNI] pack_nibbles: byte j = q[2j] | q[2j+1] << 4)
+ *     scale  [N, K/group] float32
+ *     zero   [N, K/group] float32
+ * Codes, scales and zeros are bit-exact. Requires K and the group even
+ * (W4_ERR_UNSUPPORTED otherwise), the group to divide K (W4_ERR_GROUP), w
+ * 4-byte aligned (W4_ERR_ALIGN). N == 0 does nothing. NaN/Inf in w are out of
+ * contract.
+ */
+w4_status w4_quantize_groupwise(const void* w, int32_t w_dtype, int64_t N, int64_t K, int32_t group,
+                                void* packed, float* scale, float* zero, void* stream);
+
+/*
+ * w4_repack_s4_to_uint4b8: [FP8] _repack_signed_int4_to_uint4b8. Every byte
+ * of `src` holds two signed int4 values; the output byte holds the same two
+ * values as uint4b8 codes (value + 8, so the weight is q - 8), which is XOR
+ * 0x88 on the byte. Read as int32, 8 codes per word in the same nibble order.
+ * n_bytes may be any size; src and dst must be 16-byte aligned and may be the
+ * same buffer (in place); both are caller-owned device memory. Bit-exact.
+ */
+w4_status w4_repack_s4_to_uint4b8(const void* src, void* dst, int64_t n_bytes, void* stream);
+
 /* Message for the last non-OK status returned to the calling thread ("" if none). */
 const char* w4_last_error(void);
 

@@ -17,7 +17,8 @@ import torch
 __all__ = [
     "W4Error", "load", "library_path",
     "w4_quant_act_per_token", "w4a8_gemm", "w4a8_gemm_noalloc", "w4a8_group_partials", "w4a16_gemm",
-    "w4afp8_moe_grouped_gemm", "w4_device_status", "w4_selftest_bounded_wait",
+    "w4afp8_moe_grouped_gemm", "w4_quantize_groupwise", "w4_repack_s4_to_uint4b8",
+    "w4_device_status", "w4_selftest_bounded_wait",
     "W4_OK", "W4_ERR_NULL", "W4_ERR_ALIGN", "W4_ERR_GROUP", "W4_ERR_DTYPE",
     "W4_ERR_UNSUPPORTED", "W4_ERR_SHAPE", "W4_ERR_CUDA", "W4_ERR_TIMEOUT", "W4_ERR_WORKSPACE",
     "W4_OP_W4A8", "W4_OP_W4AFP8_MOE", "w4_workspace_bytes", "EXPORTED_SYMBOLS",
@@ -41,6 +42,8 @@ _SIGNATURES = {
     "w4a8_gemm_noalloc": (_I32, [_P, _P, _P, _P, _I32, _I32, _P, _P, _I64, _I64, _I64, _P]),
     "w4a16_gemm": (_I32, [_P, _P, _P, _I32, _P, _I32, _P, _P, _I64, _I64, _I64, _P]),
     "w4afp8_moe_grouped_gemm": (_I32, [_P, _P, _P, _I32, _P, _P, _I32, _I32, _P, _I64, _I64, _I64, _P, _SZ, _P]),
+    "w4_quantize_groupwise": (_I32, [_P, _I32, _I64, _I64, _I32, _P, _P, _P, _P]),
+    "w4_repack_s4_to_uint4b8": (_I32, [_P, _P, _I64, _P]),
     "w4_last_error": (ctypes.c_char_p, []),
     "w4_status_string": (ctypes.c_char_p, [_I32]),
     "w4_device_status": (_I32, [_P]),
@@ -216,6 +219,35 @@ def w4afp8_moe_grouped_gemm(qx, x_scale, expert_offsets, qweight, w_scale, group
                                           _ptr(w_scale), _scale_dtype(w_scale), group, _ptr(y), R, N, K,
                                           _ptr(ws), wsb, _stream(stream, qx.device)), "w4afp8_moe_grouped_gemm")
     return y
+
+
+def w4_quantize_groupwise(w, group: int, packed=None, scale=None, zero=None, stream=None):
+    """Min/max 4-bit group quantization of bf16 or fp16 ``w [N, K]``; returns
+    ``(packed uint8 [N, K/2], scale f32 [N, G], zero f32 [N, G])``."""
+    _cuda2d(w, "w", (torch.bfloat16, torch.float16))
+    N, K = w.shape
+    G = 1 if group == -1 else (K // group if group > 0 else 0)
+    packed = torch.empty((N, K // 2), dtype=torch.uint8, device=w.device) if packed is None else packed
+    scale = torch.empty((N, G), dtype=torch.float32, device=w.device) if scale is None else scale
+    zero = torch.empty((N, G), dtype=torch.float32, device=w.device) if zero is None else zero
+    wdt = W4_FP16 if w.dtype == torch.float16 else W4_BF16
+    _check(load().w4_quantize_groupwise(_ptr(w), wdt, N, K, group, _ptr(packed), _ptr(scale), _ptr(zero),
+                                        _stream(stream, w.device)), "w4_quantize_groupwise")
+    return packed, scale, zero
+
+
+def w4_repack_s4_to_uint4b8(src, dst=None, stream=None):
+    """Signed int4 pairs (any contiguous 1-byte or int32 tensor) -> uint4b8 by
+    XOR 0x88 on every byte; ``dst`` may be ``src`` (in place)."""
+    if not src.is_cuda or not src.is_contiguous():
+        raise ValueError("src must be a contiguous CUDA tensor")
+    dst = torch.empty_like(src) if dst is None else dst
+    n = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != n:
+        raise ValueError("dst must hold as many bytes as src")
+    _check(load().w4_repack_s4_to_uint4b8(_ptr(src), _ptr(dst), n, _stream(stream, src.device)),
+           "w4_repack_s4_to_uint4b8")
+    return dst
 
 
 def w4_device_status(stream=None, device=None) -> int:

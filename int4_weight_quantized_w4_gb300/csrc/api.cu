@@ -231,6 +231,35 @@ w4_status w4afp8_moe_grouped_gemm(const void* qx, const float* x_scale, const in
   return from_cuda(w4::launch_w4afp8_experts(a, static_cast<cudaStream_t>(stream)), "w4afp8 experts launch");
 }
 
+w4_status w4_quantize_groupwise(const void* w, int32_t w_dtype, int64_t N, int64_t K, int32_t group,
+                                void* packed, float* scale, float* zero, void* stream) {
+  if (N < 0 || K <= 0) return fail(W4_ERR_SHAPE, "sizes must be N >= 0, K > 0 (N=%lld K=%lld)", (long long)N,
+                                   (long long)K);
+  if (w_dtype != W4_BF16 && w_dtype != W4_FP16) return fail(W4_ERR_DTYPE, "w must be W4_BF16 or W4_FP16");
+  const int64_t g = group == -1 ? K : group;
+  if (g <= 0 || K % g != 0 || g > INT32_MAX)
+    return fail(W4_ERR_GROUP, "group %d must be -1 or a positive divisor of K=%lld", group, (long long)K);
+  if (K % 2 != 0 || g % 2 != 0)
+    return fail(W4_ERR_UNSUPPORTED, "K and the group must be even (two codes per byte), got K=%lld group=%lld",
+                (long long)K, (long long)g);
+  if (N == 0) return ok();
+  if (!w || !packed || !scale || !zero) return fail(W4_ERR_NULL, "w, packed, scale and zero must be non-NULL");
+  if (!aligned(w, 4) || !aligned(scale, 4) || !aligned(zero, 4))
+    return fail(W4_ERR_ALIGN, "w, scale and zero must be 4-byte aligned");
+  return from_cuda(w4::launch_quantize_groupwise(w, w_dtype == W4_FP16, N, K, static_cast<int32_t>(g),
+                                                 static_cast<uint8_t*>(packed), scale, zero,
+                                                 static_cast<cudaStream_t>(stream)),
+                   "quantize_groupwise launch");
+}
+
+w4_status w4_repack_s4_to_uint4b8(const void* src, void* dst, int64_t n_bytes, void* stream) {
+  if (n_bytes < 0) return fail(W4_ERR_SHAPE, "n_bytes must be >= 0");
+  if (n_bytes == 0) return ok();
+  if (!src || !dst) return fail(W4_ERR_NULL, "src and dst must be non-NULL");
+  if (!aligned(src, 16) || !aligned(dst, 16)) return fail(W4_ERR_ALIGN, "src and dst must be 16-byte aligned");
+  return from_cuda(w4::launch_xor88(src, dst, n_bytes, static_cast<cudaStream_t>(stream)), "repack launch");
+}
+
 w4_status w4_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return from_cuda(e, "cudaStreamSynchronize");

@@ -53,6 +53,9 @@ w4_status report_error(w4_status st, const char* msg);
 cudaError_t launch_w4a8_dense(const W4A8Args& a, cudaStream_t s);
 cudaError_t launch_w4afp8_experts(const W4A8Args& a, cudaStream_t s);
 
+cudaError_t launch_quantize_groupwise(const void* w, bool f16, int64_t N, int64_t K, int32_t group, uint8_t* packed,
+                                      float* scale, float* zero, cudaStream_t s);
+cudaError_t launch_xor88(const void* src, void* dst, int64_t n_bytes, cudaStream_t s);
 cudaError_t launch_bounded_wait_selftest(long long limit, unsigned int* status, cudaStream_t s);
 
 }  // namespace w4

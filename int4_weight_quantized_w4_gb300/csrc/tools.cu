@@ -1,0 +1,116 @@
+// Weight-side tools: the asymmetric min/max group quantizer and the signed
+// int4 -> uint4b8 repack.
+//
+// vllm-omni quantization/cpu_int4.py, quantize_groupwise: per group of
+// `group` consecutive input columns of w [N, K], scale = max(max - min, 1e-9)
+// / 15 and zero = min + 8 scale in fp32, codes q = clamp(round((w - min) /
+// scale), 0, 15) (round half to even), packed two per byte low nibble first
+// (pack_nibbles). The fp32 steps are taken one by one with IEEE rounding
+// (__fsub_rn, __fdiv_rn, rintf), so codes, scales and zeros are bit-exact.
+//
+// vLLM API docs, quantization.w4afp8, _repack_signed_int4_to_uint4b8:
+// signed int4 nibbles become uint4b8 (q + 8 mod 16) by XOR 0x88 on every byte.
+//
+// Both are bandwidth-bound load-time passes: one warp per (row, group) for the
+// quantizer (the group is read twice, the second time from L1), and 16-byte
+// vectors for the repack.
+#include "common.cuh"
+#include "launch.h"
+
+namespace w4 {
+namespace {
+
+template <bool kF16>
+W4_DEV float2 load_pair(const uint16_t* w, size_t i) {
+  const uint32_t v = *reinterpret_cast<const uint32_t*>(w + i);
+  if (kF16) return make_float2(half_bits_to_f32(v & 0xFFFFu), half_bits_to_f32(v >> 16));
+  return make_float2(bf16_lo(v), bf16_hi(v));
+}
+
+template <bool kF16>
+__global__ void __launch_bounds__(256) quantize_groupwise_kernel(const uint16_t* w, int64_t N, int64_t K, int group,
+                                                                 uint8_t* packed, float* scale, float* zero) {
+  const int64_t G = K / group;
+  const int64_t id = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (id >= N * G) return;
+  const int lane = threadIdx.x & 31;
+  const int64_t n = id / G, g = id % G;
+  const size_t base = static_cast<size_t>(n) * K + static_cast<size_t>(g) * group;   // even: group, K even
+  const int pairs = group / 2;
+  float mn = INFINITY, mx = -INFINITY;
+  for (int p = lane; p < pairs; p += 32) {
+    const float2 v = load_pair<kF16>(w, base + 2 * p);
+    mn = fminf(mn, fminf(v.x, v.y));
+    mx = fmaxf(mx, fmaxf(v.x, v.y));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  const float s = __fdiv_rn(fmaxf(__fsub_rn(mx, mn), 1e-9f), 15.0f);
+  const float z = __fadd_rn(mn, __fmul_rn(8.0f, s));
+  for (int p = lane; p < pairs; p += 32) {
+    const float2 v = load_pair<kF16>(w, base + 2 * p);
+    const float q0 = fminf(fmaxf(rintf(__fdiv_rn(__fsub_rn(v.x, mn), s)), 0.f), 15.f);
+    const float q1 = fminf(fmaxf(rintf(__fdiv_rn(__fsub_rn(v.y, mn), s)), 0.f), 15.f);
+    packed[base / 2 + p] = static_cast<uint8_t>(static_cast<int>(q0) | (static_cast<int>(q1) << 4));
+  }
+  if (lane == 0) {
+    scale[id] = s;
+    zero[id] = z;
+  }
+}
+
+__global__ void __launch_bounds__(256) xor88_kernel(const uint4* src, uint4* dst, size_t n16, const uint8_t* src_tail,
+                                                    uint8_t* dst_tail, int tail) {
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16; i += stride) {
+    uint4 v = ld_nc_v4(src + i);
+    v.x ^= 0x88888888u;
+    v.y ^= 0x88888888u;
+    v.z ^= 0x88888888u;
+    v.w ^= 0x88888888u;
+    dst[i] = v;
+  }
+  if (blockIdx.x == 0 && static_cast<int>(threadIdx.x) < tail) dst_tail[threadIdx.x] = src_tail[threadIdx.x] ^ 0x88u;
+}
+
+int sm_count_tools() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  }
+  return n;
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_groupwise(const void* w, bool f16, int64_t N, int64_t K, int32_t group, uint8_t* packed,
+                                      float* scale, float* zero, cudaStream_t s) {
+  const int64_t warps = N * (K / group);
+  const unsigned int blocks = static_cast<unsigned int>((warps + 7) / 8);
+  if (f16)
+    quantize_groupwise_kernel<true><<<blocks, 256, 0, s>>>(static_cast<const uint16_t*>(w), N, K, group, packed, scale,
+                                                           zero);
+  else
+    quantize_groupwise_kernel<false><<<blocks, 256, 0, s>>>(static_cast<const uint16_t*>(w), N, K, group, packed,
+                                                            scale, zero);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_xor88(const void* src, void* dst, int64_t n_bytes, cudaStream_t s) {
+  const size_t n16 = static_cast<size_t>(n_bytes) / 16;
+  const int tail = static_cast<int>(n_bytes - static_cast<int64_t>(n16) * 16);
+  size_t want = (n16 + 255) / 256;
+  const size_t cap = static_cast<size_t>(sm_count_tools()) * 8;
+  const unsigned int blocks = static_cast<unsigned int>(want < 1 ? 1 : (want > cap ? cap : want));
+  xor88_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst), n16,
+                                      static_cast<const uint8_t*>(src) + n16 * 16,
+                                      static_cast<uint8_t*>(dst) + n16 * 16, tail);
+  return cudaGetLastError();
+}
+
+}  // namespace w4

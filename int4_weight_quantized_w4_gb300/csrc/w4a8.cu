@@ -330,9 +330,25 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
 #pragma unroll
     for (int j = 0; j < kEpiCols; ++j) T[j] = 0.f;
 
+    // the scales of this group and the next three, loaded ahead: with the TMA
+    // pipes full a plain load takes ~1-2 us, a group's MMAs ~0.5 us
+    auto ld_scale = [&](int gg) -> uint32_t {
+      if (partials || !n_ok || gg >= G) return 0u;
+      const size_t si = (p.mode == kExperts) ? ((size_t)expert * N + n) * G + gg : (size_t)gg * N + n;
+      return p.w_scale[si];
+    };
+    uint32_t sr0 = ld_scale(0), sr1 = ld_scale(1), sr2 = ld_scale(2), sr3 = ld_scale(3);
+    int cur_g = 0;
     int seg = 0;
     for (int k0 = 0; k0 < K; ++seg) {
       const int g = k0 / group;
+      if (g != cur_g) {   // segments walk k in order: the group advances by one
+        sr0 = sr1;
+        sr1 = sr2;
+        sr2 = sr3;
+        sr3 = ld_scale(g + 3);
+        cur_g = g;
+      }
       const int kend = min(min((g + 1) * group, k0 + SEG_MAX), K);
       const int buf = seg & 1;
       if (!tc::wait(&acc_full[buf], (seg >> 1) & 1, abort_flag, p.status, kWaitNs)) break;
@@ -352,11 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
           }
         }
       } else {
-        float s = 0.f;
-        if (n_ok) {
-          const size_t si = (p.mode == kExperts) ? ((size_t)expert * N + n) * G + g : (size_t)g * N + n;
-          s = half_bits_to_f32(p.w_scale[si]);
-        }
+        const float s = half_bits_to_f32(sr0);
 #pragma unroll
         for (int cc = 0; cc < kEpiCols / 32; ++cc) {
           uint32_t v[32];

@@ -138,3 +138,24 @@ def test_moe_validation(lib):
 
 def test_selftest_rejects_bad_limit(lib):
     assert lib.w4_selftest_bounded_wait(0, None) == w4.W4_ERR_SHAPE
+
+
+def test_weight_tools_validation(lib):
+    def q(**kw):
+        a = dict(w=FAKE, wdt=w4.W4_BF16, N=4, K=256, group=128, packed=FAKE, scale=FAKE, zero=FAKE)
+        a.update(kw)
+        return lib.w4_quantize_groupwise(a["w"], a["wdt"], a["N"], a["K"], a["group"], a["packed"], a["scale"],
+                                         a["zero"], None)
+    assert q(wdt=w4.W4_INT8) == w4.W4_ERR_DTYPE
+    assert q(group=96) == w4.W4_ERR_GROUP                    # does not divide K
+    assert q(group=0) == w4.W4_ERR_GROUP
+    assert q(K=257, group=-1) == w4.W4_ERR_UNSUPPORTED       # two codes per byte need K even ...
+    assert q(K=255, group=5) == w4.W4_ERR_UNSUPPORTED        # ... and an even group
+    assert q(w=None) == w4.W4_ERR_NULL
+    assert q(w=ctypes.c_void_p((1 << 20) + 2)) == w4.W4_ERR_ALIGN
+    assert q(N=-1) == w4.W4_ERR_SHAPE
+    assert q(N=0) == w4.W4_OK
+    assert lib.w4_repack_s4_to_uint4b8(FAKE, FAKE, -1, None) == w4.W4_ERR_SHAPE
+    assert lib.w4_repack_s4_to_uint4b8(None, FAKE, 64, None) == w4.W4_ERR_NULL
+    assert lib.w4_repack_s4_to_uint4b8(ODD, FAKE, 64, None) == w4.W4_ERR_ALIGN
+    assert lib.w4_repack_s4_to_uint4b8(FAKE, FAKE, 0, None) == w4.W4_OK
