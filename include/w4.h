@@ -157,6 +157,24 @@ w4_status w4a8_group_partials(const void* qx, const void* qweight, int32_t group
                               void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * W4A8 linear from bf16 activations: w4_quant_act_per_token (int8) fused into
+ * the GEMM's activation pass, so the int8 codes never go to memory: each row
+ * is quantized exactly as w4_quant_act_per_token does ([INC] apply_weights:
+ * per-token symmetric int8 right before the GEMM) and its codes are written
+ * straight into the workspace as the exact fp16 operands of the tensor-core
+ * kernel; then y is computed as by w4a8_gemm.
+ *
+ *   x        [M, K] bf16, 16-byte aligned
+ *   x_scale  [M] float32, written (the per-token scales the GEMM used)
+ *   other arguments, limits and errors as w4a8_gemm; workspace: at least
+ *   w4_workspace_bytes(W4_OP_W4A8, M, N, K, group) bytes.
+ * y equals w4a8_gemm applied to w4_quant_act_per_token(x) bit for bit.
+ */
+w4_status w4a8_gemm_bf16in(const void* x, const void* qweight, const void* w_scale, int32_t w_scale_dtype,
+                           int32_t group, const void* bias, void* y, float* x_scale, int64_t M, int64_t N, int64_t K,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * W4A16 linear for decode: bf16 activations x the same GPTQ qweight
  * ([INC] class docstring: int4_gemm_w4a16 reads bit-identical weights) with
  * fp16 or bf16 group scales and optional bf16 additive zeros

@@ -16,7 +16,7 @@ import torch
 
 __all__ = [
     "W4Error", "load", "library_path",
-    "w4_quant_act_per_token", "w4a8_gemm", "w4a8_gemm_noalloc", "w4a8_group_partials", "w4a16_gemm",
+    "w4_quant_act_per_token", "w4a8_gemm", "w4a8_gemm_bf16in", "w4a8_gemm_noalloc", "w4a8_group_partials", "w4a16_gemm",
     "w4afp8_moe_grouped_gemm", "w4_quantize_groupwise", "w4_repack_s4_to_uint4b8",
     "w4_device_status", "w4_selftest_bounded_wait",
     "W4_OK", "W4_ERR_NULL", "W4_ERR_ALIGN", "W4_ERR_GROUP", "W4_ERR_DTYPE",
@@ -39,6 +39,7 @@ _SIGNATURES = {
     "w4_workspace_bytes": (_SZ, [_I32, _I64, _I64, _I64, _I32]),
     "w4a8_gemm": (_I32, [_P, _P, _P, _P, _I32, _I32, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
     "w4a8_group_partials": (_I32, [_P, _P, _I32, _P, _I64, _I64, _I64, _P, _SZ, _P]),
+    "w4a8_gemm_bf16in": (_I32, [_P, _P, _P, _I32, _I32, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
     "w4a8_gemm_noalloc": (_I32, [_P, _P, _P, _P, _I32, _I32, _P, _P, _I64, _I64, _I64, _P]),
     "w4a16_gemm": (_I32, [_P, _P, _P, _I32, _P, _I32, _P, _P, _I64, _I64, _I64, _P]),
     "w4afp8_moe_grouped_gemm": (_I32, [_P, _P, _P, _I32, _P, _P, _I32, _I32, _P, _I64, _I64, _I64, _P, _SZ, _P]),
@@ -151,6 +152,24 @@ def w4a8_gemm(qx, x_scale, qweight, w_scale, group: int, bias=None, y=None, work
                             group, _ptr(bias), _ptr(y), M, N, K, _ptr(ws), wsb, _stream(stream, qx.device)),
            "w4a8_gemm")
     return y
+
+
+def w4a8_gemm_bf16in(x, qweight, w_scale, group: int, bias=None, y=None, x_scale=None, workspace=None, stream=None):
+    """W4A8 linear from bf16 ``x [M, K]``: per-token int8 quantization fused into
+    the GEMM's activation pass. Returns ``(y bf16 [M, N], x_scale f32 [M])``."""
+    _cuda2d(x, "x", (torch.bfloat16,))
+    _cuda2d(qweight, "qweight", (torch.int32,))
+    M, K = x.shape
+    N = qweight.shape[1]
+    if qweight.shape[0] * 8 != K or w_scale.dim() != 2 or w_scale.shape[1] != N:
+        raise ValueError("inconsistent shapes for w4a8_gemm_bf16in")
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device) if y is None else y
+    x_scale = torch.empty((M,), dtype=torch.float32, device=x.device) if x_scale is None else x_scale
+    ws, wsb = _workspace(workspace, W4_OP_W4A8, M, N, K, group, x.device)
+    _check(load().w4a8_gemm_bf16in(_ptr(x), _ptr(qweight), _ptr(w_scale), _scale_dtype(w_scale), group, _ptr(bias),
+                                   _ptr(y), _ptr(x_scale), M, N, K, _ptr(ws), wsb, _stream(stream, x.device)),
+           "w4a8_gemm_bf16in")
+    return y, x_scale
 
 
 def w4a8_gemm_noalloc(qx, x_scale, qweight, w_scale, group: int, bias=None, y=None, stream=None):

@@ -169,6 +169,35 @@ w4_status w4a8_gemm(const void* qx, const float* x_scale, const void* qweight, c
                      workspace_bytes, stream);
 }
 
+w4_status w4a8_gemm_bf16in(const void* x, const void* qweight, const void* w_scale, int32_t w_scale_dtype,
+                           int32_t group, const void* bias, void* y, float* x_scale, int64_t M, int64_t N, int64_t K,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+  int32_t g = 0;
+  w4_status st = check_dims_group(M, N, K, group, &g);
+  if (st != W4_OK) return st;
+  if (w_scale_dtype != W4_FP16)
+    return fail(W4_ERR_DTYPE, "w4a8_gemm_bf16in reads weight scales as fp16; pass fp16 scales (W4_FP16)");
+  if (K % 16 != 0 || g % 16 != 0)
+    return fail(W4_ERR_UNSUPPORTED, "w4a8 tiles need K and the group to be multiples of 16 (K=%lld group=%d)",
+                (long long)K, g);
+  if (M == 0) return ok();
+  if (!x || !qweight || !w_scale || !y || !x_scale) return fail(W4_ERR_NULL, "required pointer is NULL");
+  if (!aligned(x, 16) || !aligned(qweight, 16) || !aligned(y, 16) || !aligned(w_scale, 8) ||
+      !aligned(x_scale, 4) || (bias && !aligned(bias, 8)))
+    return fail(W4_ERR_ALIGN, "matrices must be 16-byte aligned, vectors 8-byte aligned");
+  if (M > INT32_MAX || N > INT32_MAX) return fail(W4_ERR_UNSUPPORTED, "M or N too large");
+  st = check_workspace(workspace, workspace_bytes, M, K);
+  if (st != W4_OK) return st;
+  unsigned int* status = nullptr;
+  cudaError_t e = status_ptr(&status);
+  if (e != cudaSuccess) return from_cuda(e, "device status word");
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  e = w4::launch_quant_widen(x, M, K, false, workspace, x_scale, s);
+  if (e != cudaSuccess) return from_cuda(e, "quantize-and-widen launch");
+  w4::W4A8Args a{nullptr, x_scale, qweight, w_scale, bias, y, nullptr, 1, M, N, K, g, false, status, workspace, true};
+  return from_cuda(w4::launch_w4a8_dense(a, s), "w4a8 launch");
+}
+
 w4_status w4a8_group_partials(const void* qx, const void* qweight, int32_t group, int32_t* partials,
                               int64_t M, int64_t N, int64_t K, void* workspace, size_t workspace_bytes,
                               void* stream) {

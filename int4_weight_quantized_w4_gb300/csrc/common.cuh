@@ -67,6 +67,38 @@ W4_DEV float half_bits_to_f32(uint32_t h16) {
 }
 
 // ---------------------------------------------------------------------------
+// 8-bit activation codes -> exact fp16, k permuted per 8-chunk
+// (the operand layout of the W4A8 tensor-core kernel)
+// ---------------------------------------------------------------------------
+
+// int8 bytes b0..b7 -> fp16 (b0,b4,b1,b5,b2,b6,b3,b7). (b ^ 0x80) in the low
+// mantissa byte of 1024 is 1152 + b; subtracting 1152 leaves b exactly.
+W4_DEV uint32_t i8pair(uint32_t u0, uint32_t u1, uint32_t sel) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(and_xor(prmt(u0, u1, sel), 0x00FF00FFu, 0x64806480u)),
+      "r"(0x64806480u));
+  return d;
+}
+
+W4_DEV uint4 widen_i8(uint32_t u0, uint32_t u1) {
+  return make_uint4(i8pair(u0, u1, 0x0400u), i8pair(u0, u1, 0x0501u), i8pair(u0, u1, 0x0602u),
+                    i8pair(u0, u1, 0x0703u));
+}
+
+W4_DEV uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+  uint32_t d;
+  asm("{.reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t;}" : "=r"(d) : "r"(two_codes));
+  return d;
+}
+
+// e4m3 codes b0..b7 -> fp16 (b0,b4,b1,b5,b2,b6,b3,b7), exactly.
+W4_DEV uint4 widen_e4m3(uint32_t u0, uint32_t u1) {
+  const uint32_t a = prmt(u0, u1, 0x5140u), b = prmt(u0, u1, 0x7362u);
+  return make_uint4(e4m3x2_to_f16x2(a & 0xFFFFu), e4m3x2_to_f16x2(a >> 16), e4m3x2_to_f16x2(b & 0xFFFFu),
+                    e4m3x2_to_f16x2(b >> 16));
+}
+
+// ---------------------------------------------------------------------------
 // global memory access
 // ---------------------------------------------------------------------------
 

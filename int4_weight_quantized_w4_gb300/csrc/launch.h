@@ -29,6 +29,10 @@ struct W4A16Args {
   unsigned int* status;
 };
 cudaError_t launch_w4a16(const W4A16Args& a, cudaStream_t s);
+// Per-token quantization whose output is the codes' exact fp16 values in the
+// W4A8 operand order (fp16 [M, K] into `wide`), plus the fp32 scales.
+cudaError_t launch_quant_widen(const void* x, int64_t M, int64_t K, bool fp8, void* wide, float* scale,
+                               cudaStream_t s);
 // Shared memory the decode kernel needs for one token row beside a minimal ring.
 size_t w4a16_smem_bytes(int64_t N, int64_t K, int32_t group);
 
@@ -46,6 +50,7 @@ struct W4A8Args {
   bool partials;          // write int32 group partials instead of y
   unsigned int* status;
   void* workspace;        // fp16 [rows, K]: the activations widened once per call
+  bool prewidened;        // the workspace already holds them (act unused)
 };
 size_t w4a8_workspace_bytes(int64_t rows, int64_t K);
 // Sets the calling thread's w4_last_error() message and returns `st`.

@@ -12,6 +12,9 @@
 // registers (16-byte loads), the row maximum is a warp-shuffle butterfly plus
 // one shared-memory step, and the quantized chunks leave as 8-byte stores, so
 // HBM sees the row read once and the codes written once (3 bytes per element).
+// The fused form for the W4A8 GEMM stores each chunk's codes instead as their
+// exact fp16 values in the GEMM's operand order (4 bytes per element, no int8
+// round trip).
 #include "common.cuh"
 #include "launch.h"
 
@@ -72,15 +75,26 @@ W4_DEV uint2 quant_chunk(const uint4& v, float s) {
   return o;
 }
 
+// The codes of one 8-chunk as stored: 8 bytes, or (kWiden) the exact fp16
+// values of the codes in the W4A8 operand order (16 bytes).
+template <bool FP8, bool kWiden>
+W4_DEV void store_chunk(void* q, size_t i, const uint4& v, float s) {
+  const uint2 c = quant_chunk<FP8>(v, s);
+  if (kWiden)
+    static_cast<uint4*>(q)[i] = FP8 ? widen_e4m3(c.x, c.y) : widen_i8(c.x, c.y);
+  else
+    static_cast<uint2*>(q)[i] = c;
+}
+
 // NCH > 0: the row fits in registers, NCH chunks per thread.
 // NCH == 0: long rows, read twice (the second read mostly hits L2).
-template <int NCH, bool FP8>
+template <int NCH, bool FP8, bool kWiden>
 __global__ void __launch_bounds__(kMaxThreads) quant_rows(const uint4* __restrict__ x, int K8,
-                                                          uint2* __restrict__ q, float* __restrict__ scale) {
+                                                          void* __restrict__ q, float* __restrict__ scale) {
   __shared__ float red[kMaxThreads / 32];
   const size_t row = blockIdx.x;
   const uint4* xr = x + row * static_cast<size_t>(K8);
-  uint2* qr = q + row * static_cast<size_t>(K8);
+  const size_t q0 = row * static_cast<size_t>(K8);
   constexpr float kQ = FP8 ? 448.f : 127.f;
   if constexpr (NCH > 0) {
     uint4 v[NCH];
@@ -96,7 +110,7 @@ __global__ void __launch_bounds__(kMaxThreads) quant_rows(const uint4* __restric
 #pragma unroll
     for (int c = 0; c < NCH; ++c) {
       const int i = threadIdx.x + c * blockDim.x;
-      if (i < K8) qr[i] = quant_chunk<FP8>(v[c], s);
+      if (i < K8) store_chunk<FP8, kWiden>(q, q0 + i, v[c], s);
     }
     if (threadIdx.x == 0) scale[row] = s;
   } else {
@@ -104,12 +118,12 @@ __global__ void __launch_bounds__(kMaxThreads) quant_rows(const uint4* __restric
     for (int i = threadIdx.x; i < K8; i += blockDim.x) m = fmaxf(m, chunk_absmax(ld_nc_v4(xr + i)));
     const float amax = row_max(m, red);
     const float s = (amax == 0.f) ? 1.f : __fdiv_rn(amax, kQ);
-    for (int i = threadIdx.x; i < K8; i += blockDim.x) qr[i] = quant_chunk<FP8>(ld_stream_v4(xr + i), s);
+    for (int i = threadIdx.x; i < K8; i += blockDim.x) store_chunk<FP8, kWiden>(q, q0 + i, ld_stream_v4(xr + i), s);
     if (threadIdx.x == 0) scale[row] = s;
   }
 }
 
-template <bool FP8>
+template <bool FP8, bool kWiden>
 cudaError_t launch(const void* x, int64_t M, int64_t K, void* q, float* scale, cudaStream_t s) {
   const int K8 = static_cast<int>(K / 8);
   int threads = ((K8 + 31) / 32) * 32;
@@ -117,13 +131,12 @@ cudaError_t launch(const void* x, int64_t M, int64_t K, void* q, float* scale, c
   const int nch = (K8 + threads - 1) / threads;
   const dim3 grid(static_cast<unsigned>(M));
   auto xp = static_cast<const uint4*>(x);
-  auto qp = static_cast<uint2*>(q);
   switch (nch) {
-    case 1: quant_rows<1, FP8><<<grid, threads, 0, s>>>(xp, K8, qp, scale); break;
-    case 2: quant_rows<2, FP8><<<grid, threads, 0, s>>>(xp, K8, qp, scale); break;
-    case 3: quant_rows<3, FP8><<<grid, threads, 0, s>>>(xp, K8, qp, scale); break;
-    case 4: quant_rows<4, FP8><<<grid, threads, 0, s>>>(xp, K8, qp, scale); break;
-    default: quant_rows<0, FP8><<<grid, threads, 0, s>>>(xp, K8, qp, scale); break;
+    case 1: quant_rows<1, FP8, kWiden><<<grid, threads, 0, s>>>(xp, K8, q, scale); break;
+    case 2: quant_rows<2, FP8, kWiden><<<grid, threads, 0, s>>>(xp, K8, q, scale); break;
+    case 3: quant_rows<3, FP8, kWiden><<<grid, threads, 0, s>>>(xp, K8, q, scale); break;
+    case 4: quant_rows<4, FP8, kWiden><<<grid, threads, 0, s>>>(xp, K8, q, scale); break;
+    default: quant_rows<0, FP8, kWiden><<<grid, threads, 0, s>>>(xp, K8, q, scale); break;
   }
   return cudaGetLastError();
 }
@@ -133,7 +146,13 @@ cudaError_t launch(const void* x, int64_t M, int64_t K, void* q, float* scale, c
 cudaError_t launch_quant_per_token(const void* x, int64_t M, int64_t K, bool fp8, void* q, float* scale,
                                    cudaStream_t s) {
   if (K / 8 > INT32_MAX) return cudaErrorInvalidValue;
-  return fp8 ? launch<true>(x, M, K, q, scale, s) : launch<false>(x, M, K, q, scale, s);
+  return fp8 ? launch<true, false>(x, M, K, q, scale, s) : launch<false, false>(x, M, K, q, scale, s);
+}
+
+cudaError_t launch_quant_widen(const void* x, int64_t M, int64_t K, bool fp8, void* wide, float* scale,
+                               cudaStream_t s) {
+  if (K / 8 > INT32_MAX) return cudaErrorInvalidValue;
+  return fp8 ? launch<true, true>(x, M, K, wide, scale, s) : launch<false, true>(x, M, K, wide, scale, s);
 }
 
 }  // namespace w4

@@ -44,21 +44,27 @@ constexpr int BK = 64;           // k per stage (one 128-byte fp16 swizzle row)
 constexpr int UMMA_K = 16;
 constexpr int A_STAGES = 3;      // converted weight tiles
 constexpr int B_STAGES = 4;      // activation tiles (TMA)
-constexpr int RAW_STAGES = 8;    // packed weight words (TMA)
+constexpr int RAW_STAGES = 2;    // packed weight words (TMA), RAW_PER k-stages per slot
+constexpr int RAW_PER = 4;       // k-stages per packed-word copy (16 KB: one copy per 256 k)
 constexpr int SEG_MAX = 16384;   // longest accumulation before a drain (exactness bound)
 
 constexpr int A_BYTES = BM * BK * 2;    // 16 KB
 constexpr int B_BYTES = BN * BK * 2;    // 32 KB
-constexpr int RAW_BYTES = BM * BK / 2;  // 4 KB
+constexpr int RAW_BYTES = RAW_PER * BM * BK / 2;  // 16 KB
 
 // Warp roles, four warpgroups: 0-7 epilogue (warp w reads TMEM lane quadrant
-// w % 4, token half w / 4), 8-11 converters, 12 weight-word TMA, 13
-// activation TMA, 14 MMA issuer (and TMEM owner), 15 idle.
+// w % 4, token half w / 4), 8-11 converters, 12 weight-word TMA, 13 and 15
+// activation TMA (even / odd k-stages), 14 MMA issuer (and TMEM owner).
+// Copies are issued from two warps and packed words 256 k at a time because
+// on GB300 the copies one thread issues complete about one per 0.5 us
+// whatever their size (4-64 KB): one issuer would feed the 32 KB activation
+// tile of a 0.25 us stage at half the rate the MMAs consume it.
 constexpr int kEpiWarps = 8;
 constexpr int kConvWarps = 4;
 constexpr int kWarpConv0 = 8;
 constexpr int kWarpLoadW = 12;
-constexpr int kWarpLoadB = 13;
+constexpr int kWarpLoadB = 13;   // activation copies of even k-stages
+constexpr int kWarpLoadB2 = 15;  // activation copies of odd k-stages
 constexpr int kWarpMma = 14;
 constexpr int kThreads = 16 * 32;
 constexpr uint32_t kTmemCols = 2 * BN;        // double-buffered accumulator
@@ -79,6 +85,7 @@ struct Params {
   const int32_t* offsets;  // [E + 1] (experts)
   int E, M, N, K, group, mode;
   int cl;                  // CTAs per cluster along N; they share each activation tile
+  int raw_rows;            // word rows (k / 8) per packed-word copy: min(RAW_PER * BK / 8, K / 8)
   unsigned int* status;
 };
 
@@ -188,23 +195,25 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
   if (warp == kWarpLoadW) {
     // ---- raw packed weight words -> ring ----
     if (lane == 0) {
-      for (int s = 0; s < nst; ++s) {
-        const int r = s % RAW_STAGES;
-        if (!tc::wait(&raw_empty[r], ((s / RAW_STAGES) & 1) ^ 1, abort_flag, p.status, kWaitNs)) break;
-        mbar_arrive_expect_tx(&raw_full[r], RAW_BYTES);
+      const int nraw = (nst + RAW_PER - 1) / RAW_PER;
+      for (int ri = 0; ri < nraw; ++ri) {
+        const int r = ri % RAW_STAGES;
+        if (!tc::wait(&raw_empty[r], ((ri / RAW_STAGES) & 1) ^ 1, abort_flag, p.status, kWaitNs)) break;
+        mbar_arrive_expect_tx(&raw_full[r], static_cast<uint32_t>(p.raw_rows * BM * 4));
         if (p.mode == kExperts)
-          tc::tma_load_3d(raw_base + r * RAW_BYTES, &p.tm_w, &raw_full[r], s * (BK / 8), n0, expert);
+          tc::tma_load_3d(raw_base + r * RAW_BYTES, &p.tm_w, &raw_full[r], ri * RAW_PER * (BK / 8), n0, expert);
         else
-          tc::tma_load_2d(raw_base + r * RAW_BYTES, &p.tm_w, &raw_full[r], n0, s * (BK / 8));
+          tc::tma_load_2d(raw_base + r * RAW_BYTES, &p.tm_w, &raw_full[r], n0, ri * RAW_PER * (BK / 8));
       }
     }
-  } else if (warp == kWarpLoadB) {
+  } else if (warp == kWarpLoadB || warp == kWarpLoadB2) {
     // ---- widened activations -> ring; with a cluster, each CTA loads 1/cl of
     // the rows and multicasts them to every CTA of the cluster ----
     if (lane == 0) {
       const int rows = BN / p.cl;
+      const int first = warp == kWarpLoadB ? 0 : 1;   // B_STAGES is even: a warp keeps its slots
       bool ok = true;
-      for (int s = 0; s < nst; ++s) {
+      for (int s = first; s < nst; s += 2) {
         const int b = s % B_STAGES;
         if (!tc::wait(&b_empty[b], ((s / B_STAGES) & 1) ^ 1, abort_flag, p.status, kWaitNs)) {
           ok = false;
@@ -219,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
       }
       // every CTA of the cluster releases every slot before anyone leaves:
       // no peer commit may still be on its way to this CTA's barriers
-      for (int b = 0; ok && b < B_STAGES && b < nst; ++b) {
+      for (int b = first; ok && b < B_STAGES && b < nst; b += 2) {
         const int uses = (nst - b + B_STAGES - 1) / B_STAGES;
         ok = tc::wait(&b_empty[b], (uses - 1) & 1, abort_flag, p.status, kWaitNs);
       }
@@ -228,21 +237,23 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
     // ---- nibbles -> fp16 operand A ----
     const int t = threadIdx.x - kWarpConv0 * 32;  // output row within the tile
     for (int s = 0; s < nst; ++s) {
-      const int r = s % RAW_STAGES, a = s % A_STAGES;
-      if (!tc::wait(&raw_full[r], (s / RAW_STAGES) & 1, abort_flag, p.status, kWaitNs)) break;
+      const int ri = s / RAW_PER, sub = s % RAW_PER;   // packed-word copy and k-stage within it
+      const int r = ri % RAW_STAGES, a = s % A_STAGES;
+      if (!tc::wait(&raw_full[r], (ri / RAW_STAGES) & 1, abort_flag, p.status, kWaitNs)) break;
       const uint32_t* raw = reinterpret_cast<const uint32_t*>(raw_base + r * RAW_BYTES);
       uint32_t w[8];
-      if (p.mode == kExperts) {  // box [128 outputs][8 words]
-        const uint4 lo = *reinterpret_cast<const uint4*>(raw + t * 8);
-        const uint4 hi = *reinterpret_cast<const uint4*>(raw + t * 8 + 4);
+      if (p.mode == kExperts) {  // box [128 outputs][raw_rows words]
+        const uint4 lo = *reinterpret_cast<const uint4*>(raw + t * p.raw_rows + sub * 8);
+        const uint4 hi = *reinterpret_cast<const uint4*>(raw + t * p.raw_rows + sub * 8 + 4);
         w[0] = lo.x; w[1] = lo.y; w[2] = lo.z; w[3] = lo.w;
         w[4] = hi.x; w[5] = hi.y; w[6] = hi.z; w[7] = hi.w;
-      } else {  // box [8 words][128 outputs]
+      } else {  // box [raw_rows words][128 outputs]
 #pragma unroll
-        for (int kb = 0; kb < 8; ++kb) w[kb] = raw[kb * BM + t];
+        for (int kb = 0; kb < 8; ++kb) w[kb] = raw[(sub * 8 + kb) * BM + t];
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&raw_empty[r]);   // words are in registers
+      // the copy's words are in registers once its last k-stage is read
+      if (lane == 0 && (sub == RAW_PER - 1 || s == nst - 1)) mbar_arrive(&raw_empty[r]);
       if (!tc::wait(&a_empty[a], ((s / A_STAGES) & 1) ^ 1, abort_flag, p.status, kWaitNs)) break;
       uint8_t* arow = a_base + a * A_BYTES + t * 128;
 #pragma unroll
@@ -415,33 +426,6 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
 // widening pass: 8-bit activations -> exact fp16, k permuted per 8-chunk
 // ---------------------------------------------------------------------------
 
-// int8 bytes b0..b7 -> fp16 (b0,b4,b1,b5,b2,b6,b3,b7). (b ^ 0x80) in the low
-// mantissa byte of 1024 is 1152 + b; subtracting 1152 leaves b exactly.
-W4_DEV uint32_t i8pair(uint32_t u0, uint32_t u1, uint32_t sel) {
-  uint32_t d;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(and_xor(prmt(u0, u1, sel), 0x00FF00FFu, 0x64806480u)),
-      "r"(0x64806480u));
-  return d;
-}
-
-W4_DEV uint4 widen_i8(uint32_t u0, uint32_t u1) {
-  return make_uint4(i8pair(u0, u1, 0x0400u), i8pair(u0, u1, 0x0501u), i8pair(u0, u1, 0x0602u),
-                    i8pair(u0, u1, 0x0703u));
-}
-
-W4_DEV uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
-  uint32_t d;
-  asm("{.reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t;}" : "=r"(d) : "r"(two_codes));
-  return d;
-}
-
-// e4m3 codes b0..b7 -> fp16 (b0,b4,b1,b5,b2,b6,b3,b7), exactly.
-W4_DEV uint4 widen_e4m3(uint32_t u0, uint32_t u1) {
-  const uint32_t a = prmt(u0, u1, 0x5140u), b = prmt(u0, u1, 0x7362u);
-  return make_uint4(e4m3x2_to_f16x2(a & 0xFFFFu), e4m3x2_to_f16x2(a >> 16), e4m3x2_to_f16x2(b & 0xFFFFu),
-                    e4m3x2_to_f16x2(b >> 16));
-}
-
 template <bool FP8>
 __global__ void __launch_bounds__(256) widen_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
                                                     size_t n16) {
@@ -506,7 +490,7 @@ cudaError_t run(const W4A8Args& a, int mode, cudaStream_t s) {
     attr_set = true;
   }
   const bool experts = mode == kExperts;
-  cudaError_t e = widen(a.act, a.workspace, a.M, a.K, experts, s);
+  cudaError_t e = a.prewidened ? cudaSuccess : widen(a.act, a.workspace, a.M, a.K, experts, s);
   if (e != cudaSuccess) return e;
 
   // Optional cluster along N: the CTAs of a cluster share one activation
@@ -519,6 +503,9 @@ cudaError_t run(const W4A8Args& a, int mode, cudaStream_t s) {
 
   Params p;
   memset(&p, 0, sizeof(p));
+  // packed-word copies cover RAW_PER k-stages, or all of a short K (expert
+  // mode needs K % 32 == 0, so its copy width is a multiple of 16 bytes)
+  p.raw_rows = static_cast<int>(a.K / 8 < RAW_PER * BK / 8 ? a.K / 8 : RAW_PER * BK / 8);
   {
     const cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.M};
     const cuuint64_t strides[1] = {(cuuint64_t)a.K * 2};
@@ -530,12 +517,12 @@ cudaError_t run(const W4A8Args& a, int mode, cudaStream_t s) {
   if (experts) {
     const cuuint64_t dims[3] = {(cuuint64_t)a.K / 8, (cuuint64_t)a.N, (cuuint64_t)a.E};
     const cuuint64_t strides[2] = {(cuuint64_t)a.K / 8 * 4, (cuuint64_t)a.N * (a.K / 8) * 4};
-    const cuuint32_t box[3] = {BK / 8, BM, 1};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(p.raw_rows), BM, 1};
     e = encode(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_INT32, 3, a.qweight, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
   } else {
     const cuuint64_t dims[2] = {(cuuint64_t)a.N, (cuuint64_t)a.K / 8};
     const cuuint64_t strides[1] = {(cuuint64_t)a.N * 4};
-    const cuuint32_t box[2] = {BM, BK / 8};
+    const cuuint32_t box[2] = {BM, static_cast<cuuint32_t>(p.raw_rows)};
     e = encode(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, a.qweight, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
   }
   if (e != cudaSuccess) return e;

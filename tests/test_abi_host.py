@@ -159,3 +159,19 @@ def test_weight_tools_validation(lib):
     assert lib.w4_repack_s4_to_uint4b8(None, FAKE, 64, None) == w4.W4_ERR_NULL
     assert lib.w4_repack_s4_to_uint4b8(ODD, FAKE, 64, None) == w4.W4_ERR_ALIGN
     assert lib.w4_repack_s4_to_uint4b8(FAKE, FAKE, 0, None) == w4.W4_OK
+
+
+def test_w4a8_bf16in_validation(lib):
+    def call(**kw):
+        a = dict(x=FAKE, qw=FAKE, ws=FAKE, wdt=w4.W4_FP16, group=128, bias=None, y=FAKE, sx=FAKE,
+                 M=16, N=256, K=256, work=FAKE, work_bytes=1 << 20)
+        a.update(kw)
+        return lib.w4a8_gemm_bf16in(a["x"], a["qw"], a["ws"], a["wdt"], a["group"], a["bias"], a["y"], a["sx"],
+                                    a["M"], a["N"], a["K"], a["work"], a["work_bytes"], None)
+    assert call(wdt=w4.W4_BF16) == w4.W4_ERR_DTYPE
+    assert call(sx=None) == w4.W4_ERR_NULL
+    assert call(x=ODD) == w4.W4_ERR_ALIGN
+    assert call(group=96) == w4.W4_ERR_GROUP
+    assert call(K=264, group=-1) == w4.W4_ERR_UNSUPPORTED
+    assert call(work=None) == w4.W4_ERR_WORKSPACE
+    assert call(M=0) == w4.W4_OK

@@ -136,3 +136,25 @@ def test_bounded_wait_selftest():
     assert w4.w4_device_status() == w4.W4_OK
     x = torch.ones(4, 4, device="cuda")
     assert float((x + x).sum()) == 32.0
+
+
+@pytest.mark.parametrize("M,N,K,group,outliers", [(16, 256, 256, 128, 0.0), (300, 384, 1024, 128, 0.01),
+                                                  (77, 136, 512, -1, 0.0), (1, 128, 4096, 64, 0.01)])
+def test_w4a8_bf16in_equals_quant_then_gemm(M, N, K, group, outliers):
+    """Quantization fused into the GEMM's activation pass: same scales and the
+    same output bits as w4_quant_act_per_token followed by w4a8_gemm, and the
+    oracle's result within tolerance."""
+    g = K if group == -1 else group
+    xb = S.activations_bf16(M, K, seed=M + K, outlier_frac=outliers)
+    qw = S.random_words((K // 8, N), seed=M + 1)
+    sw = S.scales_f16((K // g, N), seed=M + 2)
+    bb = S.bias_bf16(N, seed=M + 3)
+    x, qw_d, sw_d, b_d = bf16(xb), to_dev(qw), to_dev(sw), bf16(bb)
+    y_f, s_f = w4.w4a8_gemm_bf16in(x, qw_d, sw_d, group, bias=b_d)
+    q, s = w4.w4_quant_act_per_token(x, "int8")
+    y_u = w4.w4a8_gemm(q, s, qw_d, sw_d, group, bias=b_d)
+    torch.cuda.synchronize()
+    assert np.array_equal(s_f.cpu().numpy().view(np.uint32), s.cpu().numpy().view(np.uint32))
+    assert np.array_equal(bits(y_f), bits(y_u))
+    qr, sr = O.quant_int8_per_token(xb)
+    check_bf16_output(bits(y_f), O.w4a8_linear(qr, sr, qw, sw, group, bias_bits=bb), f"bf16in M={M}")
