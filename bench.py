@@ -91,7 +91,7 @@ class ClockSampler:
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.lines = []
+        self.lines = []        # (host monotonic time the sample arrived, csv line)
 
     def __enter__(self):
         try:
@@ -107,7 +107,13 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
+
+    def wait_first(self, timeout=5.0):
+        """Block until nvidia-smi delivers its first sample (it takes a moment to start)."""
+        t0 = time.monotonic()
+        while self.proc is not None and not self.lines and time.monotonic() - t0 < timeout:
+            time.sleep(0.01)
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -118,10 +124,13 @@ class ClockSampler:
                 self.proc.kill()
             self.thread.join(timeout=2)
 
-    def summary(self):
+    def summary(self, t0=None, t1=None):
+        """Samples that arrived within [t0, t1] (host monotonic), all if not given."""
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for t, ln in self.lines:
+            if (t0 is not None and t < t0) or (t1 is not None and t > t1):
+                continue
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 8:
                 continue
@@ -169,16 +178,26 @@ def run_ours(args, rank, world, local_rank):
             call(i)
     torch.cuda.synchronize()
 
-    # one graph of GRAPH_CALLS calls, rotating weight copies
+    # exactly K calls: a graph of up to GRAPH_CALLS calls (rotating weight
+    # copies) replayed K // calls times, and a graph of the remainder
+    steps = max(1, args.steps)
+    calls = min(GRAPH_CALLS, steps)
+    replays, rem = steps // calls, steps % calls
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
-        for i in range(GRAPH_CALLS):
+        for i in range(calls):
             call(i)
-    replays = max(1, args.steps // GRAPH_CALLS)
-    steps = replays * GRAPH_CALLS
+    g_rem = None
+    if rem:
+        g_rem = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_rem, stream=stream):
+            for i in range(rem):
+                call(calls + i)
     with torch.cuda.stream(stream):          # replay() launches on the current stream
         for _ in range(max(args.warmup, 3)):
             g.replay()
+            if g_rem is not None:
+                g_rem.replay()
     torch.cuda.synchronize()
 
     if world > 1:
@@ -186,12 +205,30 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local_rank) as clk, torch.cuda.stream(stream):
+        clk.wait_first()
+        t_begin = time.monotonic()
         e0.record(stream)
         for _ in range(replays):
             g.replay()
+        if g_rem is not None:
+            g_rem.replay()
         e1.record(stream)
         torch.cuda.synchronize()
+        t_end = time.monotonic()
+        # nvidia-smi samples every 100 ms: when the timed region is shorter
+        # than that, the same graph keeps running (untimed, one replay in
+        # flight at a time) until 0.6 s have passed, so the samples see the
+        # GPU under this load
+        window = "timed region"
+        if t_end - t_begin < 0.6:
+            window = "timed region + untimed replays of the same graph up to 0.6 s"
+            while time.monotonic() - t_begin < 0.6:
+                g.replay()
+                torch.cuda.synchronize()
+            t_end = time.monotonic()
     ms = e0.elapsed_time(e1)
+    clocks = clk.summary(t_begin, t_end)
+    clocks["window"] = window
     if world > 1:
         torch.distributed.barrier()
         t = torch.tensor([ms], device=dev)
@@ -245,7 +282,8 @@ def run_ours(args, rank, world, local_rank):
                    "scales": "fp16", "zeros": False, "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2: {N_COPIES} rotating weight copies "
                          f"({N_COPIES * nbytes / 1e6:.0f} MB)",
-                   "timing": f"CUDA graph of {GRAPH_CALLS} calls replayed {replays}x, CUDA events"},
+                   "timing": f"CUDA graph of {calls} calls replayed {replays}x"
+                             + (f" + a graph of {rem}" if rem else "") + ", CUDA events"},
         "roofline": {"bound": "hbm", "achieved": round(gbs_per_launch, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(gbs_per_launch / hbm, 4), "traffic": traffic,
                      "peak_source": f"{peak_kind} hbm_gbs", "kernel": "w4a16_kernel",
@@ -254,7 +292,7 @@ def run_ours(args, rank, world, local_rank):
                 "d2h_bytes_per_step": DEC_M * DEC_N * 2, "steps": e2e_steps,
                 "how": "per step: pinned H2D of x, w4a16_gemm, D2H of y; host wall clock"},
         "gpu_launches": 2 * steps,   # per call: the L2 prefetch grid and the GEMV grid
-        "clocks": clk.summary(),
+        "clocks": clocks,
         "sm_count": torch.cuda.get_device_properties(dev).multi_processor_count,
     }
     if not args.no_rows:
@@ -409,6 +447,35 @@ def bench_rows(dev, stream, bf16_tf, peak_kind, hbm_peak):
         "roofline": {"bound": "hbm", "achieved": round(qbytes / (t_q * 1e-3) / 1e9, 1), "peak": hbm_peak,
                      "unit": "GB/s", "frac": round(qbytes / (t_q * 1e-3) / 1e9 / hbm_peak, 4), "traffic": None,
                      "kernel": "quantize_groupwise_kernel", "algorithmic_bytes_per_launch": qbytes},
+    }
+    # tied embedding table used as the decode output head: one token against a
+    # 131072 x 2048 group-128 table (4 rotating copies, 604 MB, more than L2)
+    V, D, gh = 131072, 2048, 128
+    tabs = []
+    for c in range(4):
+        pk = on(np.tile(S.raw_u64(c, 97, 1024 * D // 16).view(np.uint8).reshape(1024, D // 2), (V // 1024, 1)))
+        scl = on(np.tile((0.002 + 0.001 * S.uniform(c, 98, 1024 * D // gh)).astype(np.float32).reshape(1024, D // gh),
+                         (V // 1024, 1)))
+        zr = on(np.tile((0.01 * S.normal(c, 99, 1024 * D // gh)).astype(np.float32).reshape(1024, D // gh),
+                        (V // 1024, 1)))
+        tabs.append((pk, scl, zr))
+    hh = bf16(S.activations_bf16(1, D, seed=0))
+    yh = torch.empty((1, V), dtype=torch.bfloat16, device=dev)
+    it = [0]
+
+    def head():
+        pk, scl, zr = tabs[it[0] % 4]
+        it[0] += 1
+        w4.w4_lm_head_gemv(hh, pk, scl, zr, gh, y=yh, stream=stream)
+
+    t_h = _time_graph(torch, stream, head, 8, 10)
+    hbytes = V * D // 2 + 2 * V * (D // gh) * 4 + D * 2 + V * 2
+    rows["lm_head_gemv"] = {
+        "config": {"M": 1, "V": V, "D": D, "group": gh, "scale_zero": "f32", "l2": "4 rotating tables (604 MB)"},
+        "value": round(hbytes / (t_h * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": t_h,
+        "roofline": {"bound": "hbm", "achieved": round(hbytes / (t_h * 1e-3) / 1e9, 1), "peak": hbm_peak,
+                     "unit": "GB/s", "frac": round(hbytes / (t_h * 1e-3) / 1e9 / hbm_peak, 4), "traffic": None,
+                     "kernel": "lm_head_kernel", "algorithmic_bytes_per_launch": hbytes},
     }
     rb = 64 * 2816 * 1024
     s4 = on((S.raw_u64(8, 80, rb // 8).view(np.uint8)))

@@ -265,6 +265,36 @@ w4_status w4_quantize_groupwise(const void* w, int32_t w_dtype, int64_t N, int64
  */
 w4_status w4_repack_s4_to_uint4b8(const void* src, void* dst, int64_t n_bytes, void* stream);
 
+/*
+ * Quantized embedding table used as the vocabulary lookup and as the tied
+ * output head ([OMNI] CPUInt4EmbeddingMethod: class docstring, embedding,
+ * tie_weights). The table is the output of w4_quantize_groupwise, kept row
+ * major and shared by both calls:
+ *     table  [V, D/2] uint8, two codes per byte, low nibble first
+ *     scale  [V, D/group] float32,  zero [V, D/group] float32
+ * group -1 means D. D and the group must be multiples of 8 (W4_ERR_ALIGN).
+ *
+ * w4_embedding_gather: out[t, :] = bf16((q[ids[t], :] - 8) * scale + zero),
+ * each fp32 step rounded as the page's fp32 code does (bit-exact). ids: [T]
+ * int32 device array; out: [T, D] bf16, 16-byte aligned. An id outside
+ * [0, V) gives a row of zeros and records W4_ERR_SHAPE in the device status
+ * word (w4_device_status). T == 0 does nothing.
+ */
+w4_status w4_embedding_gather(const int32_t* ids, int64_t T, const void* table, const float* scale,
+                              const float* zero, int64_t V, int64_t D, int32_t group, void* out, void* stream);
+
+/*
+ * w4_lm_head_gemv: the tied head for decode, logits y[m, v] =
+ * bf16(sum_d h[m, d] * ((q[v, d] - 8) * scale[v, d / group] + zero[v, d / group]))
+ * with fp32 accumulation, h [M, D] bf16, y [M, V] bf16, read from the same
+ * table (16-byte aligned). Built for small M (tokens in blocks of 8, each one
+ * pass over the table); D % 32 == 0 and D <= 5792 (8 rows of h and their
+ * per-word sums in shared memory), else W4_ERR_UNSUPPORTED. M == 0 does
+ * nothing.
+ */
+w4_status w4_lm_head_gemv(const void* h, int64_t M, const void* table, const float* scale, const float* zero,
+                          int64_t V, int64_t D, int32_t group, void* y, void* stream);
+
 /* Message for the last non-OK status returned to the calling thread ("" if none). */
 const char* w4_last_error(void);
 

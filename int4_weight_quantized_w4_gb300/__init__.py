@@ -18,6 +18,7 @@ __all__ = [
     "W4Error", "load", "library_path",
     "w4_quant_act_per_token", "w4a8_gemm", "w4a8_gemm_bf16in", "w4a8_gemm_noalloc", "w4a8_group_partials", "w4a16_gemm",
     "w4afp8_moe_grouped_gemm", "w4_quantize_groupwise", "w4_repack_s4_to_uint4b8",
+    "w4_embedding_gather", "w4_lm_head_gemv",
     "w4_device_status", "w4_selftest_bounded_wait",
     "W4_OK", "W4_ERR_NULL", "W4_ERR_ALIGN", "W4_ERR_GROUP", "W4_ERR_DTYPE",
     "W4_ERR_UNSUPPORTED", "W4_ERR_SHAPE", "W4_ERR_CUDA", "W4_ERR_TIMEOUT", "W4_ERR_WORKSPACE",
@@ -45,6 +46,8 @@ _SIGNATURES = {
     "w4afp8_moe_grouped_gemm": (_I32, [_P, _P, _P, _I32, _P, _P, _I32, _I32, _P, _I64, _I64, _I64, _P, _SZ, _P]),
     "w4_quantize_groupwise": (_I32, [_P, _I32, _I64, _I64, _I32, _P, _P, _P, _P]),
     "w4_repack_s4_to_uint4b8": (_I32, [_P, _P, _I64, _P]),
+    "w4_embedding_gather": (_I32, [_P, _I64, _P, _P, _P, _I64, _I64, _I32, _P, _P]),
+    "w4_lm_head_gemv": (_I32, [_P, _I64, _P, _P, _P, _I64, _I64, _I32, _P, _P]),
     "w4_last_error": (ctypes.c_char_p, []),
     "w4_status_string": (ctypes.c_char_p, [_I32]),
     "w4_device_status": (_I32, [_P]),
@@ -267,6 +270,35 @@ def w4_repack_s4_to_uint4b8(src, dst=None, stream=None):
     _check(load().w4_repack_s4_to_uint4b8(_ptr(src), _ptr(dst), n, _stream(stream, src.device)),
            "w4_repack_s4_to_uint4b8")
     return dst
+
+
+def w4_embedding_gather(ids, table, scale, zero, group: int, out=None, stream=None):
+    """Rows ``ids`` (int32 [T]) of the quantized table (packed uint8 [V, D/2],
+    f32 scale/zero [V, G]) dequantized to bf16 ``[T, D]``."""
+    if ids.dtype != torch.int32 or not ids.is_cuda:
+        raise ValueError("ids must be a CUDA int32 tensor")
+    _cuda2d(table, "table", (torch.uint8,))
+    V, D = table.shape[0], table.shape[1] * 2
+    T = ids.numel()
+    out = torch.empty((T, D), dtype=torch.bfloat16, device=table.device) if out is None else out
+    _check(load().w4_embedding_gather(_ptr(ids), T, _ptr(table), _ptr(scale), _ptr(zero), V, D, group, _ptr(out),
+                                      _stream(stream, table.device)), "w4_embedding_gather")
+    return out
+
+
+def w4_lm_head_gemv(h, table, scale, zero, group: int, y=None, stream=None):
+    """Tied output head: bf16 ``h [M, D]`` against the quantized table
+    (packed uint8 [V, D/2], f32 scale/zero [V, G]); returns bf16 ``[M, V]``."""
+    _cuda2d(h, "h", (torch.bfloat16,))
+    _cuda2d(table, "table", (torch.uint8,))
+    M, D = h.shape
+    V = table.shape[0]
+    if table.shape[1] * 2 != D:
+        raise ValueError("table and h disagree on D")
+    y = torch.empty((M, V), dtype=torch.bfloat16, device=h.device) if y is None else y
+    _check(load().w4_lm_head_gemv(_ptr(h), M, _ptr(table), _ptr(scale), _ptr(zero), V, D, group, _ptr(y),
+                                  _stream(stream, h.device)), "w4_lm_head_gemv")
+    return y
 
 
 def w4_device_status(stream=None, device=None) -> int:

@@ -289,6 +289,54 @@ w4_status w4_repack_s4_to_uint4b8(const void* src, void* dst, int64_t n_bytes, v
   return from_cuda(w4::launch_xor88(src, dst, n_bytes, static_cast<cudaStream_t>(stream)), "repack launch");
 }
 
+static w4_status check_table(int64_t V, int64_t D, int32_t group, int32_t* geff) {
+  if (V <= 0 || D <= 0) return fail(W4_ERR_SHAPE, "table sizes must be V > 0, D > 0 (V=%lld D=%lld)", (long long)V,
+                                    (long long)D);
+  const int64_t g = group == -1 ? D : group;
+  if (g <= 0 || D % g != 0 || g > INT32_MAX)
+    return fail(W4_ERR_GROUP, "group %d must be -1 or a positive divisor of D=%lld", group, (long long)D);
+  if (D % 8 != 0 || g % 8 != 0)
+    return fail(W4_ERR_ALIGN, "D and the group must be multiples of 8 (D=%lld group=%lld)", (long long)D,
+                (long long)g);
+  *geff = static_cast<int32_t>(g);
+  return W4_OK;
+}
+
+w4_status w4_embedding_gather(const int32_t* ids, int64_t T, const void* table, const float* scale,
+                              const float* zero, int64_t V, int64_t D, int32_t group, void* out, void* stream) {
+  int32_t g = 0;
+  w4_status st = check_table(V, D, group, &g);
+  if (st != W4_OK) return st;
+  if (T < 0) return fail(W4_ERR_SHAPE, "T must be >= 0");
+  if (T == 0) return ok();
+  if (!ids || !table || !scale || !zero || !out) return fail(W4_ERR_NULL, "ids, table, scale, zero, out must be non-NULL");
+  if (!aligned(ids, 4) || !aligned(table, 4) || !aligned(scale, 4) || !aligned(zero, 4) || !aligned(out, 16))
+    return fail(W4_ERR_ALIGN, "out must be 16-byte aligned; ids, table, scale, zero 4-byte aligned");
+  unsigned int* status = nullptr;
+  cudaError_t e = status_ptr(&status);
+  if (e != cudaSuccess) return from_cuda(e, "device status word");
+  return from_cuda(w4::launch_embedding_gather(ids, T, table, scale, zero, V, D, g, out, status,
+                                               static_cast<cudaStream_t>(stream)),
+                   "embedding gather launch");
+}
+
+w4_status w4_lm_head_gemv(const void* h, int64_t M, const void* table, const float* scale, const float* zero,
+                          int64_t V, int64_t D, int32_t group, void* y, void* stream) {
+  int32_t g = 0;
+  w4_status st = check_table(V, D, group, &g);
+  if (st != W4_OK) return st;
+  if (M < 0) return fail(W4_ERR_SHAPE, "M must be >= 0");
+  if (D % 32 != 0) return fail(W4_ERR_UNSUPPORTED, "the head reads rows 32 codes at a time: D=%lld", (long long)D);
+  if (D * 40 > 227 * 1024)   // 8 rows of h padded to 36 floats per 32, plus D/8 word sums each
+    return fail(W4_ERR_UNSUPPORTED, "the head keeps 8 rows of h in shared memory: D=%lld is too long", (long long)D);
+  if (M == 0) return ok();
+  if (!h || !table || !scale || !zero || !y) return fail(W4_ERR_NULL, "h, table, scale, zero, y must be non-NULL");
+  if (!aligned(h, 2) || !aligned(table, 16) || !aligned(scale, 4) || !aligned(zero, 4) || !aligned(y, 2))
+    return fail(W4_ERR_ALIGN, "table must be 16-byte aligned; scale, zero 4-byte; h, y 2-byte");
+  return from_cuda(w4::launch_lm_head(h, M, table, scale, zero, V, D, g, y, static_cast<cudaStream_t>(stream)),
+                   "lm_head launch");
+}
+
 w4_status w4_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return from_cuda(e, "cudaStreamSynchronize");

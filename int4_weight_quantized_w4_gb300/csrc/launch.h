@@ -61,6 +61,11 @@ cudaError_t launch_w4afp8_experts(const W4A8Args& a, cudaStream_t s);
 cudaError_t launch_quantize_groupwise(const void* w, bool f16, int64_t N, int64_t K, int32_t group, uint8_t* packed,
                                       float* scale, float* zero, cudaStream_t s);
 cudaError_t launch_xor88(const void* src, void* dst, int64_t n_bytes, cudaStream_t s);
+cudaError_t launch_embedding_gather(const int32_t* ids, int64_t T, const void* table, const float* scale,
+                                    const float* zero, int64_t V, int64_t D, int32_t group, void* out,
+                                    unsigned int* status, cudaStream_t s);
+cudaError_t launch_lm_head(const void* h, int64_t M, const void* table, const float* scale, const float* zero,
+                           int64_t V, int64_t D, int32_t group, void* y, cudaStream_t s);
 cudaError_t launch_bounded_wait_selftest(long long limit, unsigned int* status, cudaStream_t s);
 
 }  // namespace w4

@@ -52,7 +52,7 @@ __all__ = [
     "quant_int8_per_token", "quant_fp8_per_token",
     "w4a8_group_partials", "w4a8_linear",
     "w4a16_linear", "moe_grouped_linear",
-    "quantize_groupwise", "dequant_rows",
+    "quantize_groupwise", "dequant_rows", "embedding_rows", "lm_head_logits",
 ]
 
 # ---------------------------------------------------------------------------
@@ -370,3 +370,28 @@ def dequant_rows(codes: np.ndarray, scale: np.ndarray, zero: np.ndarray, group: 
     s = np.repeat(np.asarray(scale, dtype=np.float64), group, axis=1)
     z = np.repeat(np.asarray(zero, dtype=np.float64), group, axis=1)
     return (c - 8.0) * s + z
+
+
+def embedding_rows(packed: np.ndarray, scale: np.ndarray, zero: np.ndarray, group: int, ids) -> np.ndarray:
+    """[OMNI] ``CPUInt4EmbeddingMethod.embedding``: the rows ``ids`` of the
+    packed table ``[V, D/2]`` dequantized in float32, step by step as the page
+    does (codes as float32, minus 8, times the row's group scale, plus its
+    zero), then rounded to bf16. Returns bf16 bits ``[T, D]``."""
+    ids = np.asarray(ids, dtype=np.int64).reshape(-1)
+    codes = unpack_nibbles(np.asarray(packed)[ids]).astype(np.float32)
+    n, k = codes.shape
+    sc = np.asarray(scale, dtype=np.float32)[ids][:, :, None]
+    ze = np.asarray(zero, dtype=np.float32)[ids][:, :, None]
+    deq = (codes.reshape(n, k // group, group) - np.float32(8.0)) * sc + ze
+    return f32_to_bf16_bits(deq.reshape(n, k).astype(np.float32))
+
+
+def lm_head_logits(h_bits: np.ndarray, packed: np.ndarray, scale: np.ndarray, zero: np.ndarray,
+                   group: int) -> np.ndarray:
+    """[OMNI] ``CPUInt4EmbeddingMethod.tie_weights``: the output head reads the
+    same quantized table, ``logits = h . W^T`` with
+    ``W[v, d] = (q - 8) * scale + zero``. Float64 sums of exact float64
+    products (a library matmul: the float64 result is the stated precision);
+    returns the float32 result ``r`` ``[M, V]``."""
+    w = dequant_rows(unpack_nibbles(np.asarray(packed)), scale, zero, group)     # [V, D] float64
+    return (bf16_to_f64(h_bits) @ w.T).astype(np.float32)

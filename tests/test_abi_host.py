@@ -175,3 +175,29 @@ def test_w4a8_bf16in_validation(lib):
     assert call(K=264, group=-1) == w4.W4_ERR_UNSUPPORTED
     assert call(work=None) == w4.W4_ERR_WORKSPACE
     assert call(M=0) == w4.W4_OK
+
+
+def test_embedding_validation(lib):
+    def gat(**kw):
+        a = dict(ids=FAKE, T=4, table=FAKE, sc=FAKE, z=FAKE, V=100, D=256, group=128, out=FAKE)
+        a.update(kw)
+        return lib.w4_embedding_gather(a["ids"], a["T"], a["table"], a["sc"], a["z"], a["V"], a["D"], a["group"],
+                                       a["out"], None)
+    assert gat(group=96) == w4.W4_ERR_GROUP
+    assert gat(D=252, group=-1) == w4.W4_ERR_ALIGN
+    assert gat(V=0) == w4.W4_ERR_SHAPE
+    assert gat(ids=None) == w4.W4_ERR_NULL
+    assert gat(out=ODD) == w4.W4_ERR_ALIGN
+    assert gat(T=0) == w4.W4_OK
+
+    def head(**kw):
+        a = dict(h=FAKE, M=1, table=FAKE, sc=FAKE, z=FAKE, V=100, D=256, group=128, y=FAKE)
+        a.update(kw)
+        return lib.w4_lm_head_gemv(a["h"], a["M"], a["table"], a["sc"], a["z"], a["V"], a["D"], a["group"],
+                                   a["y"], None)
+    assert head(D=264, group=-1) == w4.W4_ERR_UNSUPPORTED      # rows read 32 codes at a time
+    assert head(D=8192, group=128) == w4.W4_ERR_UNSUPPORTED    # 8 rows of h must fit in shared memory
+    assert head(D=5792, group=32, M=0) == w4.W4_OK            # the longest row that fits
+    assert head(D=5824, group=32, M=0) == w4.W4_ERR_UNSUPPORTED
+    assert head(table=ODD) == w4.W4_ERR_ALIGN
+    assert head(M=0) == w4.W4_OK

@@ -436,3 +436,44 @@ def test_quantize_groupwise_reproduces_extremes():
     np.testing.assert_allclose(d.min(axis=2), g.min(axis=2), rtol=0, atol=4e-6)
     np.testing.assert_allclose(d.max(axis=2), g.max(axis=2), rtol=0, atol=4e-6)
     assert np.all(np.abs(deq - w) <= np.repeat(scale, 32, axis=1) * 0.5 + 1e-6)
+
+
+def test_embedding_rows_within_the_quantization_error():
+    """[OMNI] embedding: a gathered row dequantizes to within half a scale step
+    (plus bf16 rounding) of the weights quantize_groupwise was given, and
+    each group's extremes come back to within bf16 rounding."""
+    V, D, g = 12, 128, 32
+    w = (S.normal(3, 4, V * D).reshape(V, D) * 0.2).astype(np.float32)
+    q, sc, z = O.quantize_groupwise(w, g)
+    ids = [5, 0, 11, 5]
+    e = S.bf16_bits_to_f32(O.embedding_rows(O.pack_nibbles(q), sc, z, g, ids)).astype(np.float64)
+    ref = w[ids].astype(np.float64)
+    step = np.repeat(sc[ids], g, axis=1).astype(np.float64)
+    assert np.all(np.abs(e - ref) <= 0.5 * step * (1 + 1e-6) + np.abs(ref) * 2.0 ** -8 + 1e-12)
+    for t, v in enumerate(ids):
+        for gi in range(D // g):
+            blk = slice(gi * g, (gi + 1) * g)
+            i_max, i_min = np.argmax(w[v, blk]), np.argmin(w[v, blk])
+            assert abs(e[t, blk][i_max] - w[v, blk][i_max]) <= abs(w[v, blk][i_max]) * 2.0 ** -8 + 1e-7
+            assert abs(e[t, blk][i_min] - w[v, blk][i_min]) <= abs(w[v, blk][i_min]) * 2.0 ** -8 + 1e-7
+
+
+def test_lm_head_one_hot_reads_a_table_column():
+    """A one-hot h at column d gives logits equal to column d of the
+    dequantized table, for every vocabulary row (pins the transposition and
+    the group indexing); a constant code 8 table gives logits = sum_d h * zero."""
+    V, D, g = 9, 64, 16
+    codes = (S.raw_u64(5, 6, V * D) >> np.uint64(60)).astype(np.uint8).reshape(V, D)
+    sc = (0.01 + 0.01 * S.uniform(5, 7, V * (D // g))).astype(np.float32).reshape(V, D // g)
+    z = (0.1 * S.normal(5, 8, V * (D // g))).astype(np.float32).reshape(V, D // g)
+    packed = O.pack_nibbles(codes)
+    for d in (0, 17, 63):
+        h = np.zeros((1, D), np.float32)
+        h[0, d] = 1.0
+        r = O.lm_head_logits(S.to_bf16_bits(h), packed, sc, z, g)
+        col = (codes[:, d].astype(np.float64) - 8.0) * sc[:, d // g] + z[:, d // g]
+        assert np.allclose(r[0], col.astype(np.float32), rtol=0, atol=0)
+    h = S.activations_bf16(2, D, seed=9)
+    r = O.lm_head_logits(h, O.pack_nibbles(np.full((V, D), 8, np.uint8)), sc, z, g)
+    hz = S.bf16_bits_to_f32(h).astype(np.float64).reshape(2, D // g, g).sum(-1)      # [2, G]
+    assert np.allclose(r, (hz @ z.astype(np.float64).T).astype(np.float32), rtol=1e-6, atol=1e-7)
