@@ -34,6 +34,17 @@ Readings where the pages are silent (each is listed in the design notes):
     ``w = (q - 8) * scale + zero``.
   * Outputs are the fp32 result ``r`` of the exact (fp64) computation; the
     stored bf16 output is ``r`` rounded to nearest even.
+  * The MoE layer around the grouped GEMM ([FP8] module docstring and
+    ``get_quant_method``: the int4 weights serve the routed experts; no
+    routing or activation formula is printed). Reading, the plain top-k MoE
+    layer: per token a softmax over the router logits; the k experts with the
+    largest logits (ties to the lower expert index); weight = the softmax
+    value, divided by the sum over the k chosen when renormalizing. Rows
+    (token, expert) sorted by expert, then token. Between the GEMMs
+    ``act = silu(gate) * up`` with ``gate`` the first half of the gate_up
+    output columns, computed in fp32 and rounded to bf16, then quantized per
+    row to e4m3 as the first GEMM's input was. The output of token t is
+    ``sum_j w[t, j] * y[row(t, j)]``.
 
 Parity pins: every function here is pinned by ``tests/test_oracle_pins.py``
 against values fixed by the pages or by mathematics (exhaustive layout checks,
@@ -53,6 +64,7 @@ __all__ = [
     "w4a8_group_partials", "w4a8_linear",
     "w4a16_linear", "moe_grouped_linear",
     "quantize_groupwise", "dequant_rows", "embedding_rows", "lm_head_logits",
+    "moe_route", "moe_gather_quant_fp8", "silu_mul_bf16", "silu_mul_quant_fp8", "moe_combine",
 ]
 
 # ---------------------------------------------------------------------------
@@ -395,3 +407,89 @@ def lm_head_logits(h_bits: np.ndarray, packed: np.ndarray, scale: np.ndarray, ze
     returns the float32 result ``r`` ``[M, V]``."""
     w = dequant_rows(unpack_nibbles(np.asarray(packed)), scale, zero, group)     # [V, D] float64
     return (bf16_to_f64(h_bits) @ w.T).astype(np.float32)
+
+
+# ---------------------------------------------------------------------------
+# the MoE layer around the grouped GEMM ([FP8] routed experts; readings in the
+# module docstring)
+# ---------------------------------------------------------------------------
+
+def moe_route(logits: np.ndarray, top_k: int, renormalize: bool):
+    """Top-k routing and the expert-sorted row order.
+
+    ``logits`` ``[T, E]`` (float32 values). Per token the k experts are taken
+    by a plain selection on the logits themselves (the softmax is monotone, so
+    this is its top-k), largest first, equal logits in ascending expert order.
+    The weight of a chosen expert is its softmax probability in float64
+    (``exp(l - max) / sum exp(l - max)``); with ``renormalize`` the k weights
+    are divided by their sum. Rows are the pairs (t, j) listed by expert, then
+    by token.
+
+    Returns ``(ids int32 [T,k], weights float32 [T,k], offsets int32 [E+1],
+    row_token int32 [T*k], row_of int32 [T,k])``: expert e owns rows
+    ``offsets[e] .. offsets[e+1]-1``, ``row_token[r]`` is the token of row r
+    and ``row_of[t, j]`` the row of token t's j-th choice.
+    """
+    lg = np.asarray(logits, dtype=np.float32).astype(np.float64)
+    T, E = lg.shape
+    ids = np.zeros((T, top_k), dtype=np.int32)
+    wts = np.zeros((T, top_k), dtype=np.float32)
+    for t in range(T):
+        order = sorted(range(E), key=lambda e: (-lg[t, e], e))[:top_k]
+        ex = np.exp(lg[t] - lg[t].max())
+        p = ex[order] / ex.sum()
+        if renormalize:
+            p = p / p.sum()
+        ids[t] = order
+        wts[t] = p
+    counts = np.bincount(ids.reshape(-1), minlength=E)
+    offsets = np.zeros(E + 1, dtype=np.int32)
+    offsets[1:] = np.cumsum(counts)
+    # every (expert, token, choice) triple, listed by expert, then token
+    pairs = sorted((int(ids[t, j]), t, j) for t in range(T) for j in range(top_k))
+    row_token = np.zeros(T * top_k, dtype=np.int32)
+    row_of = np.zeros((T, top_k), dtype=np.int32)
+    for r, (_, t, j) in enumerate(pairs):
+        row_token[r] = t
+        row_of[t, j] = r
+    return ids, wts, offsets, row_token, row_of
+
+
+def moe_gather_quant_fp8(x_bits: np.ndarray, row_token: np.ndarray):
+    """The first GEMM's input: row r is token ``row_token[r]`` of ``x`` [T, K],
+    quantized per row to e4m3 (``quant_fp8_per_token``)."""
+    rows = np.asarray(x_bits)[np.asarray(row_token, dtype=np.int64)]
+    return quant_fp8_per_token(rows)
+
+
+def silu_mul_bf16(h_bits: np.ndarray) -> np.ndarray:
+    """``act = silu(gate) * up`` for a gate_up output ``[R, 2I]`` (bf16 bits):
+    gate = columns ``[0, I)``, up = ``[I, 2I)``, ``silu(g) = g / (1 + e^-g)``.
+    Evaluated in float64, rounded to float32, then to bf16 bits ``[R, I]``."""
+    h = bf16_to_f64(h_bits)
+    i = h.shape[1] // 2
+    g, u = h[:, :i], h[:, i:]
+    act = g / (1.0 + np.exp(-g)) * u
+    return f32_to_bf16_bits(act.astype(np.float32))
+
+
+def silu_mul_quant_fp8(h_bits: np.ndarray):
+    """The second GEMM's input: ``silu_mul_bf16`` then the per-row e4m3
+    quantization. Returns ``(q uint8 [R, I], s float32 [R], act bf16 bits)``."""
+    act = silu_mul_bf16(h_bits)
+    q, sc = quant_fp8_per_token(act)
+    return q, sc, act
+
+
+def moe_combine(y_bits: np.ndarray, weights: np.ndarray, row_of: np.ndarray) -> np.ndarray:
+    """Token outputs ``out[t] = sum_j w[t, j] * y[row_of[t, j]]`` from the
+    second GEMM's bf16 rows ``[R, H]``; float64 sums, returned as float32
+    ``[T, H]``."""
+    y = bf16_to_f64(y_bits)
+    w = np.asarray(weights, dtype=np.float32).astype(np.float64)
+    ro = np.asarray(row_of, dtype=np.int64)
+    T, k = ro.shape
+    out = np.zeros((T, y.shape[1]))
+    for j in range(k):
+        out += w[:, j:j + 1] * y[ro[:, j]]
+    return out.astype(np.float32)

@@ -124,25 +124,9 @@ def fp8_codes(shape, seed: int = 0, tag: int = 60) -> np.ndarray:
     return c.reshape(shape)
 
 
-def moe_routing(tokens: int, experts: int, topk: int, seed: int = 5):
-    """Top-k routing from a softmax over N(0,1) router logits.
-
-    Returns ``(token_of_row, expert_of_row, offsets)``: rows are the (token,
-    expert) pairs sorted by expert, then by token (stable), and ``offsets`` is
-    the int32 ``[E+1]`` prefix of rows per expert. Softmax is monotone, so the
-    top-k of the softmax equals the top-k of the logits; ties go to the lower
-    expert index.
-    """
-    logits = normal(seed, 70, tokens * experts).reshape(tokens, experts)
-    order = np.argsort(-logits, axis=1, kind="stable")[:, :topk]
-    tok = np.repeat(np.arange(tokens, dtype=np.int64), topk)
-    exp = order.reshape(-1).astype(np.int64)
-    perm = np.lexsort((tok, exp))
-    tok, exp = tok[perm], exp[perm]
-    counts = np.bincount(exp, minlength=experts)
-    offsets = np.zeros(experts + 1, dtype=np.int32)
-    offsets[1:] = np.cumsum(counts)
-    return tok, exp, offsets
+def router_logits(tokens: int, experts: int, seed: int = 5) -> np.ndarray:
+    """MoE router logits ``[tokens, experts]``: N(0,1) rounded to float32."""
+    return normal(seed, 70, tokens * experts).reshape(tokens, experts).astype(np.float32)
 
 
 def offsets_from_counts(counts) -> np.ndarray:

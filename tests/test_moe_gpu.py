@@ -41,7 +41,7 @@ def test_moe_routed_layer_from_bf16():
     """Seeded top-8 routing of 64 tokens over 16 experts; fp8 quantization on
     the GPU, then the grouped GEMM, against the oracle's quantizer and GEMM."""
     T, E, top, N, K, g = 64, 16, 8, 256, 512, 128
-    tok, exp, off = S.moe_routing(T, E, top, seed=5)
+    _, _, off, tok, _ = O.moe_route(S.router_logits(T, E, seed=5), top, False)
     x_tok = S.activations_bf16(T, K, seed=0)
     xb = x_tok[tok]
     qw = S.random_words((E, N, K // 8), seed=1)
@@ -72,7 +72,7 @@ def test_moe_full_size(N, K):
     """4096 tokens, 64 experts, top-8 (32768 rows): the gate_up (K=2048,
     N=2816) and down (K=1408, N=2048) projections; sampled rows."""
     T, E, top, g = 4096, 64, 8, 128
-    tok, exp, off = S.moe_routing(T, E, top, seed=5)
+    _, _, off, _, _ = O.moe_route(S.router_logits(T, E, seed=5), top, False)
     R = T * top
     xb = S.activations_bf16(R, K, seed=11 + K)
     qx8, sx = O.quant_fp8_per_token(xb)

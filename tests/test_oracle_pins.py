@@ -411,12 +411,101 @@ def test_moe_empty_experts_and_permutation():
     np.testing.assert_array_equal(O.moe_grouped_linear(qx8, sx, off, qw, sw, g, rows=sub), r[sub])
 
 
-def test_moe_routing_structure():
-    tok, exp, off = S.moe_routing(64, 16, 4, seed=5)
-    assert off[0] == 0 and off[-1] == 64 * 4 and np.all(np.diff(off) >= 0)
-    assert np.all(np.diff(exp) >= 0)
-    for t in range(64):
-        assert len(set(exp[tok == t])) == 4
+def test_moe_route_worked_example():
+    """tests/golden/moe_route_worked.txt, worked by hand: selection order, the
+    tie to the lower expert index, renormalized weights, the expert-then-token
+    row order and its inverse."""
+    g = {k: v for k, v in _golden_rows("moe_route_worked.txt")}
+    lg = np.array([[1, 3, 2, 0], [0, 0, 0, 0], [5, -1, 5, 2]], np.float32)
+    ids, w, off, rt, ro = O.moe_route(lg, 2, True)
+    np.testing.assert_array_equal(ids.reshape(-1), [int(v) for v in g["ids"].split()])
+    np.testing.assert_allclose(w.reshape(-1), [float(v) for v in g["weights"].split()], rtol=1e-7)
+    np.testing.assert_array_equal(off, [int(v) for v in g["offsets"].split()])
+    np.testing.assert_array_equal(rt, [int(v) for v in g["row_token"].split()])
+    np.testing.assert_array_equal(ro.reshape(-1), [int(v) for v in g["row_of"].split()])
+
+
+@pytest.mark.parametrize("renorm", [False, True])
+def test_moe_route_properties(renorm):
+    """For random logits: no unchosen expert beats a chosen one; the chosen are
+    listed by falling logit; 1 / w equals sum_e exp(l_e - l_chosen) (softmax
+    written the other way round), or the k weights sum to 1 with ratios
+    exp(l_i - l_j) when renormalized; the rows form a bijection with the
+    (token, choice) pairs, sorted by expert, then token."""
+    T, E, k = 37, 11, 3
+    lg = S.router_logits(T, E, seed=12)
+    lg[5, :] = lg[5, 0]                              # a fully tied token
+    ids, w, off, rt, ro = O.moe_route(lg, k, renorm)
+    l64 = lg.astype(np.float64)
+    for t in range(T):
+        ch = list(ids[t])
+        rest = [e for e in range(E) if e not in ch]
+        assert min(lg[t, ch]) >= max(lg[t, rest])
+        for a, b in zip(ch, ch[1:]):
+            assert lg[t, a] > lg[t, b] or (lg[t, a] == lg[t, b] and a < b)
+        if renorm:
+            assert abs(w[t].astype(np.float64).sum() - 1.0) < 1e-6
+            assert np.allclose(w[t][0] / w[t][1:], np.exp(l64[t, ch[0]] - l64[t, ch[1:]]), rtol=1e-6)
+        else:
+            inv = np.exp(l64[t][None, :] - l64[t, ch][:, None]).sum(axis=1)
+            assert np.allclose(w[t] * inv, 1.0, rtol=1e-6)
+    np.testing.assert_array_equal(ids[5], np.arange(k))
+    assert off[0] == 0 and off[-1] == T * k
+    np.testing.assert_array_equal(np.diff(off), np.bincount(ids.reshape(-1), minlength=E))
+    assert sorted(ro.reshape(-1).tolist()) == list(range(T * k))
+    for t in range(T):
+        for j in range(k):
+            r = ro[t, j]
+            assert rt[r] == t
+            assert off[ids[t, j]] <= r < off[ids[t, j] + 1]
+    for e in range(E):
+        assert np.all(np.diff(rt[off[e]:off[e + 1]]) > 0)
+
+
+def test_silu_mul_values_and_halves():
+    """silu(g) * u with g from the first half: g = 1, u = 2 gives
+    2 / (1 + e^-1) = 1.46211716 (swapped halves would give silu(2) = 1.76);
+    silu(0) = 0; silu(20) rounds to 20; and silu(x) - silu(-x) = x."""
+    def h(g, u):
+        return S.to_bf16_bits(np.array([list(g) + list(u)], np.float32))
+    a = S.bf16_bits_to_f32(O.silu_mul_bf16(h([1.0, 0.0, 20.0], [2.0, 5.0, 1.0])))[0]
+    assert a[0] == S.bf16_bits_to_f32(S.to_bf16_bits(np.array([1.4621171572600098], np.float32)))[0]
+    assert a[1] == 0.0 and a[2] == 20.0
+    x = S.bf16_bits_to_f32(S.activations_bf16(1, 64, seed=13))[0]
+    pos = S.bf16_bits_to_f32(O.silu_mul_bf16(h(x, np.ones(64))))[0].astype(np.float64)
+    neg = S.bf16_bits_to_f32(O.silu_mul_bf16(h(-x, np.ones(64))))[0].astype(np.float64)
+    bound = (np.abs(pos) + np.abs(neg)) * 2.0 ** -8
+    assert np.all(np.abs(pos - neg - x) <= bound + 1e-30)
+
+
+def test_silu_mul_quant_round_trip():
+    """The requantized activations decode to within half an e4m3 step of the
+    bf16 activations, and the row maximum maps to 448."""
+    hb = S.activations_bf16(6, 2 * 96, seed=14)
+    q, sc, act = O.silu_mul_quant_fp8(hb)
+    a = S.bf16_bits_to_f32(act).astype(np.float64)
+    d = O.e4m3_decode(q) * sc[:, None].astype(np.float64)
+    assert np.all(np.abs(d - a) <= np.abs(a) * 2.0 ** -4 + sc[:, None] * 2.0 ** -9 + 1e-30)
+    am = np.abs(a).max(axis=1)
+    np.testing.assert_array_equal(np.abs(O.e4m3_decode(q)).max(axis=1), 448.0)
+    np.testing.assert_array_equal(sc, (am / 448.0).astype(np.float32))
+
+
+def test_moe_combine_bruteforce():
+    """k = 1 with weight 1 copies y's rows; in general each output element is
+    the k-term weighted sum, computed here one element at a time."""
+    T, k, H, R = 5, 3, 7, 15
+    y = S.activations_bf16(R, H, seed=15)
+    ro = np.arange(R, dtype=np.int32)[::-1].reshape(T, k).copy()
+    w = S.uniform(16, 1, T * k).reshape(T, k).astype(np.float32)
+    out = O.moe_combine(y, w, ro)
+    yf = S.bf16_bits_to_f32(y).astype(np.float64)
+    for t in range(T):
+        for hh in range(H):
+            ref = sum(float(w[t, j]) * yf[ro[t, j], hh] for j in range(k))
+            assert out[t, hh] == np.float32(ref)
+    one = O.moe_combine(y, np.ones((R, 1), np.float32), np.arange(R, dtype=np.int32)[:, None])
+    np.testing.assert_array_equal(one, S.bf16_bits_to_f32(y))
 
 
 # ---------------------------------------------------------------------------
