@@ -386,50 +386,74 @@ def bench_rows(dev, stream, bf16_tf, peak_kind, hbm_peak):
     dense("w4a8_prefill", 4096, 11008, 4096, 128, 0.01)
     dense("w4a8_diffusion", 16384, 3072, 3072, -1, 0.0)
 
-    # grouped experts: 4096 tokens, 64 experts, top-8
-    T, E, top, g = 4096, 64, 8, 128
-    tok, exp, off = S.moe_routing(T, E, top, seed=5)
+    # the routed MoE layer: 4096 tokens, hidden 2048, 64 experts, top-8,
+    # intermediate 1408 (gate_up N = 2816, down K = 1408)
+    T, E, top, g, Hd, I = 4096, 64, 8, 128, 2048, 1408
     R = T * top
-    off_d = on(off)
-    shapes = {"gate_up": (2048, 2816), "down": (1408, 2048)}
-    bufs = {}
-    for nm, (K, N) in shapes.items():
-        x = bf16(S.activations_bf16(R, K, seed=3 if nm == "down" else 0))
-        bufs[nm] = dict(
-            K=K, N=N, x=x,
-            qw=on(S.random_words((E, N, K // 8), seed=1)), sw=on(S.scales_f16((E, N, K // g), seed=2)),
-            q=torch.empty((R, K), dtype=torch.float8_e4m3fn, device=dev), s=torch.empty((R,), dtype=torch.float32, device=dev),
-            y=torch.empty((R, N), dtype=torch.bfloat16, device=dev),
-            ws=torch.empty((w4.w4_workspace_bytes(w4.W4_OP_W4AFP8_MOE, R, N, K, g),), dtype=torch.uint8, device=dev))
+    lg = on(S.router_logits(T, E, seed=5))
+    xt = bf16(S.activations_bf16(T, Hd, seed=0))
+    w1, s1 = on(S.random_words((E, 2 * I, Hd // 8), seed=1)), on(S.scales_f16((E, 2 * I, Hd // g), seed=2))
+    w2 = on(S.random_words((E, Hd, I // 8), seed=1, tag=21))
+    s2 = on(S.scales_f16((E, Hd, I // g), seed=2, tag=31))
+    route = w4.w4_moe_route(lg, top, True)
+    ids, wts, off, rt, ro = route
+    h1 = torch.empty((R, 2 * I), dtype=torch.bfloat16, device=dev)
+    sx1 = torch.empty((R,), dtype=torch.float32, device=dev)
+    qa = torch.empty((R, I), dtype=torch.float8_e4m3fn, device=dev)
+    sa = torch.empty((R,), dtype=torch.float32, device=dev)
+    y2 = torch.empty((R, Hd), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((T, Hd), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty((max(w4.w4_workspace_bytes(w4.W4_OP_W4AFP8_MOE, R, 2 * I, Hd, g),
+                          w4.w4_workspace_bytes(w4.W4_OP_W4AFP8_MOE, R, Hd, I, g)),), dtype=torch.uint8, device=dev)
+    rws = torch.empty((max(16, w4.w4_workspace_bytes(w4.W4_OP_MOE_ROUTE, T, E, 1, 0)),), dtype=torch.uint8,
+                      device=dev)
 
-    def moe_step():
-        for nm in ("gate_up", "down"):
-            b = bufs[nm]
-            w4.w4_quant_act_per_token(b["x"], "fp8", q=b["q"], scale=b["s"], stream=stream)
-            w4.w4afp8_moe_grouped_gemm(b["q"], b["s"], off_d, b["qw"], b["sw"], g, y=b["y"], workspace=b["ws"],
-                                       stream=stream)
+    def st_route():
+        w4.w4_moe_route(lg, top, True, out=route, workspace=rws, stream=stream)
 
-    def moe_gemms():
-        for nm in ("gate_up", "down"):
-            b = bufs[nm]
-            w4.w4afp8_moe_grouped_gemm(b["q"], b["s"], off_d, b["qw"], b["sw"], g, y=b["y"], workspace=b["ws"],
-                                       stream=stream)
+    def st_gate_up():
+        w4.w4afp8_moe_gemm_bf16in(xt, rt, off, w1, s1, g, y=h1, x_scale=sx1, workspace=ws, stream=stream)
 
-    t_step = _time_graph(torch, stream, moe_step, 3, 10)
-    t_gemm = _time_graph(torch, stream, moe_gemms, 3, 10)
-    flops = sum(2.0 * R * N * K for K, N in shapes.values())
+    def st_act():
+        w4.w4_moe_silu_mul_quant_fp8(h1, q=qa, scale=sa, stream=stream)
+
+    def st_down():
+        w4.w4afp8_moe_grouped_gemm(qa, sa, off, w2, s2, g, y=y2, workspace=ws, stream=stream)
+
+    def st_combine():
+        w4.w4_moe_combine(y2, wts, ro, out=out, stream=stream)
+
+    def moe_layer():
+        st_route()
+        st_gate_up()
+        st_act()
+        st_down()
+        st_combine()
+
+    t_layer = _time_graph(torch, stream, moe_layer, 3, 10)
+    t_st = {nm: _time_graph(torch, stream, fn, 3, 10) for nm, fn in
+            (("route", st_route), ("gate_up", st_gate_up), ("act", st_act), ("down", st_down),
+             ("combine", st_combine))}
+    flops = 2.0 * R * (2 * I) * Hd + 2.0 * R * Hd * I
+    t_gemm = t_st["gate_up"] + t_st["down"]
     tf_gemm = flops / (t_gemm * 1e-3) / 1e12
+    act_bytes = R * 2 * I * 2 + R * I + R * 4
+    comb_bytes = R * Hd * 2 + T * top * 8 + T * Hd * 2
     rows["w4afp8_moe"] = {
-        "config": {"tokens": T, "experts": E, "top_k": top, "rows": R, "gate_up": [2048, 2816], "down": [1408, 2048],
-                   "group": g},
-        "value": round(flops / (t_step * 1e-3) / 1e12, 1), "unit": "TFLOP/s", "ms_per_step": t_step,
-        "step": "fp8 quantization + grouped GEMM, gate_up then down",
-        "gemm_ms": t_gemm, "gemm_tflops": round(tf_gemm, 1),
+        "config": {"tokens": T, "hidden": Hd, "experts": E, "top_k": top, "intermediate": I, "rows": R,
+                   "gate_up": [Hd, 2 * I], "down": [I, Hd], "group": g, "renormalize": True},
+        "value": round(flops / (t_layer * 1e-3) / 1e12, 1), "unit": "TFLOP/s", "ms_per_step": t_layer,
+        "step": "the whole routed layer: route, gather + fp8 quant + gate_up GEMM, SiLU*up + fp8 requant, "
+                "down GEMM, weighted combine",
+        "stage_ms": {k: round(v, 5) for k, v in t_st.items()},
+        "gemm_tflops": round(tf_gemm, 1),
+        "act_gbs": round(act_bytes / (t_st["act"] * 1e-3) / 1e9, 1),
+        "combine_gbs": round(comb_bytes / (t_st["combine"] * 1e-3) / 1e9, 1),
         "roofline": {"bound": "tensor", "achieved": round(tf_gemm, 1), "peak": bf16_tf, "unit": "TFLOP/s",
                      "frac": round(tf_gemm / bf16_tf, 4), "traffic": None,
                      "peak_source": f"{peak_kind} bf16_tflops (e4m3 activations widened to exact fp16; "
                                     "fp16 tensor datapath)",
-                     "kernel": "w4afp8_moe_grouped_gemm call = widen_kernel + w4a8_tc_kernel"},
+                     "kernel": "the two grouped GEMM calls (quantize/widen + w4a8_tc_kernel each)"},
     }
     # weight-side tools (load time): the group quantizer on a 14336 x 4096 bf16
     # weight, and the XOR 0x88 repack of a 64-expert [E, N, K/2] int4 tensor

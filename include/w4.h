@@ -71,7 +71,8 @@ typedef enum {
 /* Operations that take a workspace (see w4_workspace_bytes). */
 typedef enum {
   W4_OP_W4A8 = 0,           /* w4a8_gemm and w4a8_group_partials */
-  W4_OP_W4AFP8_MOE = 1      /* w4afp8_moe_grouped_gemm (M = R, the row count) */
+  W4_OP_W4AFP8_MOE = 1,     /* w4afp8_moe_grouped_gemm, w4afp8_moe_gemm_bf16in (M = R, the row count) */
+  W4_OP_MOE_ROUTE = 2       /* w4_moe_route (M = T tokens, N = E experts; K = 1, group ignored) */
 } w4_op;
 
 /*
@@ -231,6 +232,84 @@ w4_status w4afp8_moe_grouped_gemm(const void* qx, const float* x_scale, const in
                                   int32_t w_scale_dtype, int32_t group, void* y,
                                   int64_t R, int64_t N, int64_t K,
                                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The routed MoE layer around w4afp8_moe_grouped_gemm. [FP8] (module
+ * docstring, W4AFP8Config.get_quant_method) gives int4 routed experts with
+ * fp8 per-token activations but prints no routing or activation formula; the
+ * plain top-k layer is taken:
+ *   route:    per token the k experts with the largest logits, equal logits
+ *             in ascending expert order; weight = softmax probability over
+ *             all E experts (fp32), or divided by the sum over the k chosen
+ *             when renormalize != 0;
+ *   rows:     the T*k pairs (token, choice) listed by expert, then token;
+ *   between:  act = bf16(silu(gate) * up) in fp32, gate = columns [0, I) of the
+ *             gate_up output, up = [I, 2I); act quantized per row to e4m3
+ *             exactly as w4_quant_act_per_token does;
+ *   combine:  out[t] = bf16(sum_j w[t, j] * y[row_of[t, j]]), fp32, j ascending.
+ * A layer is: w4_moe_route; w4afp8_moe_gemm_bf16in (gate_up, gathering the
+ * token rows); w4_moe_silu_mul_quant_fp8; w4afp8_moe_grouped_gemm (down);
+ * w4_moe_combine.
+ */
+
+/*
+ * w4_moe_route: logits [T, E], bf16 (logits_f32 == 0) or fp32 (logits_f32
+ * != 0); 1 <= E <= 1024, 1 <= top_k <= min(E, 64). Outputs, device buffers
+ * owned by the caller:
+ *   topk_ids      int32 [T, top_k]  chosen experts, largest logit first
+ *   topk_weights  fp32  [T, top_k]  weights
+ *   offsets       int32 [E+1]       expert e owns rows [offsets[e], offsets[e+1])
+ *   row_token     int32 [T*top_k]   token of each row
+ *   row_of        int32 [T, top_k]  row of each (token, choice)
+ * workspace: at least w4_workspace_bytes(W4_OP_MOE_ROUTE, T, E, 1, 0) bytes,
+ * 4-byte aligned. NaN logits are outside the contract (they are taken as
+ * -inf). T == 0 launches nothing and returns W4_OK.
+ */
+w4_status w4_moe_route(const void* logits, int32_t logits_f32, int64_t T, int32_t E, int32_t top_k,
+                       int32_t renormalize, int32_t* topk_ids, float* topk_weights, int32_t* offsets,
+                       int32_t* row_token, int32_t* row_of, void* workspace, size_t workspace_bytes,
+                       void* stream);
+
+/*
+ * w4_moe_gather_quant_fp8: row r of q/scale is token row_token[r] of x
+ * [T, K] bf16 quantized per row to e4m3 (the codes and scale that
+ * w4_quant_act_per_token gives that row). q [R, K] (x and q 16-byte aligned),
+ * scale [R] fp32, K % 8 == 0. A row_token entry outside [0, T) gives a zero row
+ * with scale 1 and sets W4_ERR_SHAPE in the device status word
+ * (w4_device_status).
+ */
+w4_status w4_moe_gather_quant_fp8(const void* x, int64_t T, int64_t K, const int32_t* row_token, int64_t R,
+                                  void* q, float* scale, void* stream);
+
+/*
+ * w4afp8_moe_gemm_bf16in: w4_moe_gather_quant_fp8 fused into
+ * w4afp8_moe_grouped_gemm. The gathered rows are quantized straight into the
+ * GEMM's workspace (no fp8 copy in HBM); x_scale [R] receives the row scales.
+ * row_token may be NULL (then R must equal T and row r is token r). y equals
+ * w4afp8_moe_grouped_gemm applied to w4_moe_gather_quant_fp8(x) bit for bit.
+ * Other arguments and limits as w4afp8_moe_grouped_gemm.
+ */
+w4_status w4afp8_moe_gemm_bf16in(const void* x, int64_t T, const int32_t* row_token, const int32_t* expert_offsets,
+                                 int32_t E, const void* qweight, const void* w_scale, int32_t w_scale_dtype,
+                                 int32_t group, void* y, float* x_scale, int64_t R, int64_t N, int64_t K,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * w4_moe_silu_mul_quant_fp8: h [R, 2I] bf16 (the gate_up output) -> q [R, I]
+ * e4m3 codes and scale [R] fp32; act [R, I] bf16 receives the activations
+ * before quantization when not NULL. I % 8 == 0; h, q and act 16-byte aligned.
+ */
+w4_status w4_moe_silu_mul_quant_fp8(const void* h, int64_t R, int64_t I, void* q, float* scale, void* act,
+                                    void* stream);
+
+/*
+ * w4_moe_combine: y [R, H] bf16 (the down output, expert-sorted rows),
+ * topk_weights [T, top_k] fp32 and row_of [T, top_k] int32 from w4_moe_route;
+ * out [T, H] bf16. H % 8 == 0; y and out 16-byte aligned. A row_of entry
+ * outside [0, R) adds nothing and sets W4_ERR_SHAPE in the device status word.
+ */
+w4_status w4_moe_combine(const void* y, int64_t R, int64_t H, const float* topk_weights, const int32_t* row_of,
+                         int64_t T, int32_t top_k, void* out, void* stream);
 
 /*
  * Weight-side tools (load time, not on the per-token path).

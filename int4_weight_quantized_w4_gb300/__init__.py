@@ -19,16 +19,18 @@ __all__ = [
     "w4_quant_act_per_token", "w4a8_gemm", "w4a8_gemm_bf16in", "w4a8_gemm_noalloc", "w4a8_group_partials", "w4a16_gemm",
     "w4afp8_moe_grouped_gemm", "w4_quantize_groupwise", "w4_repack_s4_to_uint4b8",
     "w4_embedding_gather", "w4_lm_head_gemv",
+    "w4_moe_route", "w4_moe_gather_quant_fp8", "w4afp8_moe_gemm_bf16in", "w4_moe_silu_mul_quant_fp8",
+    "w4_moe_combine",
     "w4_device_status", "w4_selftest_bounded_wait",
     "W4_OK", "W4_ERR_NULL", "W4_ERR_ALIGN", "W4_ERR_GROUP", "W4_ERR_DTYPE",
     "W4_ERR_UNSUPPORTED", "W4_ERR_SHAPE", "W4_ERR_CUDA", "W4_ERR_TIMEOUT", "W4_ERR_WORKSPACE",
-    "W4_OP_W4A8", "W4_OP_W4AFP8_MOE", "w4_workspace_bytes", "EXPORTED_SYMBOLS",
+    "W4_OP_W4A8", "W4_OP_W4AFP8_MOE", "W4_OP_MOE_ROUTE", "w4_workspace_bytes", "EXPORTED_SYMBOLS",
 ]
 
 (W4_OK, W4_ERR_NULL, W4_ERR_ALIGN, W4_ERR_GROUP, W4_ERR_DTYPE, W4_ERR_UNSUPPORTED,
  W4_ERR_SHAPE, W4_ERR_CUDA, W4_ERR_TIMEOUT, W4_ERR_WORKSPACE) = range(10)
 W4_BF16, W4_FP16, W4_INT8, W4_FP8_E4M3 = range(4)
-W4_OP_W4A8, W4_OP_W4AFP8_MOE = range(2)
+W4_OP_W4A8, W4_OP_W4AFP8_MOE, W4_OP_MOE_ROUTE = range(3)
 
 _DIR = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_DIR, "libw4.so")
@@ -48,6 +50,12 @@ _SIGNATURES = {
     "w4_repack_s4_to_uint4b8": (_I32, [_P, _P, _I64, _P]),
     "w4_embedding_gather": (_I32, [_P, _I64, _P, _P, _P, _I64, _I64, _I32, _P, _P]),
     "w4_lm_head_gemv": (_I32, [_P, _I64, _P, _P, _P, _I64, _I64, _I32, _P, _P]),
+    "w4_moe_route": (_I32, [_P, _I32, _I64, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "w4_moe_gather_quant_fp8": (_I32, [_P, _I64, _I64, _P, _I64, _P, _P, _P]),
+    "w4afp8_moe_gemm_bf16in": (_I32, [_P, _I64, _P, _P, _I32, _P, _P, _I32, _I32, _P, _P, _I64, _I64, _I64, _P, _SZ,
+                                      _P]),
+    "w4_moe_silu_mul_quant_fp8": (_I32, [_P, _I64, _I64, _P, _P, _P, _P]),
+    "w4_moe_combine": (_I32, [_P, _I64, _I64, _P, _P, _I64, _I32, _P, _P]),
     "w4_last_error": (ctypes.c_char_p, []),
     "w4_status_string": (ctypes.c_char_p, [_I32]),
     "w4_device_status": (_I32, [_P]),
@@ -241,6 +249,90 @@ def w4afp8_moe_grouped_gemm(qx, x_scale, expert_offsets, qweight, w_scale, group
                                           _ptr(w_scale), _scale_dtype(w_scale), group, _ptr(y), R, N, K,
                                           _ptr(ws), wsb, _stream(stream, qx.device)), "w4afp8_moe_grouped_gemm")
     return y
+
+
+def w4_moe_route(logits, top_k: int, renormalize: bool = False, out=None, workspace=None, stream=None):
+    """Top-k routing of router ``logits [T, E]`` (bf16 or fp32). Returns
+    ``(topk_ids int32 [T,k], topk_weights fp32 [T,k], offsets int32 [E+1],
+    row_token int32 [T*k], row_of int32 [T,k])``; ``out`` may pass that tuple
+    preallocated."""
+    _cuda2d(logits, "logits", (torch.bfloat16, torch.float32))
+    T, E = logits.shape
+    dev = logits.device
+    if out is None:
+        out = (torch.empty((T, top_k), dtype=torch.int32, device=dev),
+               torch.empty((T, top_k), dtype=torch.float32, device=dev),
+               torch.zeros((E + 1,), dtype=torch.int32, device=dev),
+               torch.empty((T * top_k,), dtype=torch.int32, device=dev),
+               torch.empty((T, top_k), dtype=torch.int32, device=dev))
+    ids, wts, off, rt, ro = out
+    ws, wsb = _workspace(workspace, W4_OP_MOE_ROUTE, T, E, 1, 0, dev)
+    _check(load().w4_moe_route(_ptr(logits), int(logits.dtype == torch.float32), T, E, top_k, int(bool(renormalize)),
+                               _ptr(ids), _ptr(wts), _ptr(off), _ptr(rt), _ptr(ro), _ptr(ws), wsb,
+                               _stream(stream, dev)), "w4_moe_route")
+    return out
+
+
+def w4_moe_gather_quant_fp8(x, row_token, q=None, scale=None, stream=None):
+    """Rows ``x[row_token[r]]`` of bf16 ``x [T, K]`` quantized per row to e4m3;
+    returns ``(q float8_e4m3fn [R, K], scale fp32 [R])``."""
+    _cuda2d(x, "x", (torch.bfloat16,))
+    T, K = x.shape
+    R = row_token.numel()
+    q = torch.empty((R, K), dtype=torch.float8_e4m3fn, device=x.device) if q is None else q
+    scale = torch.empty((R,), dtype=torch.float32, device=x.device) if scale is None else scale
+    _check(load().w4_moe_gather_quant_fp8(_ptr(x), T, K, _ptr(row_token), R, _ptr(q), _ptr(scale),
+                                          _stream(stream, x.device)), "w4_moe_gather_quant_fp8")
+    return q, scale
+
+
+def w4afp8_moe_gemm_bf16in(x, row_token, expert_offsets, qweight, w_scale, group: int, y=None, x_scale=None,
+                           workspace=None, stream=None):
+    """Grouped expert linear from bf16 token rows: row r is ``x[row_token[r]]``
+    (``row_token`` None: row r is token r), quantized per row to e4m3 inside
+    the call. Returns ``(y bf16 [R, N], x_scale fp32 [R])``."""
+    _cuda2d(x, "x", (torch.bfloat16,))
+    T, K = x.shape
+    R = T if row_token is None else row_token.numel()
+    if qweight.dim() != 3 or not qweight.is_contiguous() or qweight.dtype != torch.int32:
+        raise ValueError("qweight must be a contiguous int32 [E, N, K/8] tensor")
+    E, N = qweight.shape[0], qweight.shape[1]
+    if qweight.shape[2] * 8 != K or expert_offsets.shape != (E + 1,) or w_scale.dim() != 3 \
+            or w_scale.shape[:2] != (E, N):
+        raise ValueError("inconsistent shapes for w4afp8_moe_gemm_bf16in")
+    y = torch.empty((R, N), dtype=torch.bfloat16, device=x.device) if y is None else y
+    x_scale = torch.empty((R,), dtype=torch.float32, device=x.device) if x_scale is None else x_scale
+    ws, wsb = _workspace(workspace, W4_OP_W4AFP8_MOE, R, N, K, group, x.device)
+    _check(load().w4afp8_moe_gemm_bf16in(_ptr(x), T, _ptr(row_token), _ptr(expert_offsets), E, _ptr(qweight),
+                                         _ptr(w_scale), _scale_dtype(w_scale), group, _ptr(y), _ptr(x_scale), R, N,
+                                         K, _ptr(ws), wsb, _stream(stream, x.device)), "w4afp8_moe_gemm_bf16in")
+    return y, x_scale
+
+
+def w4_moe_silu_mul_quant_fp8(h, q=None, scale=None, act=None, stream=None):
+    """``silu(gate) * up`` of the bf16 gate_up output ``h [R, 2I]``, quantized per
+    row to e4m3; returns ``(q [R, I], scale [R])``, and writes the bf16
+    activations to ``act`` when given."""
+    _cuda2d(h, "h", (torch.bfloat16,))
+    R, I2 = h.shape
+    I = I2 // 2
+    q = torch.empty((R, I), dtype=torch.float8_e4m3fn, device=h.device) if q is None else q
+    scale = torch.empty((R,), dtype=torch.float32, device=h.device) if scale is None else scale
+    _check(load().w4_moe_silu_mul_quant_fp8(_ptr(h), R, I, _ptr(q), _ptr(scale), _ptr(act),
+                                            _stream(stream, h.device)), "w4_moe_silu_mul_quant_fp8")
+    return q, scale
+
+
+def w4_moe_combine(y, topk_weights, row_of, out=None, stream=None):
+    """``out[t] = sum_j topk_weights[t, j] * y[row_of[t, j]]`` for bf16 ``y [R, H]``;
+    returns bf16 ``[T, H]``."""
+    _cuda2d(y, "y", (torch.bfloat16,))
+    R, H = y.shape
+    T, k = row_of.shape
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=y.device) if out is None else out
+    _check(load().w4_moe_combine(_ptr(y), R, H, _ptr(topk_weights), _ptr(row_of), T, k, _ptr(out),
+                                 _stream(stream, y.device)), "w4_moe_combine")
+    return out
 
 
 def w4_quantize_groupwise(w, group: int, packed=None, scale=None, zero=None, stream=None):

@@ -122,6 +122,7 @@ size_t w4_workspace_bytes(int32_t op, int64_t M, int64_t N, int64_t K, int32_t g
   (void)group;
   if (M <= 0 || K <= 0) return 0;
   if (op == W4_OP_W4A8 || op == W4_OP_W4AFP8_MOE) return w4::w4a8_workspace_bytes(M, K);
+  if (op == W4_OP_MOE_ROUTE) return (N > 0 && N <= 1024) ? w4::moe_route_workspace_bytes(M, static_cast<int32_t>(N)) : 0;
   return 0;
 }
 
@@ -231,19 +232,26 @@ w4_status w4a16_gemm(const void* x, const void* qweight, const void* w_scale, in
   return from_cuda(w4::launch_w4a16(a, static_cast<cudaStream_t>(stream)), "w4a16 launch");
 }
 
+static w4_status check_experts(int64_t R, int64_t N, int64_t K, int32_t group, int32_t E, int32_t w_scale_dtype,
+                               int32_t* g) {
+  w4_status st = check_dims_group(R, N, K, group, g);
+  if (st != W4_OK) return st;
+  if (E <= 0) return fail(W4_ERR_SHAPE, "E must be positive, got %d", E);
+  if (w_scale_dtype != W4_FP16) return fail(W4_ERR_DTYPE, "expert weight scales must be fp16 (W4_FP16)");
+  if (K % 32 != 0 || *g % 16 != 0)
+    return fail(W4_ERR_UNSUPPORTED, "expert tiles need K % 32 == 0 and the group a multiple of 16 (K=%lld group=%d)",
+                (long long)K, *g);
+  if ((R + 127) / 128 + E > 65535) return fail(W4_ERR_UNSUPPORTED, "too many row tiles plus experts");
+  return W4_OK;
+}
+
 w4_status w4afp8_moe_grouped_gemm(const void* qx, const float* x_scale, const int32_t* expert_offsets, int32_t E,
                                   const void* qweight, const void* w_scale, int32_t w_scale_dtype, int32_t group,
                                   void* y, int64_t R, int64_t N, int64_t K, void* workspace,
                                   size_t workspace_bytes, void* stream) {
   int32_t g = 0;
-  w4_status st = check_dims_group(R, N, K, group, &g);
+  w4_status st = check_experts(R, N, K, group, E, w_scale_dtype, &g);
   if (st != W4_OK) return st;
-  if (E <= 0) return fail(W4_ERR_SHAPE, "E must be positive, got %d", E);
-  if (w_scale_dtype != W4_FP16) return fail(W4_ERR_DTYPE, "expert weight scales must be fp16 (W4_FP16)");
-  if (K % 32 != 0 || g % 16 != 0)
-    return fail(W4_ERR_UNSUPPORTED, "expert tiles need K % 32 == 0 and the group a multiple of 16 (K=%lld group=%d)",
-                (long long)K, g);
-  if ((R + 127) / 128 + E > 65535) return fail(W4_ERR_UNSUPPORTED, "too many row tiles plus experts");
   if (R == 0) return ok();
   if (!qx || !x_scale || !expert_offsets || !qweight || !w_scale || !y)
     return fail(W4_ERR_NULL, "required pointer is NULL");
@@ -287,6 +295,106 @@ w4_status w4_repack_s4_to_uint4b8(const void* src, void* dst, int64_t n_bytes, v
   if (!src || !dst) return fail(W4_ERR_NULL, "src and dst must be non-NULL");
   if (!aligned(src, 16) || !aligned(dst, 16)) return fail(W4_ERR_ALIGN, "src and dst must be 16-byte aligned");
   return from_cuda(w4::launch_xor88(src, dst, n_bytes, static_cast<cudaStream_t>(stream)), "repack launch");
+}
+
+w4_status w4_moe_route(const void* logits, int32_t logits_f32, int64_t T, int32_t E, int32_t top_k,
+                       int32_t renormalize, int32_t* topk_ids, float* topk_weights, int32_t* offsets,
+                       int32_t* row_token, int32_t* row_of, void* workspace, size_t workspace_bytes, void* stream) {
+  if (T < 0) return fail(W4_ERR_SHAPE, "T must be >= 0");
+  if (E < 1 || E > 1024) return fail(W4_ERR_UNSUPPORTED, "E must be in [1, 1024], got %d", E);
+  if (top_k < 1 || top_k > E || top_k > 64)
+    return fail(W4_ERR_SHAPE, "top_k must be in [1, min(E, 64)], got %d (E=%d)", top_k, E);
+  if (T * top_k > INT32_MAX) return fail(W4_ERR_UNSUPPORTED, "T * top_k rows must fit in int32");
+  if (T == 0) return ok();
+  if (!logits || !topk_ids || !topk_weights || !offsets || !row_token || !row_of)
+    return fail(W4_ERR_NULL, "logits and every output must be non-NULL");
+  if (!aligned(logits, logits_f32 ? 4 : 2) || !aligned(topk_ids, 4) || !aligned(topk_weights, 4) ||
+      !aligned(offsets, 4) || !aligned(row_token, 4) || !aligned(row_of, 4))
+    return fail(W4_ERR_ALIGN, "route buffers must be aligned to their element size");
+  const size_t need = w4::moe_route_workspace_bytes(T, E);
+  if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 4))
+    return fail(W4_ERR_WORKSPACE, "route workspace must be 4-byte aligned and at least %zu bytes (got %zu)", need,
+                workspace_bytes);
+  return from_cuda(w4::launch_moe_route(logits, logits_f32 == 0, T, E, top_k, renormalize != 0, topk_ids,
+                                        topk_weights, offsets, row_token, row_of, workspace,
+                                        static_cast<cudaStream_t>(stream)),
+                   "moe route launch");
+}
+
+w4_status w4_moe_gather_quant_fp8(const void* x, int64_t T, int64_t K, const int32_t* row_token, int64_t R,
+                                  void* q, float* scale, void* stream) {
+  if (T < 0 || R < 0 || K <= 0) return fail(W4_ERR_SHAPE, "sizes must be T >= 0, R >= 0, K > 0");
+  if (K % 8 != 0) return fail(W4_ERR_ALIGN, "K must be a multiple of 8, got %lld", (long long)K);
+  if (R == 0) return ok();
+  if (!x || !row_token || !q || !scale) return fail(W4_ERR_NULL, "x, row_token, q and scale must be non-NULL");
+  if (!aligned(x, 16) || !aligned(q, 16) || !aligned(scale, 4) || !aligned(row_token, 4))
+    return fail(W4_ERR_ALIGN, "x and q must be 16-byte aligned; scale and row_token 4-byte aligned");
+  if (R > INT32_MAX) return fail(W4_ERR_UNSUPPORTED, "R too large");
+  unsigned int* status = nullptr;
+  cudaError_t e = status_ptr(&status);
+  if (e != cudaSuccess) return from_cuda(e, "device status word");
+  return from_cuda(w4::launch_quant_gather(x, T, K, row_token, R, true, false, q, scale, status,
+                                           static_cast<cudaStream_t>(stream)),
+                   "gather-quant launch");
+}
+
+w4_status w4afp8_moe_gemm_bf16in(const void* x, int64_t T, const int32_t* row_token, const int32_t* expert_offsets,
+                                 int32_t E, const void* qweight, const void* w_scale, int32_t w_scale_dtype,
+                                 int32_t group, void* y, float* x_scale, int64_t R, int64_t N, int64_t K,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+  int32_t g = 0;
+  w4_status st = check_experts(R, N, K, group, E, w_scale_dtype, &g);
+  if (st != W4_OK) return st;
+  if (T < 0) return fail(W4_ERR_SHAPE, "T must be >= 0");
+  if (row_token == nullptr && R != T) return fail(W4_ERR_SHAPE, "without row_token R must equal T");
+  if (R == 0) return ok();
+  if (!x || !x_scale || !expert_offsets || !qweight || !w_scale || !y)
+    return fail(W4_ERR_NULL, "required pointer is NULL");
+  if (!aligned(x, 16) || !aligned(qweight, 16) || !aligned(y, 16) || !aligned(w_scale, 8) ||
+      !aligned(x_scale, 4) || !aligned(expert_offsets, 4) || (row_token && !aligned(row_token, 4)))
+    return fail(W4_ERR_ALIGN, "matrices must be 16-byte aligned, vectors aligned to their element size");
+  if (R > INT32_MAX || N > INT32_MAX) return fail(W4_ERR_UNSUPPORTED, "R or N too large");
+  st = check_workspace(workspace, workspace_bytes, R, K);
+  if (st != W4_OK) return st;
+  unsigned int* status = nullptr;
+  cudaError_t e = status_ptr(&status);
+  if (e != cudaSuccess) return from_cuda(e, "device status word");
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  e = w4::launch_quant_gather(x, T, K, row_token, R, true, true, workspace, x_scale, status, s);
+  if (e != cudaSuccess) return from_cuda(e, "gather-quant-widen launch");
+  w4::W4A8Args a{nullptr, x_scale, qweight, w_scale, nullptr, y, expert_offsets, E, R, N, K, g, false, status,
+                 workspace, true};
+  return from_cuda(w4::launch_w4afp8_experts(a, s), "w4afp8 experts launch");
+}
+
+w4_status w4_moe_silu_mul_quant_fp8(const void* h, int64_t R, int64_t I, void* q, float* scale, void* act,
+                                    void* stream) {
+  if (R < 0 || I <= 0) return fail(W4_ERR_SHAPE, "sizes must be R >= 0, I > 0");
+  if (I % 8 != 0) return fail(W4_ERR_ALIGN, "I must be a multiple of 8, got %lld", (long long)I);
+  if (R == 0) return ok();
+  if (!h || !q || !scale) return fail(W4_ERR_NULL, "h, q and scale must be non-NULL");
+  if (!aligned(h, 16) || !aligned(q, 16) || !aligned(scale, 4) || (act && !aligned(act, 16)))
+    return fail(W4_ERR_ALIGN, "h, q and act must be 16-byte aligned, scale 4-byte aligned");
+  if (R > INT32_MAX || I / 8 > INT32_MAX) return fail(W4_ERR_UNSUPPORTED, "R or I too large");
+  return from_cuda(w4::launch_silu_mul_quant(h, R, I, q, scale, act, static_cast<cudaStream_t>(stream)),
+                   "silu-mul-quant launch");
+}
+
+w4_status w4_moe_combine(const void* y, int64_t R, int64_t H, const float* topk_weights, const int32_t* row_of,
+                         int64_t T, int32_t top_k, void* out, void* stream) {
+  if (R < 0 || T < 0 || H <= 0 || top_k < 1) return fail(W4_ERR_SHAPE, "sizes must be R, T >= 0, H > 0, top_k >= 1");
+  if (H % 8 != 0) return fail(W4_ERR_ALIGN, "H must be a multiple of 8, got %lld", (long long)H);
+  if (T == 0) return ok();
+  if (!y || !topk_weights || !row_of || !out) return fail(W4_ERR_NULL, "y, topk_weights, row_of, out must be non-NULL");
+  if (!aligned(y, 16) || !aligned(out, 16) || !aligned(topk_weights, 4) || !aligned(row_of, 4))
+    return fail(W4_ERR_ALIGN, "y and out must be 16-byte aligned; weights and row_of 4-byte aligned");
+  if (H / 8 > INT32_MAX || T * (H / 8) > (int64_t(1) << 40)) return fail(W4_ERR_UNSUPPORTED, "T or H too large");
+  unsigned int* status = nullptr;
+  cudaError_t e = status_ptr(&status);
+  if (e != cudaSuccess) return from_cuda(e, "device status word");
+  return from_cuda(w4::launch_moe_combine(y, R, H, topk_weights, row_of, T, top_k, out, status,
+                                          static_cast<cudaStream_t>(stream)),
+                   "combine launch");
 }
 
 static w4_status check_table(int64_t V, int64_t D, int32_t group, int32_t* geff) {

@@ -66,6 +66,16 @@ cudaError_t launch_embedding_gather(const int32_t* ids, int64_t T, const void* t
                                     unsigned int* status, cudaStream_t s);
 cudaError_t launch_lm_head(const void* h, int64_t M, const void* table, const float* scale, const float* zero,
                            int64_t V, int64_t D, int32_t group, void* y, cudaStream_t s);
+cudaError_t launch_quant_gather(const void* x, int64_t T, int64_t K, const int32_t* rows, int64_t R, bool fp8,
+                                bool widen, void* q, float* scale, unsigned int* status, cudaStream_t s);
+size_t moe_route_workspace_bytes(int64_t T, int32_t E);
+cudaError_t launch_moe_route(const void* logits, bool bf16, int64_t T, int32_t E, int32_t k, bool renorm,
+                             int32_t* ids, float* wts, int32_t* offsets, int32_t* row_token, int32_t* row_of,
+                             void* workspace, cudaStream_t s);
+cudaError_t launch_silu_mul_quant(const void* h, int64_t R, int64_t I, void* q, float* scale, void* act,
+                                  cudaStream_t s);
+cudaError_t launch_moe_combine(const void* y, int64_t R, int64_t H, const float* w, const int32_t* row_of, int64_t T,
+                               int32_t k, void* out, unsigned int* status, cudaStream_t s);
 cudaError_t launch_bounded_wait_selftest(long long limit, unsigned int* status, cudaStream_t s);
 
 }  // namespace w4

@@ -14,7 +14,9 @@
 // HBM sees the row read once and the codes written once (3 bytes per element).
 // The fused form for the W4A8 GEMM stores each chunk's codes instead as their
 // exact fp16 values in the GEMM's operand order (4 bytes per element, no int8
-// round trip).
+// round trip). The gathered form quantizes row gather[r] of x into row r (the
+// expert-sorted rows of a routed MoE layer): the codes are those of
+// quantizing x and then gathering, without the intermediate copy.
 #include "common.cuh"
 #include "launch.h"
 
@@ -88,13 +90,35 @@ W4_DEV void store_chunk(void* q, size_t i, const uint4& v, float s) {
 
 // NCH > 0: the row fits in registers, NCH chunks per thread.
 // NCH == 0: long rows, read twice (the second read mostly hits L2).
+// gather (may be null): source row of each output row, checked against T; an
+// id outside [0, T) gives a zero row with scale 1 and W4_ERR_SHAPE in status.
 template <int NCH, bool FP8, bool kWiden>
 __global__ void __launch_bounds__(kMaxThreads) quant_rows(const uint4* __restrict__ x, int K8,
-                                                          void* __restrict__ q, float* __restrict__ scale) {
+                                                          void* __restrict__ q, float* __restrict__ scale,
+                                                          const int32_t* __restrict__ gather, int64_t T,
+                                                          unsigned int* status) {
   __shared__ float red[kMaxThreads / 32];
   const size_t row = blockIdx.x;
-  const uint4* xr = x + row * static_cast<size_t>(K8);
   const size_t q0 = row * static_cast<size_t>(K8);
+  size_t src = row;
+  if (gather != nullptr) {
+    const int64_t g = gather[row];
+    if (g < 0 || g >= T) {     // the same for the whole block: no barrier is skipped by part of it
+      for (int i = threadIdx.x; i < K8; i += blockDim.x) {
+        if (kWiden)
+          static_cast<uint4*>(q)[q0 + i] = make_uint4(0, 0, 0, 0);
+        else
+          static_cast<uint2*>(q)[q0 + i] = make_uint2(0, 0);
+      }
+      if (threadIdx.x == 0) {
+        scale[row] = 1.f;
+        report(status, W4_ERR_SHAPE);
+      }
+      return;
+    }
+    src = static_cast<size_t>(g);
+  }
+  const uint4* xr = x + src * static_cast<size_t>(K8);
   constexpr float kQ = FP8 ? 448.f : 127.f;
   if constexpr (NCH > 0) {
     uint4 v[NCH];
@@ -124,7 +148,8 @@ __global__ void __launch_bounds__(kMaxThreads) quant_rows(const uint4* __restric
 }
 
 template <bool FP8, bool kWiden>
-cudaError_t launch(const void* x, int64_t M, int64_t K, void* q, float* scale, cudaStream_t s) {
+cudaError_t launch(const void* x, int64_t M, int64_t K, void* q, float* scale, cudaStream_t s,
+                   const int32_t* gather = nullptr, int64_t T = 0, unsigned int* status = nullptr) {
   const int K8 = static_cast<int>(K / 8);
   int threads = ((K8 + 31) / 32) * 32;
   if (threads > kMaxThreads) threads = kMaxThreads;
@@ -132,11 +157,11 @@ cudaError_t launch(const void* x, int64_t M, int64_t K, void* q, float* scale, c
   const dim3 grid(static_cast<unsigned>(M));
   auto xp = static_cast<const uint4*>(x);
   switch (nch) {
-    case 1: quant_rows<1, FP8, kWiden><<<grid, threads, 0, s>>>(xp, K8, q, scale); break;
-    case 2: quant_rows<2, FP8, kWiden><<<grid, threads, 0, s>>>(xp, K8, q, scale); break;
-    case 3: quant_rows<3, FP8, kWiden><<<grid, threads, 0, s>>>(xp, K8, q, scale); break;
-    case 4: quant_rows<4, FP8, kWiden><<<grid, threads, 0, s>>>(xp, K8, q, scale); break;
-    default: quant_rows<0, FP8, kWiden><<<grid, threads, 0, s>>>(xp, K8, q, scale); break;
+    case 1: quant_rows<1, FP8, kWiden><<<grid, threads, 0, s>>>(xp, K8, q, scale, gather, T, status); break;
+    case 2: quant_rows<2, FP8, kWiden><<<grid, threads, 0, s>>>(xp, K8, q, scale, gather, T, status); break;
+    case 3: quant_rows<3, FP8, kWiden><<<grid, threads, 0, s>>>(xp, K8, q, scale, gather, T, status); break;
+    case 4: quant_rows<4, FP8, kWiden><<<grid, threads, 0, s>>>(xp, K8, q, scale, gather, T, status); break;
+    default: quant_rows<0, FP8, kWiden><<<grid, threads, 0, s>>>(xp, K8, q, scale, gather, T, status); break;
   }
   return cudaGetLastError();
 }
@@ -153,6 +178,16 @@ cudaError_t launch_quant_widen(const void* x, int64_t M, int64_t K, bool fp8, vo
                                cudaStream_t s) {
   if (K / 8 > INT32_MAX) return cudaErrorInvalidValue;
   return fp8 ? launch<true, true>(x, M, K, wide, scale, s) : launch<false, true>(x, M, K, wide, scale, s);
+}
+
+cudaError_t launch_quant_gather(const void* x, int64_t T, int64_t K, const int32_t* rows, int64_t R, bool fp8,
+                                bool widen, void* q, float* scale, unsigned int* status, cudaStream_t s) {
+  if (K / 8 > INT32_MAX) return cudaErrorInvalidValue;
+  if (fp8)
+    return widen ? launch<true, true>(x, R, K, q, scale, s, rows, T, status)
+                 : launch<true, false>(x, R, K, q, scale, s, rows, T, status);
+  return widen ? launch<false, true>(x, R, K, q, scale, s, rows, T, status)
+               : launch<false, false>(x, R, K, q, scale, s, rows, T, status);
 }
 
 }  // namespace w4

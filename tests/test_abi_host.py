@@ -201,3 +201,47 @@ def test_embedding_validation(lib):
     assert head(D=5824, group=32, M=0) == w4.W4_ERR_UNSUPPORTED
     assert head(table=ODD) == w4.W4_ERR_ALIGN
     assert head(M=0) == w4.W4_OK
+
+
+def test_moe_glue_validation(lib):
+    def route(**kw):
+        a = dict(lg=FAKE, f32=1, T=100, E=64, k=8, ren=0, ids=FAKE, w=FAKE, off=FAKE, rt=FAKE, ro=FAKE, ws=FAKE,
+                 wsb=1 << 20)
+        a.update(kw)
+        return lib.w4_moe_route(a["lg"], a["f32"], a["T"], a["E"], a["k"], a["ren"], a["ids"], a["w"], a["off"],
+                                a["rt"], a["ro"], a["ws"], a["wsb"], None)
+    assert route(E=1025) == w4.W4_ERR_UNSUPPORTED
+    assert route(k=65, E=128) == w4.W4_ERR_SHAPE
+    assert route(k=9, E=8) == w4.W4_ERR_SHAPE
+    assert route(ids=None) == w4.W4_ERR_NULL
+    assert route(ws=None) == w4.W4_ERR_WORKSPACE
+    need = lib.w4_workspace_bytes(w4.W4_OP_MOE_ROUTE, 100, 64, 1, 0)
+    assert need == 64 * 4                                   # one 256-token tile x 64 experts
+    assert route(wsb=need - 1) == w4.W4_ERR_WORKSPACE
+    assert route(T=0) == w4.W4_OK
+
+    assert lib.w4_moe_gather_quant_fp8(FAKE, 10, 260, FAKE, 5, FAKE, FAKE, None) == w4.W4_ERR_ALIGN
+    assert lib.w4_moe_gather_quant_fp8(FAKE, 10, 256, None, 5, FAKE, FAKE, None) == w4.W4_ERR_NULL
+    assert lib.w4_moe_gather_quant_fp8(FAKE, 10, 256, FAKE, 0, FAKE, FAKE, None) == w4.W4_OK
+
+    def moe_in(**kw):
+        a = dict(x=FAKE, T=64, rt=FAKE, off=FAKE, E=8, qw=FAKE, sw=FAKE, sdt=w4.W4_FP16, group=128, y=FAKE, sx=FAKE,
+                 R=128, N=256, K=256, ws=FAKE, wsb=1 << 30)
+        a.update(kw)
+        return lib.w4afp8_moe_gemm_bf16in(a["x"], a["T"], a["rt"], a["off"], a["E"], a["qw"], a["sw"], a["sdt"],
+                                          a["group"], a["y"], a["sx"], a["R"], a["N"], a["K"], a["ws"], a["wsb"], None)
+    assert moe_in(rt=None) == w4.W4_ERR_SHAPE               # without row_token R must equal T
+    assert moe_in(sdt=w4.W4_BF16) == w4.W4_ERR_DTYPE
+    assert moe_in(K=240, group=-1) == w4.W4_ERR_UNSUPPORTED
+    assert moe_in(wsb=16) == w4.W4_ERR_WORKSPACE
+    assert moe_in(x=ODD) == w4.W4_ERR_ALIGN
+    assert moe_in(R=0, T=0, rt=None) == w4.W4_OK
+
+    assert lib.w4_moe_silu_mul_quant_fp8(FAKE, 4, 12, FAKE, FAKE, None, None) == w4.W4_ERR_ALIGN
+    assert lib.w4_moe_silu_mul_quant_fp8(FAKE, 4, 16, FAKE, FAKE, ODD, None) == w4.W4_ERR_ALIGN
+    assert lib.w4_moe_silu_mul_quant_fp8(FAKE, 0, 16, FAKE, FAKE, None, None) == w4.W4_OK
+
+    assert lib.w4_moe_combine(FAKE, 16, 12, FAKE, FAKE, 2, 8, FAKE, None) == w4.W4_ERR_ALIGN
+    assert lib.w4_moe_combine(FAKE, 16, 16, FAKE, None, 2, 8, FAKE, None) == w4.W4_ERR_NULL
+    assert lib.w4_moe_combine(FAKE, 16, 16, FAKE, FAKE, 2, 0, FAKE, None) == w4.W4_ERR_SHAPE
+    assert lib.w4_moe_combine(FAKE, 16, 16, FAKE, FAKE, 0, 8, FAKE, None) == w4.W4_OK

@@ -1,0 +1,206 @@
+"""The routed MoE layer around the grouped GEMM on the GPU against the oracle,
+through the C ABI: routing and the row order, the gathered fp8 input, the
+fused gather + GEMM, SiLU(gate)*up with fp8 requantization, the combine, and
+a whole layer end to end."""
+import numpy as np
+import pytest
+import torch
+
+import int4_weight_quantized_w4_gb300 as w4
+import oracle as O
+import synthetic as S
+from _compare import check_bf16_output
+from _gpu import bf16, bits, requires_cuda, to_dev
+
+pytestmark = [pytest.mark.gpu, requires_cuda]
+
+
+def _logits(T, E, seed, dtype):
+    lg = S.router_logits(T, E, seed=seed)
+    if dtype == "bf16":
+        b = S.to_bf16_bits(lg)
+        return bf16(b), S.bf16_bits_to_f32(b)
+    return to_dev(lg), lg
+
+
+def _route_check(T, E, k, renorm, dtype, seed, tie_rows=()):
+    lg_d, lg = _logits(T, E, seed, dtype)
+    for t in tie_rows:                         # fully tied tokens: lowest indices win
+        lg[t, :] = lg[t, 0]
+    if tie_rows:
+        lg_d = bf16(S.to_bf16_bits(lg)) if dtype == "bf16" else to_dev(lg)
+    ids, wts, off, rt, ro = w4.w4_moe_route(lg_d, k, renorm)
+    torch.cuda.synchronize()
+    r_ids, r_w, r_off, r_rt, r_ro = O.moe_route(lg, k, renorm)
+    np.testing.assert_array_equal(ids.cpu().numpy(), r_ids)
+    np.testing.assert_array_equal(off.cpu().numpy(), r_off)
+    np.testing.assert_array_equal(rt.cpu().numpy(), r_rt)
+    np.testing.assert_array_equal(ro.cpu().numpy(), r_ro)
+    np.testing.assert_allclose(wts.cpu().numpy(), r_w, rtol=2e-5, atol=1e-9)
+
+
+@pytest.mark.parametrize("T,E,k,renorm,dtype", [
+    (100, 64, 8, False, "f32"), (1000, 60, 6, True, "f32"), (37, 1, 1, False, "f32"), (300, 256, 8, True, "bf16"),
+    (513, 1024, 64, False, "f32"), (257, 33, 33, True, "bf16"), (1, 8, 2, True, "f32")])
+def test_route_matches_oracle(T, E, k, renorm, dtype):
+    """ids, offsets, row order and its inverse bit-exact; weights to fp32
+    rounding. bf16 logits tie often, so the lower-index rule is exercised."""
+    _route_check(T, E, k, renorm, dtype, seed=T + E, tie_rows=(0,) if T > 1 else ())
+
+
+def test_route_full_size():
+    """4096 tokens, 64 experts, top-8: the MoE workload's routing."""
+    _route_check(4096, 64, 8, False, "f32", seed=5)
+
+
+def test_gather_quant_bit_exact_and_bad_row():
+    T, K = 50, 264
+    x = S.activations_bf16(T, K, seed=21)
+    x[7] = 0                                   # a zero row: scale 1, all codes 0
+    rows = np.array([3, 3, 49, 0, 7, 12, 12, 12], np.int32)
+    q, s = w4.w4_moe_gather_quant_fp8(bf16(x), to_dev(rows))
+    torch.cuda.synchronize()
+    rq, rs = O.moe_gather_quant_fp8(x, rows)
+    np.testing.assert_array_equal(q.view(torch.uint8).cpu().numpy(), rq)
+    np.testing.assert_array_equal(s.cpu().numpy(), rs)
+    assert w4.w4_device_status() == w4.W4_OK
+    q, s = w4.w4_moe_gather_quant_fp8(bf16(x), to_dev(np.array([1, T, -2], np.int32)))
+    assert w4.w4_device_status() == w4.W4_ERR_SHAPE
+    qb = q.view(torch.uint8).cpu().numpy()
+    np.testing.assert_array_equal(qb[0], O.moe_gather_quant_fp8(x, [1])[0][0])
+    assert not qb[1:].any() and np.all(s.cpu().numpy()[1:] == 1.0)
+
+
+@pytest.mark.parametrize("T,E,k,N,K,g", [(64, 8, 2, 256, 256, 128), (200, 16, 4, 384, 512, -1)])
+def test_moe_gemm_bf16in_equals_gather_then_gemm(T, E, k, N, K, g):
+    """The fused gather + quant + GEMM is bit-identical to the two-step path,
+    and matches the oracle."""
+    x = S.activations_bf16(T, K, seed=T)
+    _, _, off, rt, _ = w4.w4_moe_route(to_dev(S.router_logits(T, E, seed=E)), k)
+    qw = S.random_words((E, N, K // 8), seed=1)
+    sw = S.scales_f16((E, N, K // (K if g == -1 else g)), seed=2)
+    y, sx = w4.w4afp8_moe_gemm_bf16in(bf16(x), rt, off, to_dev(qw), to_dev(sw), g)
+    q2, s2 = w4.w4_moe_gather_quant_fp8(bf16(x), rt)
+    y2 = w4.w4afp8_moe_grouped_gemm(q2, s2, off, to_dev(qw), to_dev(sw), g)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(bits(y), bits(y2))
+    np.testing.assert_array_equal(sx.cpu().numpy(), s2.cpu().numpy())
+    _, _, r_off, r_rt, _ = O.moe_route(S.router_logits(T, E, seed=E), k, False)
+    rq, rs = O.moe_gather_quant_fp8(x, r_rt)
+    r = O.moe_grouped_linear(rq, rs, r_off, qw, sw, g)
+    check_bf16_output(bits(y), r, "moe_gemm_bf16in")
+
+
+def test_moe_gemm_bf16in_without_gather():
+    T, E, N, K, g = 96, 3, 128, 256, 128
+    x = S.activations_bf16(T, K, seed=8)
+    off = S.offsets_from_counts([40, 0, 56])
+    qw = S.random_words((E, N, K // 8), seed=1)
+    sw = S.scales_f16((E, N, K // g), seed=2)
+    y, _ = w4.w4afp8_moe_gemm_bf16in(bf16(x), None, to_dev(off), to_dev(qw), to_dev(sw), g)
+    torch.cuda.synchronize()
+    rq, rs = O.quant_fp8_per_token(x)
+    check_bf16_output(bits(y), O.moe_grouped_linear(rq, rs, off, qw, sw, g), "moe_gemm_bf16in rows as tokens")
+
+
+def _act_check(h, what):
+    R, I2 = h.shape
+    I = I2 // 2
+    act = torch.empty((R, I), dtype=torch.bfloat16, device="cuda")
+    q, s = w4.w4_moe_silu_mul_quant_fp8(bf16(h), act=act)
+    torch.cuda.synchronize()
+    rq, rs, ract = O.silu_mul_quant_fp8(h)
+    a, ra = bits(act), ract
+    # activations: one fp32 exp apart at most, so equal or one bf16 step apart
+    av, rav = S.bf16_bits_to_f32(a).astype(np.float64), S.bf16_bits_to_f32(ra).astype(np.float64)
+    same = a == ra
+    assert same.mean() >= 0.999, f"{what}: only {same.mean():.5f} of activations bit-equal"
+    assert np.all(np.abs(av - rav) <= np.abs(rav) * 2.0 ** -7 + 1e-38), f"{what}: activation off by > 1 bf16 ulp"
+    # scales: bit-equal where the row's activation maximum is; codes: bit-equal
+    # wherever the activation and the row's scale are
+    sg, qg = s.cpu().numpy(), q.view(torch.uint8).cpu().numpy()
+    amax_same = np.abs(av).max(axis=1) == np.abs(rav).max(axis=1)
+    np.testing.assert_array_equal(sg[amax_same], rs[amax_same])
+    np.testing.assert_allclose(sg, rs, rtol=2.0 ** -7)
+    mask = same & (sg == rs)[:, None]
+    np.testing.assert_array_equal(qg[mask], rq[mask])
+    # every code is a faithful e4m3 quantization of the GPU's own activation
+    dq = O.e4m3_decode(qg) * sg[:, None].astype(np.float64)
+    assert np.all(np.abs(dq - av) <= np.abs(av) * 2.0 ** -4 + sg[:, None] * 2.0 ** -9 * 1.0001)
+
+
+@pytest.mark.parametrize("R,I", [(300, 1408), (5, 8), (17, 2056), (3, 8200)])
+def test_silu_mul_quant(R, I):
+    """Row lengths for one, two and several chunks per thread and for the
+    long-row path."""
+    h = S.activations_bf16(R, 2 * I, seed=R + I)
+    _act_check(h, f"silu R={R} I={I}")
+
+
+def test_silu_mul_quant_edge_values():
+    """Gates far below zero (silu -> -0), a zero row (scale 1, codes 0), large
+    gates (silu(g) = g)."""
+    R, I = 4, 64
+    h = S.activations_bf16(R, 2 * I, seed=3)
+    gf = S.bf16_bits_to_f32(h).copy()
+    gf[0, :I] = -200.0
+    gf[1, :] = 0.0
+    gf[2, :I] = 90.0
+    _act_check(S.to_bf16_bits(gf), "silu edges")
+
+
+@pytest.mark.parametrize("T,k,H", [(100, 8, 2048), (7, 1, 64), (33, 3, 136)])
+def test_combine(T, k, H):
+    R = T * k
+    y = S.activations_bf16(R, H, seed=T)
+    ro = np.argsort(S.raw_u64(T, 9, R), kind="stable").astype(np.int32).reshape(T, k)   # a seeded permutation
+    w = S.uniform(T, 3, T * k).reshape(T, k).astype(np.float32)
+    out = w4.w4_moe_combine(bf16(y), to_dev(w), to_dev(ro))
+    torch.cuda.synchronize()
+    check_bf16_output(bits(out), O.moe_combine(y, w, ro), f"combine T={T} k={k}")
+
+
+def test_combine_bad_row_sets_status():
+    y = S.activations_bf16(4, 16, seed=1)
+    ro = np.array([[0, 9], [3, 1]], np.int32)
+    w = np.array([[0.5, 0.5], [0.25, 0.75]], np.float32)
+    assert w4.w4_device_status() == w4.W4_OK
+    out = w4.w4_moe_combine(bf16(y), to_dev(w), to_dev(ro))
+    assert w4.w4_device_status() == w4.W4_ERR_SHAPE
+    r = O.moe_combine(y, np.array([[0.5, 0.0], [0.25, 0.75]], np.float32), np.array([[0, 0], [3, 1]], np.int32))
+    check_bf16_output(bits(out), r, "combine with a bad row")
+
+
+def test_moe_layer_end_to_end():
+    """route -> gather + gate_up GEMM -> SiLU*up + requant -> down GEMM ->
+    combine, on the GPU and in the oracle from the same inputs. The two sides
+    may requantize a rare activation one e4m3 step apart (the bf16 gate_up
+    outputs can differ in the last bit), so the layer output is held to 2% of
+    its rms for every element and to the parity bar for 99% of them."""
+    T, E, k, Hd, I, g = 128, 8, 2, 256, 128, 128
+    lg = S.router_logits(T, E, seed=31)
+    x = S.activations_bf16(T, Hd, seed=32)
+    w1 = S.random_words((E, 2 * I, Hd // 8), seed=1, tag=40)
+    s1 = S.scales_f16((E, 2 * I, Hd // g), seed=2, tag=41)
+    w2 = S.random_words((E, Hd, I // 8), seed=1, tag=42)
+    s2 = S.scales_f16((E, Hd, I // g), seed=2, tag=43)
+    ids, wts, off, rt, ro = w4.w4_moe_route(to_dev(lg), k, True)
+    h1, _ = w4.w4afp8_moe_gemm_bf16in(bf16(x), rt, off, to_dev(w1), to_dev(s1), g)
+    qa, sa = w4.w4_moe_silu_mul_quant_fp8(h1)
+    y2 = w4.w4afp8_moe_grouped_gemm(qa, sa, off, to_dev(w2), to_dev(s2), g)
+    out = w4.w4_moe_combine(y2, wts, ro)
+    torch.cuda.synchronize()
+
+    r_ids, r_w, r_off, r_rt, r_ro = O.moe_route(lg, k, True)
+    rq, rs = O.moe_gather_quant_fp8(x, r_rt)
+    rh1 = O.f32_to_bf16_bits(O.moe_grouped_linear(rq, rs, r_off, w1, s1, g))
+    check_bf16_output(bits(h1), O.moe_grouped_linear(rq, rs, r_off, w1, s1, g), "layer gate_up")
+    rqa, rsa, _ = O.silu_mul_quant_fp8(rh1)
+    ry2 = O.f32_to_bf16_bits(O.moe_grouped_linear(rqa, rsa, r_off, w2, s2, g))
+    r = O.moe_combine(ry2, r_w, r_ro).astype(np.float64)
+    yv = S.bf16_bits_to_f32(bits(out)).astype(np.float64)
+    rms = np.sqrt(np.mean(r * r))
+    err = np.abs(yv - r)
+    assert err.max() <= 0.02 * rms, f"layer: max err {err.max():.3e} vs rms {rms:.3e}"
+    rel = err / np.maximum(np.abs(r), 1e-2 * rms)
+    assert np.mean(rel <= 8e-3) >= 0.99
