@@ -296,7 +296,8 @@ def run_ours(args, rank, world, local_rank):
         "sm_count": torch.cuda.get_device_properties(dev).multi_processor_count,
     }
     if not args.no_rows:
-        line["rows"] = bench_rows(dev, stream, bf16_tf, peak_kind, hbm)
+        only = set(args.rows.split(",")) if args.rows else None
+        line["rows"] = bench_rows(dev, stream, bf16_tf, peak_kind, hbm, only)
     return line
 
 
@@ -326,7 +327,8 @@ def _time_graph(torch, stream, fn, calls, replays, warmup=3):
     return e0.elapsed_time(e1) / (calls * replays)
 
 
-def bench_rows(dev, stream, bf16_tf, peak_kind, hbm_peak):
+def bench_rows(dev, stream, bf16_tf, peak_kind, hbm_peak, only=None):
+    """The other rows; ``only`` (a set of row names) limits which run."""
     import torch
     import int4_weight_quantized_w4_gb300 as w4
 
@@ -337,6 +339,9 @@ def bench_rows(dev, stream, bf16_tf, peak_kind, hbm_peak):
         return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
     rows = {}
+
+    def want(name):
+        return only is None or name in only
 
     def dense(name, M, N, K, group, outliers):
         g = K if group == -1 else group
@@ -383,135 +388,141 @@ def bench_rows(dev, stream, bf16_tf, peak_kind, hbm_peak):
             "l2": "inputs + outputs per step larger than L2",
         }
 
-    dense("w4a8_prefill", 4096, 11008, 4096, 128, 0.01)
-    dense("w4a8_diffusion", 16384, 3072, 3072, -1, 0.0)
+    if want("w4a8_prefill"):
+        dense("w4a8_prefill", 4096, 11008, 4096, 128, 0.01)
+    if want("w4a8_diffusion"):
+        dense("w4a8_diffusion", 16384, 3072, 3072, -1, 0.0)
 
-    # the routed MoE layer: 4096 tokens, hidden 2048, 64 experts, top-8,
-    # intermediate 1408 (gate_up N = 2816, down K = 1408)
-    T, E, top, g, Hd, I = 4096, 64, 8, 128, 2048, 1408
-    R = T * top
-    lg = on(S.router_logits(T, E, seed=5))
-    xt = bf16(S.activations_bf16(T, Hd, seed=0))
-    w1, s1 = on(S.random_words((E, 2 * I, Hd // 8), seed=1)), on(S.scales_f16((E, 2 * I, Hd // g), seed=2))
-    w2 = on(S.random_words((E, Hd, I // 8), seed=1, tag=21))
-    s2 = on(S.scales_f16((E, Hd, I // g), seed=2, tag=31))
-    route = w4.w4_moe_route(lg, top, True)
-    ids, wts, off, rt, ro = route
-    h1 = torch.empty((R, 2 * I), dtype=torch.bfloat16, device=dev)
-    sx1 = torch.empty((R,), dtype=torch.float32, device=dev)
-    qa = torch.empty((R, I), dtype=torch.float8_e4m3fn, device=dev)
-    sa = torch.empty((R,), dtype=torch.float32, device=dev)
-    y2 = torch.empty((R, Hd), dtype=torch.bfloat16, device=dev)
-    out = torch.empty((T, Hd), dtype=torch.bfloat16, device=dev)
-    ws = torch.empty((max(w4.w4_workspace_bytes(w4.W4_OP_W4AFP8_MOE, R, 2 * I, Hd, g),
-                          w4.w4_workspace_bytes(w4.W4_OP_W4AFP8_MOE, R, Hd, I, g)),), dtype=torch.uint8, device=dev)
-    rws = torch.empty((max(16, w4.w4_workspace_bytes(w4.W4_OP_MOE_ROUTE, T, E, 1, 0)),), dtype=torch.uint8,
-                      device=dev)
+    if want('w4afp8_moe'):
+        # the routed MoE layer: 4096 tokens, hidden 2048, 64 experts, top-8,
+        # intermediate 1408 (gate_up N = 2816, down K = 1408)
+        T, E, top, g, Hd, I = 4096, 64, 8, 128, 2048, 1408
+        R = T * top
+        lg = on(S.router_logits(T, E, seed=5))
+        xt = bf16(S.activations_bf16(T, Hd, seed=0))
+        w1, s1 = on(S.random_words((E, 2 * I, Hd // 8), seed=1)), on(S.scales_f16((E, 2 * I, Hd // g), seed=2))
+        w2 = on(S.random_words((E, Hd, I // 8), seed=1, tag=21))
+        s2 = on(S.scales_f16((E, Hd, I // g), seed=2, tag=31))
+        route = w4.w4_moe_route(lg, top, True)
+        ids, wts, off, rt, ro = route
+        h1 = torch.empty((R, 2 * I), dtype=torch.bfloat16, device=dev)
+        sx1 = torch.empty((R,), dtype=torch.float32, device=dev)
+        qa = torch.empty((R, I), dtype=torch.float8_e4m3fn, device=dev)
+        sa = torch.empty((R,), dtype=torch.float32, device=dev)
+        y2 = torch.empty((R, Hd), dtype=torch.bfloat16, device=dev)
+        out = torch.empty((T, Hd), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty((max(w4.w4_workspace_bytes(w4.W4_OP_W4AFP8_MOE, R, 2 * I, Hd, g),
+                              w4.w4_workspace_bytes(w4.W4_OP_W4AFP8_MOE, R, Hd, I, g)),), dtype=torch.uint8, device=dev)
+        rws = torch.empty((max(16, w4.w4_workspace_bytes(w4.W4_OP_MOE_ROUTE, T, E, 1, 0)),), dtype=torch.uint8,
+                          device=dev)
 
-    def st_route():
-        w4.w4_moe_route(lg, top, True, out=route, workspace=rws, stream=stream)
+        def st_route():
+            w4.w4_moe_route(lg, top, True, out=route, workspace=rws, stream=stream)
 
-    def st_gate_up():
-        w4.w4afp8_moe_gemm_bf16in(xt, rt, off, w1, s1, g, y=h1, x_scale=sx1, workspace=ws, stream=stream)
+        def st_gate_up():
+            w4.w4afp8_moe_gemm_bf16in(xt, rt, off, w1, s1, g, y=h1, x_scale=sx1, workspace=ws, stream=stream)
 
-    def st_act():
-        w4.w4_moe_silu_mul_quant_fp8(h1, q=qa, scale=sa, stream=stream)
+        def st_act():
+            w4.w4_moe_silu_mul_quant_fp8(h1, q=qa, scale=sa, stream=stream)
 
-    def st_down():
-        w4.w4afp8_moe_grouped_gemm(qa, sa, off, w2, s2, g, y=y2, workspace=ws, stream=stream)
+        def st_down():
+            w4.w4afp8_moe_grouped_gemm(qa, sa, off, w2, s2, g, y=y2, workspace=ws, stream=stream)
 
-    def st_combine():
-        w4.w4_moe_combine(y2, wts, ro, out=out, stream=stream)
+        def st_combine():
+            w4.w4_moe_combine(y2, wts, ro, out=out, stream=stream)
 
-    def moe_layer():
-        st_route()
-        st_gate_up()
-        st_act()
-        st_down()
-        st_combine()
+        def moe_layer():
+            st_route()
+            st_gate_up()
+            st_act()
+            st_down()
+            st_combine()
 
-    t_layer = _time_graph(torch, stream, moe_layer, 3, 10)
-    t_st = {nm: _time_graph(torch, stream, fn, 3, 10) for nm, fn in
-            (("route", st_route), ("gate_up", st_gate_up), ("act", st_act), ("down", st_down),
-             ("combine", st_combine))}
-    flops = 2.0 * R * (2 * I) * Hd + 2.0 * R * Hd * I
-    t_gemm = t_st["gate_up"] + t_st["down"]
-    tf_gemm = flops / (t_gemm * 1e-3) / 1e12
-    act_bytes = R * 2 * I * 2 + R * I + R * 4
-    comb_bytes = R * Hd * 2 + T * top * 8 + T * Hd * 2
-    rows["w4afp8_moe"] = {
-        "config": {"tokens": T, "hidden": Hd, "experts": E, "top_k": top, "intermediate": I, "rows": R,
-                   "gate_up": [Hd, 2 * I], "down": [I, Hd], "group": g, "renormalize": True},
-        "value": round(flops / (t_layer * 1e-3) / 1e12, 1), "unit": "TFLOP/s", "ms_per_step": t_layer,
-        "step": "the whole routed layer: route, gather + fp8 quant + gate_up GEMM, SiLU*up + fp8 requant, "
-                "down GEMM, weighted combine",
-        "stage_ms": {k: round(v, 5) for k, v in t_st.items()},
-        "gemm_tflops": round(tf_gemm, 1),
-        "act_gbs": round(act_bytes / (t_st["act"] * 1e-3) / 1e9, 1),
-        "combine_gbs": round(comb_bytes / (t_st["combine"] * 1e-3) / 1e9, 1),
-        "roofline": {"bound": "tensor", "achieved": round(tf_gemm, 1), "peak": bf16_tf, "unit": "TFLOP/s",
-                     "frac": round(tf_gemm / bf16_tf, 4), "traffic": None,
-                     "peak_source": f"{peak_kind} bf16_tflops (e4m3 activations widened to exact fp16; "
-                                    "fp16 tensor datapath)",
-                     "kernel": "the two grouped GEMM calls (quantize/widen + w4a8_tc_kernel each)"},
-    }
-    # weight-side tools (load time): the group quantizer on a 14336 x 4096 bf16
-    # weight, and the XOR 0x88 repack of a 64-expert [E, N, K/2] int4 tensor
-    Nq, Kq, gq = 14336, 4096, 128
-    blk = S.to_bf16_bits(S.normal(0, 90, 1024 * Kq).reshape(1024, Kq) * 0.05)
-    wq = bf16(np.tile(blk, (Nq // 1024, 1)))
-    pk = torch.empty((Nq, Kq // 2), dtype=torch.uint8, device=dev)
-    sq = torch.empty((Nq, Kq // gq), dtype=torch.float32, device=dev)
-    zq = torch.empty((Nq, Kq // gq), dtype=torch.float32, device=dev)
-    t_q = _time_graph(torch, stream, lambda: w4.w4_quantize_groupwise(wq, gq, pk, sq, zq, stream=stream), 5, 10)
-    qbytes = Nq * Kq * 2 + Nq * Kq // 2 + 2 * Nq * (Kq // gq) * 4
-    rows["weight_quantize_groupwise"] = {
-        "config": {"N": Nq, "K": Kq, "group": gq, "w": "bf16"}, "value": round(qbytes / (t_q * 1e-3) / 1e9, 1),
-        "unit": "GB/s", "ms_per_step": t_q,
-        "roofline": {"bound": "hbm", "achieved": round(qbytes / (t_q * 1e-3) / 1e9, 1), "peak": hbm_peak,
-                     "unit": "GB/s", "frac": round(qbytes / (t_q * 1e-3) / 1e9 / hbm_peak, 4), "traffic": None,
-                     "kernel": "quantize_groupwise_kernel", "algorithmic_bytes_per_launch": qbytes},
-    }
-    # tied embedding table used as the decode output head: one token against a
-    # 131072 x 2048 group-128 table (4 rotating copies, 604 MB, more than L2)
-    V, D, gh = 131072, 2048, 128
-    tabs = []
-    for c in range(4):
-        pk = on(np.tile(S.raw_u64(c, 97, 1024 * D // 16).view(np.uint8).reshape(1024, D // 2), (V // 1024, 1)))
-        scl = on(np.tile((0.002 + 0.001 * S.uniform(c, 98, 1024 * D // gh)).astype(np.float32).reshape(1024, D // gh),
-                         (V // 1024, 1)))
-        zr = on(np.tile((0.01 * S.normal(c, 99, 1024 * D // gh)).astype(np.float32).reshape(1024, D // gh),
-                        (V // 1024, 1)))
-        tabs.append((pk, scl, zr))
-    hh = bf16(S.activations_bf16(1, D, seed=0))
-    yh = torch.empty((1, V), dtype=torch.bfloat16, device=dev)
-    it = [0]
+        t_layer = _time_graph(torch, stream, moe_layer, 3, 10)
+        t_st = {nm: _time_graph(torch, stream, fn, 3, 10) for nm, fn in
+                (("route", st_route), ("gate_up", st_gate_up), ("act", st_act), ("down", st_down),
+                 ("combine", st_combine))}
+        flops = 2.0 * R * (2 * I) * Hd + 2.0 * R * Hd * I
+        t_gemm = t_st["gate_up"] + t_st["down"]
+        tf_gemm = flops / (t_gemm * 1e-3) / 1e12
+        act_bytes = R * 2 * I * 2 + R * I + R * 4
+        comb_bytes = R * Hd * 2 + T * top * 8 + T * Hd * 2
+        rows["w4afp8_moe"] = {
+            "config": {"tokens": T, "hidden": Hd, "experts": E, "top_k": top, "intermediate": I, "rows": R,
+                       "gate_up": [Hd, 2 * I], "down": [I, Hd], "group": g, "renormalize": True},
+            "value": round(flops / (t_layer * 1e-3) / 1e12, 1), "unit": "TFLOP/s", "ms_per_step": t_layer,
+            "step": "the whole routed layer: route, gather + fp8 quant + gate_up GEMM, SiLU*up + fp8 requant, "
+                    "down GEMM, weighted combine",
+            "stage_ms": {k: round(v, 5) for k, v in t_st.items()},
+            "gemm_tflops": round(tf_gemm, 1),
+            "act_gbs": round(act_bytes / (t_st["act"] * 1e-3) / 1e9, 1),
+            "combine_gbs": round(comb_bytes / (t_st["combine"] * 1e-3) / 1e9, 1),
+            "roofline": {"bound": "tensor", "achieved": round(tf_gemm, 1), "peak": bf16_tf, "unit": "TFLOP/s",
+                         "frac": round(tf_gemm / bf16_tf, 4), "traffic": None,
+                         "peak_source": f"{peak_kind} bf16_tflops (e4m3 activations widened to exact fp16; "
+                                        "fp16 tensor datapath)",
+                         "kernel": "the two grouped GEMM calls (quantize/widen + w4a8_tc_kernel each)"},
+        }
+    if want('weight_quantize_groupwise'):
+        # weight-side tool (load time): the group quantizer on a 14336 x 4096 bf16 weight
+        Nq, Kq, gq = 14336, 4096, 128
+        blk = S.to_bf16_bits(S.normal(0, 90, 1024 * Kq).reshape(1024, Kq) * 0.05)
+        wq = bf16(np.tile(blk, (Nq // 1024, 1)))
+        pk = torch.empty((Nq, Kq // 2), dtype=torch.uint8, device=dev)
+        sq = torch.empty((Nq, Kq // gq), dtype=torch.float32, device=dev)
+        zq = torch.empty((Nq, Kq // gq), dtype=torch.float32, device=dev)
+        t_q = _time_graph(torch, stream, lambda: w4.w4_quantize_groupwise(wq, gq, pk, sq, zq, stream=stream), 5, 10)
+        qbytes = Nq * Kq * 2 + Nq * Kq // 2 + 2 * Nq * (Kq // gq) * 4
+        rows["weight_quantize_groupwise"] = {
+            "config": {"N": Nq, "K": Kq, "group": gq, "w": "bf16"}, "value": round(qbytes / (t_q * 1e-3) / 1e9, 1),
+            "unit": "GB/s", "ms_per_step": t_q,
+            "roofline": {"bound": "hbm", "achieved": round(qbytes / (t_q * 1e-3) / 1e9, 1), "peak": hbm_peak,
+                         "unit": "GB/s", "frac": round(qbytes / (t_q * 1e-3) / 1e9 / hbm_peak, 4), "traffic": None,
+                         "kernel": "quantize_groupwise_kernel", "algorithmic_bytes_per_launch": qbytes},
+        }
+    if want('lm_head_gemv'):
+        # tied embedding table used as the decode output head: one token against a
+        # 131072 x 2048 group-128 table (4 rotating copies, 604 MB, more than L2)
+        V, D, gh = 131072, 2048, 128
+        tabs = []
+        for c in range(4):
+            pk = on(np.tile(S.raw_u64(c, 97, 1024 * D // 16).view(np.uint8).reshape(1024, D // 2), (V // 1024, 1)))
+            scl = on(np.tile((0.002 + 0.001 * S.uniform(c, 98, 1024 * D // gh)).astype(np.float32).reshape(1024, D // gh),
+                             (V // 1024, 1)))
+            zr = on(np.tile((0.01 * S.normal(c, 99, 1024 * D // gh)).astype(np.float32).reshape(1024, D // gh),
+                            (V // 1024, 1)))
+            tabs.append((pk, scl, zr))
+        hh = bf16(S.activations_bf16(1, D, seed=0))
+        yh = torch.empty((1, V), dtype=torch.bfloat16, device=dev)
+        it = [0]
 
-    def head():
-        pk, scl, zr = tabs[it[0] % 4]
-        it[0] += 1
-        w4.w4_lm_head_gemv(hh, pk, scl, zr, gh, y=yh, stream=stream)
+        def head():
+            pk, scl, zr = tabs[it[0] % 4]
+            it[0] += 1
+            w4.w4_lm_head_gemv(hh, pk, scl, zr, gh, y=yh, stream=stream)
 
-    t_h = _time_graph(torch, stream, head, 8, 10)
-    hbytes = V * D // 2 + 2 * V * (D // gh) * 4 + D * 2 + V * 2
-    rows["lm_head_gemv"] = {
-        "config": {"M": 1, "V": V, "D": D, "group": gh, "scale_zero": "f32", "l2": "4 rotating tables (604 MB)"},
-        "value": round(hbytes / (t_h * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": t_h,
-        "roofline": {"bound": "hbm", "achieved": round(hbytes / (t_h * 1e-3) / 1e9, 1), "peak": hbm_peak,
-                     "unit": "GB/s", "frac": round(hbytes / (t_h * 1e-3) / 1e9 / hbm_peak, 4), "traffic": None,
-                     "kernel": "lm_head_kernel", "algorithmic_bytes_per_launch": hbytes},
-    }
-    rb = 64 * 2816 * 1024
-    s4 = on((S.raw_u64(8, 80, rb // 8).view(np.uint8)))
-    s4o = torch.empty_like(s4)
-    t_r = _time_graph(torch, stream, lambda: w4.w4_repack_s4_to_uint4b8(s4, s4o, stream=stream), 5, 10)
-    rows["s4_repack_uint4b8"] = {
-        "config": {"bytes": rb, "layout": "[64, 2816, 1024] int8 -> int32 [64, 2816, 256]"},
-        "value": round(2 * rb / (t_r * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": t_r,
-        "roofline": {"bound": "hbm", "achieved": round(2 * rb / (t_r * 1e-3) / 1e9, 1), "peak": hbm_peak,
-                     "unit": "GB/s", "frac": round(2 * rb / (t_r * 1e-3) / 1e9 / hbm_peak, 4), "traffic": None,
-                     "kernel": "xor88_kernel", "algorithmic_bytes_per_launch": 2 * rb},
-    }
+        t_h = _time_graph(torch, stream, head, 8, 10)
+        hbytes = V * D // 2 + 2 * V * (D // gh) * 4 + D * 2 + V * 2
+        rows["lm_head_gemv"] = {
+            "config": {"M": 1, "V": V, "D": D, "group": gh, "scale_zero": "f32", "l2": "4 rotating tables (604 MB)"},
+            "value": round(hbytes / (t_h * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": t_h,
+            "roofline": {"bound": "hbm", "achieved": round(hbytes / (t_h * 1e-3) / 1e9, 1), "peak": hbm_peak,
+                         "unit": "GB/s", "frac": round(hbytes / (t_h * 1e-3) / 1e9 / hbm_peak, 4), "traffic": None,
+                         "kernel": "lm_head_kernel", "algorithmic_bytes_per_launch": hbytes},
+        }
+    if want('s4_repack_uint4b8'):
+        # weight-side tool (load time): the XOR 0x88 repack of a 64-expert [E, N, K/2] int4 tensor
+        rb = 64 * 2816 * 1024
+        s4 = on((S.raw_u64(8, 80, rb // 8).view(np.uint8)))
+        s4o = torch.empty_like(s4)
+        t_r = _time_graph(torch, stream, lambda: w4.w4_repack_s4_to_uint4b8(s4, s4o, stream=stream), 5, 10)
+        rows["s4_repack_uint4b8"] = {
+            "config": {"bytes": rb, "layout": "[64, 2816, 1024] int8 -> int32 [64, 2816, 256]"},
+            "value": round(2 * rb / (t_r * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": t_r,
+            "roofline": {"bound": "hbm", "achieved": round(2 * rb / (t_r * 1e-3) / 1e9, 1), "peak": hbm_peak,
+                         "unit": "GB/s", "frac": round(2 * rb / (t_r * 1e-3) / 1e9 / hbm_peak, 4), "traffic": None,
+                         "kernel": "xor88_kernel", "algorithmic_bytes_per_launch": 2 * rb},
+        }
     return rows
 
 
@@ -587,6 +598,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rows", action="store_true", help="time only the headline workload")
+    ap.add_argument("--rows", default="", help="comma-separated names of the other rows to run (default: all)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
