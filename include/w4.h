@@ -367,9 +367,9 @@ w4_status w4_embedding_gather(const int32_t* ids, int64_t T, const void* table, 
  * bf16(sum_d h[m, d] * ((q[v, d] - 8) * scale[v, d / group] + zero[v, d / group]))
  * with fp32 accumulation, h [M, D] bf16, y [M, V] bf16, read from the same
  * table (16-byte aligned). Built for small M (tokens in blocks of 8, each one
- * pass over the table); D % 32 == 0 and D <= 5792 (8 rows of h and their
- * per-word sums in shared memory), else W4_ERR_UNSUPPORTED. M == 0 does
- * nothing.
+ * pass over the table); D % 32 == 0, and D <= 8192 when D and the group are
+ * multiples of 128 (tensor-core form), else D <= 5792 (8 rows of h in shared
+ * memory), otherwise W4_ERR_UNSUPPORTED. M == 0 does nothing.
  */
 w4_status w4_lm_head_gemv(const void* h, int64_t M, const void* table, const float* scale, const float* zero,
                           int64_t V, int64_t D, int32_t group, void* y, void* stream);

@@ -435,7 +435,10 @@ w4_status w4_lm_head_gemv(const void* h, int64_t M, const void* table, const flo
   if (st != W4_OK) return st;
   if (M < 0) return fail(W4_ERR_SHAPE, "M must be >= 0");
   if (D % 32 != 0) return fail(W4_ERR_UNSUPPORTED, "the head reads rows 32 codes at a time: D=%lld", (long long)D);
-  if (D * 40 > 227 * 1024)   // 8 rows of h padded to 36 floats per 32, plus D/8 word sums each
+  // 8 rows of h in shared memory: as fp16 in MMA order (D and the group multiples of 128), else as fp32 padded to
+  // 36 floats per 32 plus D/8 word sums each
+  const bool tc = D % 128 == 0 && g % 128 == 0;
+  if (tc ? D > 8192 : D * 40 > 227 * 1024)
     return fail(W4_ERR_UNSUPPORTED, "the head keeps 8 rows of h in shared memory: D=%lld is too long", (long long)D);
   if (M == 0) return ok();
   if (!h || !table || !scale || !zero || !y) return fail(W4_ERR_NULL, "h, table, scale, zero, y must be non-NULL");

@@ -11,13 +11,26 @@
 // Gather: one thread per 8 codes; the fp32 steps are taken one by one with
 // IEEE rounding (__fmul_rn, __fadd_rn), so the rows are bit-exact.
 //
-// Head: logits[m, v] = sum_d h[m, d] * w[v, d] for decode (M <= 8 tokens).
-// One warp per vocabulary row at a time (the row is D/2 contiguous bytes, read
-// with 16-byte loads), h held in shared memory as fp32. A nibble becomes its
-// float exactly by placing it in the mantissa of 2^23 (0x4B000000 | q is
-// 2^23 + q) and subtracting 2^23; per 8-code word the partial is folded as
+// Head: logits[m, v] = sum_d h[m, d] * w[v, d] for decode, tokens in blocks
+// of 8 (one pass over the table per block). Bound: HBM (the table is read
+// once per pass). Per scale group the partial is folded as
 // s * (sum h q - 8 sum h) + z * sum h, so no weight is ever dequantized.
-// Bound: HBM (the table is read once per call).
+//
+// Tensor-core form (D and the group multiples of 128, D <= 8192): a warp
+// owns 16-row tiles of the table and runs swap-AB m16n8k16 MMAs (table rows
+// are the MMA rows, the 8 tokens its columns, fp16 in, fp32 accumulate) over
+// 128-code segments. Lane (g, t) loads bytes [16t, 16t + 16) of the segment
+// from rows g and g + 8 straight from global memory, 4 segments ahead, and
+// turns every word into 4 A registers with one AND each: nibbles in bits 0-3
+// of an fp16 half are the exact subnormal q 2^-24, nibbles in bits 4-7 are
+// 16 q 2^-24 (the h values they meet carry an extra 1/16). The k order inside
+// a segment is permuted the same way for h, which every CTA stages once in
+// shared memory as fp16 2^e h, with 2^e a power of two per (segment, token)
+// that puts the segment's largest |h| in [2^14, 2^15) (exact; the fold
+// multiplies by 2^-e). Other shapes: one warp per row on the FMA pipes, a
+// nibble becoming its float as float(0x4B000000 | q) - 2^23.
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -158,6 +171,158 @@ __global__ void __launch_bounds__(kHeadWarps * 32) lm_head_kernel(const uint16_t
   }
 }
 
+constexpr int kTcWarps = 8;
+constexpr int kTcAhead = 4;        // segments of loads in flight per warp
+constexpr int kSegBytes = 288;     // one (segment, token) block of staged h: 4 x 64 B + 32 B of padding
+
+W4_DEV void mma_f16_acc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                        uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Staged h for one (segment, token, lane quad position t): the 32 codes
+// [32t, 32t + 32) of the segment in MMA order. For word c' (codes 32t + 8c'
+// + j) and half h' the B registers are (x[2h'], x[2h' + 4]) and
+// (x[2h' + 1], x[2h' + 5]) / 16 with x the word's 8 values.
+W4_DEV int stage_offset(int seg, int token, int t) { return (seg * 8 + token) * kSegBytes + t * 64 + (t >> 1) * 16; }
+
+__global__ void __launch_bounds__(kTcWarps * 32) lm_head_tc_kernel(const uint16_t* __restrict__ h, int Mact,
+                                                                     const uint8_t* __restrict__ table,
+                                                                     const float* __restrict__ scale,
+                                                                     const float* __restrict__ zero, int64_t V,
+                                                                     int D, int group, uint16_t* __restrict__ y) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int S = D / 128;
+  float4* fold = reinterpret_cast<float4*>(smem + S * 8 * kSegBytes);   // [S][4]: (X_2t, X_2t+1, f_2t, f_2t+1)
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+
+  // --- stage h: one warp per (segment, token); lane i holds codes 4i..4i+3
+  for (int task = warp; task < S * 8; task += kTcWarps) {
+    const int seg = task >> 3, tok = task & 7;
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    if (tok < Mact) {
+      const uint16_t* hp = h + static_cast<int64_t>(tok) * D + seg * 128 + lane * 4;   // h is only 2-byte aligned
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(static_cast<uint32_t>(hp[i]) << 16);
+    }
+    float mx = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+    float sm = (v[0] + v[1]) + (v[2] + v[3]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      sm += __shfl_xor_sync(0xffffffffu, sm, o);
+    }
+    int ex = 0;
+    if (mx > 0.f) frexpf(mx, &ex);           // mx = m 2^ex, m in [0.5, 1)
+    const int e = mx > 0.f ? 15 - ex : 0;    // largest |h| 2^e in [2^14, 2^15)
+    // code c = 4 lane + i sits in chunk t = c / 32, word c' = (c % 32) / 8, slot j = c % 8
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int c = lane * 4 + i;
+      const int tt = c >> 5, cw = (c & 31) >> 3, j = c & 7;
+      // j -> (half h', register r, element): j = 2h' + {0: r0 lo, 4: r0 hi, 1: r1 lo, 5: r1 hi}
+      const int hp = (j >> 1) & 1, odd = j & 1, hi = j >> 2;
+      const int reg = cw * 4 + hp * 2 + odd;    // B register index 0..15 within (seg, tok, tt)
+      const float xv = ldexpf(v[i], odd ? e - 4 : e);
+      const __half hv = __float2half_rn(xv);
+      uint16_t* dst = reinterpret_cast<uint16_t*>(smem + stage_offset(seg, tok, tt)) + reg * 2 + hi;
+      *dst = __half_as_ushort(hv);
+    }
+    if (lane < 1) {
+      // fold data for the token pair (tok & ~1, tok | 1) lives at fold[seg * 4 + tok / 2]
+      float* f = reinterpret_cast<float*>(&fold[seg * 4 + (tok >> 1)]);
+      f[tok & 1] = ldexpf(sm, -24);
+      f[2 + (tok & 1)] = ldexpf(1.f, -e);
+    }
+  }
+  __syncthreads();
+
+  const int64_t ntiles = (V + 15) / 16;
+  const int64_t wg = static_cast<int64_t>(blockIdx.x) * kTcWarps + warp;
+  const int64_t nw = static_cast<int64_t>(gridDim.x) * kTcWarps;
+  if (wg >= ntiles) return;
+  const int64_t my_tiles = (ntiles - 1 - wg) / nw + 1;
+  const int64_t npos = my_tiles * S;
+  const int64_t rowb = D / 2;
+  const int G = D / group, spg = group / 128;   // segments per scale group
+
+  // load cursor
+  int64_t ltile = wg;
+  int lseg = 0;
+  auto load = [&](uint4& a, uint4& b) {
+    const int64_t r0 = ltile * 16 + g, r1 = r0 + 8;
+    const int64_t ra = r0 < V ? r0 : V - 1, rb = r1 < V ? r1 : V - 1;
+    a = ld_stream_v4(table + ra * rowb + lseg * 64 + t * 16);
+    b = ld_stream_v4(table + rb * rowb + lseg * 64 + t * 16);
+    if (++lseg == S) {
+      lseg = 0;
+      ltile += nw;
+    }
+  };
+  uint4 A[kTcAhead][2];
+#pragma unroll
+  for (int p = 0; p < kTcAhead; ++p)
+    if (p < npos) load(A[p][0], A[p][1]);
+
+  int64_t ctile = wg;
+  int cseg = 0;
+  float tot[4] = {0.f, 0.f, 0.f, 0.f};
+  float s0 = 0.f, z0 = 0.f, s1 = 0.f, z1 = 0.f;
+  for (int64_t pos0 = 0; pos0 < npos; pos0 += kTcAhead) {
+#pragma unroll
+    for (int p = 0; p < kTcAhead; ++p) {
+      if (pos0 + p < npos) {
+        const int64_t r0 = ctile * 16 + g;
+        if (cseg % spg == 0) {                    // a new scale group for this tile's rows
+          const int64_t ra = r0 < V ? r0 : V - 1, rb = r0 + 8 < V ? r0 + 8 : V - 1;
+          const int grp = cseg / spg;
+          s0 = __ldg(scale + ra * G + grp);
+          z0 = __ldg(zero + ra * G + grp);
+          s1 = __ldg(scale + rb * G + grp);
+          z1 = __ldg(zero + rb * G + grp);
+        }
+        const uint4* bp = reinterpret_cast<const uint4*>(smem + stage_offset(cseg, g, t));
+        const uint4 B0 = bp[0], B1 = bp[1], B2 = bp[2], B3 = bp[3];
+        const uint32_t b[16] = {B0.x, B0.y, B0.z, B0.w, B1.x, B1.y, B1.z, B1.w,
+                                B2.x, B2.y, B2.z, B2.w, B3.x, B3.y, B3.z, B3.w};
+        const uint32_t wv[4] = {A[p][0].x, A[p][0].y, A[p][0].z, A[p][0].w};
+        const uint32_t vv[4] = {A[p][1].x, A[p][1].y, A[p][1].z, A[p][1].w};
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int cw = 0; cw < 4; ++cw) {
+          mma_f16_acc(acc, wv[cw] & 0x000F000Fu, vv[cw] & 0x000F000Fu, wv[cw] & 0x00F000F0u, vv[cw] & 0x00F000F0u,
+                      b[cw * 4 + 0], b[cw * 4 + 1]);
+          const uint32_t w2 = wv[cw] >> 8, v2 = vv[cw] >> 8;
+          mma_f16_acc(acc, w2 & 0x000F000Fu, v2 & 0x000F000Fu, w2 & 0x00F000F0u, v2 & 0x00F000F0u, b[cw * 4 + 2],
+                      b[cw * 4 + 3]);
+        }
+        if (pos0 + p + kTcAhead < npos) load(A[p][0], A[p][1]);
+        const float4 f = fold[cseg * 4 + t];
+        tot[0] = fmaf(s0 * f.z, acc[0], fmaf(fmaf(-8.f, s0, z0), f.x, tot[0]));
+        tot[1] = fmaf(s0 * f.w, acc[1], fmaf(fmaf(-8.f, s0, z0), f.y, tot[1]));
+        tot[2] = fmaf(s1 * f.z, acc[2], fmaf(fmaf(-8.f, s1, z1), f.x, tot[2]));
+        tot[3] = fmaf(s1 * f.w, acc[3], fmaf(fmaf(-8.f, s1, z1), f.y, tot[3]));
+        if (++cseg == S) {                        // tile done: rows g, g + 8; tokens 2t, 2t + 1
+          const int64_t r1 = r0 + 8;
+          const int m0 = 2 * t, m1 = 2 * t + 1;
+          if (r0 < V && m0 < Mact) y[m0 * V + r0] = static_cast<uint16_t>(f32_to_bf16_bits(tot[0] * 16777216.f));
+          if (r0 < V && m1 < Mact) y[m1 * V + r0] = static_cast<uint16_t>(f32_to_bf16_bits(tot[1] * 16777216.f));
+          if (r1 < V && m0 < Mact) y[m0 * V + r1] = static_cast<uint16_t>(f32_to_bf16_bits(tot[2] * 16777216.f));
+          if (r1 < V && m1 < Mact) y[m1 * V + r1] = static_cast<uint16_t>(f32_to_bf16_bits(tot[3] * 16777216.f));
+          tot[0] = tot[1] = tot[2] = tot[3] = 0.f;
+          cseg = 0;
+          ctile += nw;
+        }
+      }
+    }
+  }
+}
+
 int sm_count_embed() {
   static int n = 0;
   if (n == 0) {
@@ -209,15 +374,39 @@ cudaError_t launch_embedding_gather(const int32_t* ids, int64_t T, const void* t
   return cudaGetLastError();
 }
 
+cudaError_t launch_head_tc(const void* h, int Mact, const void* table, const float* scale, const float* zero,
+                           int64_t V, int D, int group, void* y, cudaStream_t s) {
+  const int S = D / 128;
+  const size_t smem = static_cast<size_t>(S) * 8 * kSegBytes + static_cast<size_t>(S) * 4 * sizeof(float4);
+  cudaError_t e = cudaFuncSetAttribute(lm_head_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, lm_head_tc_kernel, kTcWarps * 32, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) per_sm = 1;
+  const int64_t ntiles = (V + 15) / 16;
+  const int64_t want = (ntiles + kTcWarps - 1) / kTcWarps;
+  const int64_t cap = static_cast<int64_t>(sm_count_embed()) * per_sm;   // one wave
+  const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
+  lm_head_tc_kernel<<<grid, kTcWarps * 32, smem, s>>>(static_cast<const uint16_t*>(h), Mact,
+                                                      static_cast<const uint8_t*>(table), scale, zero, V, D, group,
+                                                      static_cast<uint16_t*>(y));
+  return cudaGetLastError();
+}
+
 cudaError_t launch_lm_head(const void* h, int64_t M, const void* table, const float* scale, const float* zero,
                            int64_t V, int64_t D, int32_t group, void* y, cudaStream_t s) {
   const int Di = static_cast<int>(D);
+  const bool tc = D % 128 == 0 && group % 128 == 0 && D <= 8192;
   for (int64_t m0 = 0; m0 < M; m0 += kHeadTok) {
     const int mb = static_cast<int>(M - m0 < kHeadTok ? M - m0 : kHeadTok);
     const void* hb = static_cast<const uint16_t*>(h) + m0 * D;
     void* yb = static_cast<uint16_t*>(y) + m0 * V;
     cudaError_t e;
-    if (mb == 1) {
+    if (tc) {
+      e = launch_head_tc(hb, mb, table, scale, zero, V, Di, group, yb, s);
+    } else if (mb == 1) {
       e = head_cpl<1>(hb, mb, table, scale, zero, V, Di, group, yb, s);
     } else if (mb <= 2) {
       e = head_cpl<2>(hb, mb, table, scale, zero, V, Di, group, yb, s);

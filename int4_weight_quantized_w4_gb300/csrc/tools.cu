@@ -11,9 +11,14 @@
 // vLLM API docs, quantization.w4afp8, _repack_signed_int4_to_uint4b8:
 // signed int4 nibbles become uint4b8 (q + 8 mod 16) by XOR 0x88 on every byte.
 //
-// Both are bandwidth-bound load-time passes: one warp per (row, group) for the
-// quantizer (the group is read twice, the second time from L1), and 16-byte
-// vectors for the repack.
+// Both are bandwidth-bound load-time passes. Groups are contiguous in memory
+// (row n's group j starts at element n K + j group), so the quantizer walks
+// the weight as one flat array of 8-element chunks: for groups of 8 to 256
+// elements one thread takes one chunk (a 16-byte load, kept in registers),
+// the group's kC = group / 8 neighbouring lanes reduce its min and max with
+// shuffles, and every thread stores its 8 codes as one 32-bit word. Other
+// groups take one warp per (row, group), reading the group twice (the
+// second time from L1). The repack moves 16-byte vectors.
 #include "common.cuh"
 #include "launch.h"
 
@@ -62,6 +67,49 @@ __global__ void __launch_bounds__(256) quantize_groupwise_kernel(const uint16_t*
   }
 }
 
+// kC chunks of 8 elements per group (1..32, a power of two); chunk i of the
+// flat array belongs to group i / kC.
+template <bool kF16, int kC>
+__global__ void __launch_bounds__(256) quantize_chunks_kernel(const uint4* __restrict__ w, int64_t chunks,
+                                                              uint32_t* __restrict__ packed, float* __restrict__ scale,
+                                                              float* __restrict__ zero) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const bool live = i < chunks;   // dead lanes still join the shuffles
+  float v[8];
+  if (live) {
+    const uint4 c = ld_stream_v4(w + i);
+    const uint32_t u[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[2 * j] = kF16 ? half_bits_to_f32(u[j] & 0xFFFFu) : bf16_lo(u[j]);
+      v[2 * j + 1] = kF16 ? half_bits_to_f32(u[j] >> 16) : bf16_hi(u[j]);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = 0.f;
+  }
+  float mn = fminf(fminf(fminf(v[0], v[1]), fminf(v[2], v[3])), fminf(fminf(v[4], v[5]), fminf(v[6], v[7])));
+  float mx = fmaxf(fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])), fmaxf(fmaxf(v[4], v[5]), fmaxf(v[6], v[7])));
+#pragma unroll
+  for (int o = kC / 2; o > 0; o >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  if (!live) return;
+  const float s = __fdiv_rn(fmaxf(__fsub_rn(mx, mn), 1e-9f), 15.0f);
+  uint32_t word = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int q = min(max(__float2int_rn(__fdiv_rn(__fsub_rn(v[j], mn), s)), 0), 15);
+    word |= static_cast<uint32_t>(q) << (4 * j);
+  }
+  packed[i] = word;
+  if ((i & (kC - 1)) == 0) {
+    scale[i / kC] = s;
+    zero[i / kC] = __fadd_rn(mn, __fmul_rn(8.0f, s));
+  }
+}
+
 __global__ void __launch_bounds__(256) xor88_kernel(const uint4* src, uint4* dst, size_t n16, const uint8_t* src_tail,
                                                     uint8_t* dst_tail, int tail) {
   const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
@@ -88,8 +136,33 @@ int sm_count_tools() {
 
 }  // namespace
 
+template <bool kF16>
+cudaError_t launch_chunks(const void* w, int64_t chunks, int32_t group, uint8_t* packed, float* scale, float* zero,
+                          cudaStream_t s) {
+  const unsigned int blocks = static_cast<unsigned int>((chunks + 255) / 256);
+  auto wp = static_cast<const uint4*>(w);
+  auto pp = reinterpret_cast<uint32_t*>(packed);
+  switch (group / 8) {
+    case 1: quantize_chunks_kernel<kF16, 1><<<blocks, 256, 0, s>>>(wp, chunks, pp, scale, zero); break;
+    case 2: quantize_chunks_kernel<kF16, 2><<<blocks, 256, 0, s>>>(wp, chunks, pp, scale, zero); break;
+    case 4: quantize_chunks_kernel<kF16, 4><<<blocks, 256, 0, s>>>(wp, chunks, pp, scale, zero); break;
+    case 8: quantize_chunks_kernel<kF16, 8><<<blocks, 256, 0, s>>>(wp, chunks, pp, scale, zero); break;
+    case 16: quantize_chunks_kernel<kF16, 16><<<blocks, 256, 0, s>>>(wp, chunks, pp, scale, zero); break;
+    default: quantize_chunks_kernel<kF16, 32><<<blocks, 256, 0, s>>>(wp, chunks, pp, scale, zero); break;
+  }
+  return cudaGetLastError();
+}
+
 cudaError_t launch_quantize_groupwise(const void* w, bool f16, int64_t N, int64_t K, int32_t group, uint8_t* packed,
                                       float* scale, float* zero, cudaStream_t s) {
+  const bool chunked = K % 8 == 0 && (group == 8 || group == 16 || group == 32 || group == 64 || group == 128 ||
+                                      group == 256) &&
+                       reinterpret_cast<uintptr_t>(w) % 16 == 0 && reinterpret_cast<uintptr_t>(packed) % 4 == 0;
+  if (chunked) {
+    const int64_t chunks = N * K / 8;
+    return f16 ? launch_chunks<true>(w, chunks, group, packed, scale, zero, s)
+               : launch_chunks<false>(w, chunks, group, packed, scale, zero, s);
+  }
   const int64_t warps = N * (K / group);
   const unsigned int blocks = static_cast<unsigned int>((warps + 7) / 8);
   if (f16)

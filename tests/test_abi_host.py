@@ -196,7 +196,9 @@ def test_embedding_validation(lib):
         return lib.w4_lm_head_gemv(a["h"], a["M"], a["table"], a["sc"], a["z"], a["V"], a["D"], a["group"],
                                    a["y"], None)
     assert head(D=264, group=-1) == w4.W4_ERR_UNSUPPORTED      # rows read 32 codes at a time
-    assert head(D=8192, group=128) == w4.W4_ERR_UNSUPPORTED    # 8 rows of h must fit in shared memory
+    assert head(D=8320, group=128) == w4.W4_ERR_UNSUPPORTED    # 8 rows of h must fit in shared memory
+    assert head(D=8192, group=128, M=0) == w4.W4_OK           # tensor-core form: fp16 h
+    assert head(D=8192, group=64, M=0) == w4.W4_ERR_UNSUPPORTED
     assert head(D=5792, group=32, M=0) == w4.W4_OK            # the longest row that fits
     assert head(D=5824, group=32, M=0) == w4.W4_ERR_UNSUPPORTED
     assert head(table=ODD) == w4.W4_ERR_ALIGN

@@ -64,6 +64,34 @@ def test_lm_head_shapes(V, D, g, M):
     check_bf16_output(bits(y), O.lm_head_logits(h, packed, sc, z, gg), f"lm_head V={V} D={D} g={g} M={M}")
 
 
+@pytest.mark.parametrize("V,D,g,M", [(37, 8192, 256, 9), (48, 1024, 512, 8), (17, 256, -1, 2)])
+def test_lm_head_tensor_core_shapes(V, D, g, M):
+    """The tensor-core form: a group spanning several 128-code segments, the
+    longest row it takes, two passes of tokens (9 = 8 + 1), a row as one
+    group, and whole vs. partial 16-row tiles."""
+    gg = D if g == -1 else g
+    packed, sc, z = _table(V, D, gg, seed=V * 3 + D)
+    h = S.activations_bf16(M, D, seed=V + 1)
+    y = w4.w4_lm_head_gemv(bf16(h), to_dev(packed), to_dev(sc), to_dev(z), g)
+    torch.cuda.synchronize()
+    check_bf16_output(bits(y), O.lm_head_logits(h, packed, sc, z, gg), f"lm_head tc V={V} D={D} g={g} M={M}")
+
+
+def test_lm_head_wide_range_h():
+    """h whose 128-code segments differ by up to 2^40 in magnitude (and one
+    all-zero segment): the per-segment power-of-two staging keeps every
+    segment exact."""
+    V, D, g, M = 300, 1024, 128, 3
+    packed, sc, z = _table(V, D, g, seed=77)
+    hf = S.bf16_bits_to_f32(S.activations_bf16(M, D, seed=78)).astype(np.float64).reshape(M, D // 128, 128)
+    hf *= 2.0 ** np.array([-20, 0, 20, 7, -13, 0, 3, -1])[None, :, None]
+    hf[1, 5] = 0.0
+    h = S.to_bf16_bits(hf.reshape(M, D).astype(np.float32))
+    y = w4.w4_lm_head_gemv(bf16(h), to_dev(packed), to_dev(sc), to_dev(z), g)
+    torch.cuda.synchronize()
+    check_bf16_output(bits(y), O.lm_head_logits(h, packed, sc, z, g), "lm_head wide-range h")
+
+
 def test_tied_table_full_size():
     """131072 x 2048 group 128: the head for one token, checked on every 7th
     vocabulary row, and a gather of 8 ids from the same tensors."""

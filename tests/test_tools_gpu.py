@@ -37,7 +37,7 @@ def _quant_and_check(wbits_or_half, N, K, group, fp16, label):
     return packed, scale, zero
 
 
-@pytest.mark.parametrize("group", [2, 32, 64, 128, 512, -1])
+@pytest.mark.parametrize("group", [2, 8, 16, 32, 64, 128, 256, 512, -1])
 def test_quantize_groupwise_bf16(group):
     N, K = 96, 512
     _quant_and_check(S.to_bf16_bits(_weights(N, K, seed=group % 7)), N, K, group, False, f"bf16 g={group}")
@@ -48,6 +48,13 @@ def test_quantize_groupwise_fp16_and_spread():
     w = _weights(N, K, seed=3, spread=True).astype(np.float16)
     _quant_and_check(w, N, K, 64, True, "fp16 spread")
     _quant_and_check(S.to_bf16_bits(_weights(N, K, seed=4, spread=True)), N, K, 32, False, "bf16 spread")
+
+
+@pytest.mark.parametrize("N,K,group", [(7, 200, 8), (5, 48, 16), (3, 776, 8), (9, 264, 24)])
+def test_quantize_groupwise_ragged(N, K, group):
+    """Chunk counts that leave the last block partly empty, and a group of 24
+    (not a power of two: one warp per group)."""
+    _quant_and_check(S.to_bf16_bits(_weights(N, K, seed=K)), N, K, group, False, f"ragged {N}x{K} g={group}")
 
 
 def test_quantize_groupwise_edges():
