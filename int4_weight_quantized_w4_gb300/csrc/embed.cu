@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(kHeadWarps * 32) lm_head_kernel(const uint16_t
   }
 }
 
-constexpr int kTcWarps = 8;
+constexpr int kTcWarps = 20;   // one CTA per SM (640 threads, up to 96 registers): h is staged once per SM
 constexpr int kTcAhead = 4;        // segments of loads in flight per warp
 constexpr int kSegBytes = 288;     // one (segment, token) block of staged h: 4 x 64 B + 32 B of padding
 
@@ -217,27 +217,28 @@ __global__ void __launch_bounds__(kTcWarps * 32) lm_head_tc_kernel(const uint16_
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
       sm += __shfl_xor_sync(0xffffffffu, sm, o);
     }
-    int ex = 0;
-    if (mx > 0.f) frexpf(mx, &ex);           // mx = m 2^ex, m in [0.5, 1)
-    const int e = mx > 0.f ? 15 - ex : 0;    // largest |h| 2^e in [2^14, 2^15)
-    // code c = 4 lane + i sits in chunk t = c / 32, word c' = (c % 32) / 8, slot j = c % 8
+    // 2^e with the largest |h| 2^e in [2^14, 2^15): from the exponent field
+    // of mx (mx in [2^(E-127), 2^(E-126))), clamped so that 2^e, 2^(e-4) and
+    // 2^-e are normal floats (every bf16 magnitude stays in range)
+    const int E = static_cast<int>(__float_as_uint(mx) >> 23);
+    const int e = mx > 0.f ? min(max(141 - E, -113), 121) : 0;
+    const float sc = __int_as_float((127 + e) << 23), sc16 = __int_as_float((123 + e) << 23);
+    // code c = 4 lane + i sits in quad position tt = c / 32, word c' = (c % 32) / 8, slot j = c % 8;
+    // slot j -> B register 4 c' + 2 h' + odd (h' = (j / 2) % 2, odd = j % 2), half j / 4
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int c = lane * 4 + i;
       const int tt = c >> 5, cw = (c & 31) >> 3, j = c & 7;
-      // j -> (half h', register r, element): j = 2h' + {0: r0 lo, 4: r0 hi, 1: r1 lo, 5: r1 hi}
       const int hp = (j >> 1) & 1, odd = j & 1, hi = j >> 2;
-      const int reg = cw * 4 + hp * 2 + odd;    // B register index 0..15 within (seg, tok, tt)
-      const float xv = ldexpf(v[i], odd ? e - 4 : e);
-      const __half hv = __float2half_rn(xv);
-      uint16_t* dst = reinterpret_cast<uint16_t*>(smem + stage_offset(seg, tok, tt)) + reg * 2 + hi;
-      *dst = __half_as_ushort(hv);
+      const __half hv = __float2half_rn(v[i] * (odd ? sc16 : sc));
+      reinterpret_cast<uint16_t*>(smem + stage_offset(seg, tok, tt))[(cw * 4 + hp * 2 + odd) * 2 + hi] =
+          __half_as_ushort(hv);
     }
-    if (lane < 1) {
+    if (lane == 0) {
       // fold data for the token pair (tok & ~1, tok | 1) lives at fold[seg * 4 + tok / 2]
       float* f = reinterpret_cast<float*>(&fold[seg * 4 + (tok >> 1)]);
-      f[tok & 1] = ldexpf(sm, -24);
-      f[2 + (tok & 1)] = ldexpf(1.f, -e);
+      f[tok & 1] = sm * 5.9604644775390625e-8f;            // 2^-24 sum h, exact scaling
+      f[2 + (tok & 1)] = __int_as_float((127 - e) << 23);  // 2^-e
     }
   }
   __syncthreads();
@@ -251,17 +252,31 @@ __global__ void __launch_bounds__(kTcWarps * 32) lm_head_tc_kernel(const uint16_
   const int64_t rowb = D / 2;
   const int G = D / group, spg = group / 128;   // segments per scale group
 
-  // load cursor
+  // load cursor: rows g and g + 8 of tile ltile (clamped into the table), at segment lseg
   int64_t ltile = wg;
   int lseg = 0;
+  const uint8_t* la;
+  const uint8_t* lb;
+  auto rows_of = [&](int64_t tile, int64_t& r0, int64_t& r1) {
+    r0 = tile * 16 + g;
+    r1 = r0 + 8;
+    r0 = r0 < V ? r0 : V - 1;
+    r1 = r1 < V ? r1 : V - 1;
+  };
+  auto set_load_tile = [&]() {
+    int64_t r0, r1;
+    rows_of(ltile, r0, r1);
+    la = table + r0 * rowb + t * 16;
+    lb = table + r1 * rowb + t * 16;
+  };
+  set_load_tile();
   auto load = [&](uint4& a, uint4& b) {
-    const int64_t r0 = ltile * 16 + g, r1 = r0 + 8;
-    const int64_t ra = r0 < V ? r0 : V - 1, rb = r1 < V ? r1 : V - 1;
-    a = ld_stream_v4(table + ra * rowb + lseg * 64 + t * 16);
-    b = ld_stream_v4(table + rb * rowb + lseg * 64 + t * 16);
+    a = ld_stream_v4(la + lseg * 64);
+    b = ld_stream_v4(lb + lseg * 64);
     if (++lseg == S) {
       lseg = 0;
       ltile += nw;
+      if (ltile < ntiles) set_load_tile();
     }
   };
   uint4 A[kTcAhead][2];
@@ -269,24 +284,39 @@ __global__ void __launch_bounds__(kTcWarps * 32) lm_head_tc_kernel(const uint16_
   for (int p = 0; p < kTcAhead; ++p)
     if (p < npos) load(A[p][0], A[p][1]);
 
+  // compute cursor: tile ctile at segment cseg, its rows' scale and zero rows
   int64_t ctile = wg;
-  int cseg = 0;
+  int cseg = 0, cgrp = 0, cin = 0;   // segment, its scale group, segments left in the group
+  const float* sa;
+  const float* sb;
+  const float* za;
+  const float* zb;
+  auto set_compute_tile = [&]() {
+    int64_t r0, r1;
+    rows_of(ctile, r0, r1);
+    sa = scale + r0 * G;
+    sb = scale + r1 * G;
+    za = zero + r0 * G;
+    zb = zero + r1 * G;
+  };
+  set_compute_tile();
+  const uint8_t* bbase = smem + stage_offset(0, g, t);
   float tot[4] = {0.f, 0.f, 0.f, 0.f};
-  float s0 = 0.f, z0 = 0.f, s1 = 0.f, z1 = 0.f;
+  float s0 = 0.f, s1 = 0.f, b0 = 0.f, b1 = 0.f;
   for (int64_t pos0 = 0; pos0 < npos; pos0 += kTcAhead) {
 #pragma unroll
     for (int p = 0; p < kTcAhead; ++p) {
       if (pos0 + p < npos) {
-        const int64_t r0 = ctile * 16 + g;
-        if (cseg % spg == 0) {                    // a new scale group for this tile's rows
-          const int64_t ra = r0 < V ? r0 : V - 1, rb = r0 + 8 < V ? r0 + 8 : V - 1;
-          const int grp = cseg / spg;
-          s0 = __ldg(scale + ra * G + grp);
-          z0 = __ldg(zero + ra * G + grp);
-          s1 = __ldg(scale + rb * G + grp);
-          z1 = __ldg(zero + rb * G + grp);
+        if (cin == 0) {                           // a new scale group for this tile's rows
+          s0 = __ldg(sa + cgrp);
+          s1 = __ldg(sb + cgrp);
+          b0 = fmaf(-8.f, s0, __ldg(za + cgrp));
+          b1 = fmaf(-8.f, s1, __ldg(zb + cgrp));
+          ++cgrp;
+          cin = spg;
         }
-        const uint4* bp = reinterpret_cast<const uint4*>(smem + stage_offset(cseg, g, t));
+        --cin;
+        const uint4* bp = reinterpret_cast<const uint4*>(bbase + cseg * (8 * kSegBytes));
         const uint4 B0 = bp[0], B1 = bp[1], B2 = bp[2], B3 = bp[3];
         const uint32_t b[16] = {B0.x, B0.y, B0.z, B0.w, B1.x, B1.y, B1.z, B1.w,
                                 B2.x, B2.y, B2.z, B2.w, B3.x, B3.y, B3.z, B3.w};
@@ -303,12 +333,12 @@ __global__ void __launch_bounds__(kTcWarps * 32) lm_head_tc_kernel(const uint16_
         }
         if (pos0 + p + kTcAhead < npos) load(A[p][0], A[p][1]);
         const float4 f = fold[cseg * 4 + t];
-        tot[0] = fmaf(s0 * f.z, acc[0], fmaf(fmaf(-8.f, s0, z0), f.x, tot[0]));
-        tot[1] = fmaf(s0 * f.w, acc[1], fmaf(fmaf(-8.f, s0, z0), f.y, tot[1]));
-        tot[2] = fmaf(s1 * f.z, acc[2], fmaf(fmaf(-8.f, s1, z1), f.x, tot[2]));
-        tot[3] = fmaf(s1 * f.w, acc[3], fmaf(fmaf(-8.f, s1, z1), f.y, tot[3]));
+        tot[0] = fmaf(s0 * f.z, acc[0], fmaf(b0, f.x, tot[0]));
+        tot[1] = fmaf(s0 * f.w, acc[1], fmaf(b0, f.y, tot[1]));
+        tot[2] = fmaf(s1 * f.z, acc[2], fmaf(b1, f.x, tot[2]));
+        tot[3] = fmaf(s1 * f.w, acc[3], fmaf(b1, f.y, tot[3]));
         if (++cseg == S) {                        // tile done: rows g, g + 8; tokens 2t, 2t + 1
-          const int64_t r1 = r0 + 8;
+          const int64_t r0 = ctile * 16 + g, r1 = r0 + 8;
           const int m0 = 2 * t, m1 = 2 * t + 1;
           if (r0 < V && m0 < Mact) y[m0 * V + r0] = static_cast<uint16_t>(f32_to_bf16_bits(tot[0] * 16777216.f));
           if (r0 < V && m1 < Mact) y[m1 * V + r0] = static_cast<uint16_t>(f32_to_bf16_bits(tot[1] * 16777216.f));
@@ -316,7 +346,10 @@ __global__ void __launch_bounds__(kTcWarps * 32) lm_head_tc_kernel(const uint16_
           if (r1 < V && m1 < Mact) y[m1 * V + r1] = static_cast<uint16_t>(f32_to_bf16_bits(tot[3] * 16777216.f));
           tot[0] = tot[1] = tot[2] = tot[3] = 0.f;
           cseg = 0;
+          cgrp = 0;
+          cin = 0;
           ctile += nw;
+          if (ctile < ntiles) set_compute_tile();
         }
       }
     }

@@ -67,6 +67,20 @@ __global__ void __launch_bounds__(256) quantize_groupwise_kernel(const uint16_t*
   }
 }
 
+// rint(fl(d / s)) for 0 <= d <= fl(max - min) and s = fl(max(fl(max - min),
+// 1e-9) / 15), without an IEEE divide on the common path. With r = fl(1/s)
+// and y = fl(d r), y = Q (1 + e1)(1 + e2) for Q = d / s and |e1|, |e2| <=
+// 2^-24, while fl(Q) = Q (1 + e3); Q < 15.001, so |y - fl(Q)| < 3.0001 * 2^-24
+// * 15.001 < 2^-18. When y is more than 2^-17 away from every half-integer,
+// fl(Q) lies strictly on the same side of each as y and rounds to the same
+// integer; otherwise the IEEE quotient decides.
+W4_DEV int quant_code(float d, float s, float r) {
+  const float y = __fmul_rn(d, r);
+  const float fy = floorf(y);
+  if (fabsf((y - fy) - 0.5f) > 7.62939453125e-6f) return __float2int_rn(y);
+  return __float2int_rn(__fdiv_rn(d, s));
+}
+
 // kC chunks of 8 elements per group (1..32, a power of two); chunk i of the
 // flat array belongs to group i / kC.
 template <bool kF16, int kC>
@@ -97,10 +111,11 @@ __global__ void __launch_bounds__(256) quantize_chunks_kernel(const uint4* __res
   }
   if (!live) return;
   const float s = __fdiv_rn(fmaxf(__fsub_rn(mx, mn), 1e-9f), 15.0f);
+  const float r = __frcp_rn(s);
   uint32_t word = 0;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    const int q = min(max(__float2int_rn(__fdiv_rn(__fsub_rn(v[j], mn), s)), 0), 15);
+    const int q = min(max(quant_code(__fsub_rn(v[j], mn), s, r), 0), 15);
     word |= static_cast<uint32_t>(q) << (4 * j);
   }
   packed[i] = word;

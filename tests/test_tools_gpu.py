@@ -57,6 +57,28 @@ def test_quantize_groupwise_ragged(N, K, group):
     _quant_and_check(S.to_bf16_bits(_weights(N, K, seed=K)), N, K, group, False, f"ragged {N}x{K} g={group}")
 
 
+def test_quantize_groupwise_ties():
+    """Quotients on and next to half-integers: groups with min 0 and max 15
+    (scale exactly 1) holding k + 0.5 (ties to even) and k + 0.5 +- 1/16, and
+    groups with max 1 (scale fl(1/15)) holding bf16 values next to
+    (k + 0.5) / 15, where the fast reciprocal product must hand over to the
+    IEEE quotient."""
+    N, K, g = 8, 256, 32
+    w = np.zeros((N, K), np.float32)
+    for n in range(N):
+        for j in range(K // g):
+            blk = np.zeros(g, np.float32)
+            blk[1] = 15.0 if n % 2 == 0 else 1.0
+            for i in range(2, g):
+                k = (i + j + n) % 15
+                if n % 2 == 0:
+                    blk[i] = k + 0.5 + ((i % 3) - 1) / 16.0
+                else:
+                    blk[i] = (k + 0.5) / 15.0
+            w[n, j * g:(j + 1) * g] = blk
+    _quant_and_check(S.to_bf16_bits(w), N, K, g, False, "ties")
+
+
 def test_quantize_groupwise_edges():
     _quant_and_check(S.to_bf16_bits(np.array([[0.5, -0.25]])), 1, 2, -1, False, "1x2")
     _quant_and_check(S.to_bf16_bits(np.zeros((3, 64))), 3, 64, 64, False, "all zeros")
