@@ -5,20 +5,23 @@
 // `group` consecutive input columns of w [N, K], scale = max(max - min, 1e-9)
 // / 15 and zero = min + 8 scale in fp32, codes q = clamp(round((w - min) /
 // scale), 0, 15) (round half to even), packed two per byte low nibble first
-// (pack_nibbles). The fp32 steps are taken one by one with IEEE rounding
-// (__fsub_rn, __fdiv_rn, rintf), so codes, scales and zeros are bit-exact.
+// (pack_nibbles). The fp32 steps are taken with IEEE rounding (__fsub_rn,
+// __fdiv_rn, rintf; the code of an element comes from a reciprocal product
+// wherever that provably rounds like the IEEE quotient, see quant_code), so
+// codes, scales and zeros are bit-exact.
 //
 // vLLM API docs, quantization.w4afp8, _repack_signed_int4_to_uint4b8:
 // signed int4 nibbles become uint4b8 (q + 8 mod 16) by XOR 0x88 on every byte.
 //
 // Both are bandwidth-bound load-time passes. Groups are contiguous in memory
-// (row n's group j starts at element n K + j group), so the quantizer walks
-// the weight as one flat array of 8-element chunks: for groups of 8 to 256
-// elements one thread takes one chunk (a 16-byte load, kept in registers),
-// the group's kC = group / 8 neighbouring lanes reduce its min and max with
-// shuffles, and every thread stores its 8 codes as one 32-bit word. Other
-// groups take one warp per (row, group), reading the group twice (the
-// second time from L1). The repack moves 16-byte vectors.
+// (row n's group j starts at element n K + j group), so for groups of 8 to
+// 256 elements the quantizer walks the weight as one flat array of 8-element
+// chunks (16-byte loads, kept in registers; two chunks per thread for groups
+// of 16 or more, so a group's scale and reciprocal serve 16 elements). The
+// group's neighbouring lanes reduce its min and max with shuffles and every
+// thread stores its codes as 32-bit words. Other groups take one warp per
+// (row, group), reading the group twice (the second time from L1). The
+// repack moves 16-byte vectors.
 #include "common.cuh"
 #include "launch.h"
 
@@ -71,57 +74,69 @@ __global__ void __launch_bounds__(256) quantize_groupwise_kernel(const uint16_t*
 // 1e-9) / 15), without an IEEE divide on the common path. With r = fl(1/s)
 // and y = fl(d r), y = Q (1 + e1)(1 + e2) for Q = d / s and |e1|, |e2| <=
 // 2^-24, while fl(Q) = Q (1 + e3); Q < 15.001, so |y - fl(Q)| < 3.0001 * 2^-24
-// * 15.001 < 2^-18. When y is more than 2^-17 away from every half-integer,
-// fl(Q) lies strictly on the same side of each as y and rounds to the same
-// integer; otherwise the IEEE quotient decides.
-W4_DEV int quant_code(float d, float s, float r) {
+// * 15.001 < 2^-18. When y is more than 2^-17 away from every half-integer
+// (|y - rint(y)| < 1/2 - 2^-17), fl(Q) lies strictly on the same side of each
+// as y and rounds to the same integer; otherwise the IEEE quotient decides.
+// The code is in [0, 15] either way (0 <= Q < 15.5), so no clamp is needed.
+W4_DEV uint32_t quant_code(float d, float s, float r) {
   const float y = __fmul_rn(d, r);
-  const float fy = floorf(y);
-  if (fabsf((y - fy) - 0.5f) > 7.62939453125e-6f) return __float2int_rn(y);
-  return __float2int_rn(__fdiv_rn(d, s));
+  const float qf = rintf(y);
+  if (fabsf(y - qf) < 0.49999237060546875f) return static_cast<uint32_t>(qf);
+  return static_cast<uint32_t>(__float2int_rn(__fdiv_rn(d, s)));
 }
 
-// kC chunks of 8 elements per group (1..32, a power of two); chunk i of the
-// flat array belongs to group i / kC.
-template <bool kF16, int kC>
-__global__ void __launch_bounds__(256) quantize_chunks_kernel(const uint4* __restrict__ w, int64_t chunks,
+// kC chunks of 8 elements per group (1..32, a power of two), kCPT of them
+// per thread (consecutive); thread i takes chunks kCPT i .. kCPT i + kCPT - 1,
+// all in group kCPT i / kC.
+template <bool kF16, int kC, int kCPT>
+__global__ void __launch_bounds__(256) quantize_chunks_kernel(const uint4* __restrict__ w, int64_t threads,
                                                               uint32_t* __restrict__ packed, float* __restrict__ scale,
                                                               float* __restrict__ zero) {
+  constexpr int kLanes = kC / kCPT;   // lanes per group
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const bool live = i < chunks;   // dead lanes still join the shuffles
-  float v[8];
-  if (live) {
-    const uint4 c = ld_stream_v4(w + i);
-    const uint32_t u[4] = {c.x, c.y, c.z, c.w};
+  const bool live = i < threads;   // dead lanes still join the shuffles
+  float v[kCPT][8];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      v[2 * j] = kF16 ? half_bits_to_f32(u[j] & 0xFFFFu) : bf16_lo(u[j]);
-      v[2 * j + 1] = kF16 ? half_bits_to_f32(u[j] >> 16) : bf16_hi(u[j]);
+  for (int c = 0; c < kCPT; ++c) {
+    if (live) {
+      const uint4 q = ld_stream_v4(w + i * kCPT + c);
+      const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        v[c][2 * j] = kF16 ? half_bits_to_f32(u[j] & 0xFFFFu) : bf16_lo(u[j]);
+        v[c][2 * j + 1] = kF16 ? half_bits_to_f32(u[j] >> 16) : bf16_hi(u[j]);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[c][j] = 0.f;
     }
-  } else {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = 0.f;
   }
-  float mn = fminf(fminf(fminf(v[0], v[1]), fminf(v[2], v[3])), fminf(fminf(v[4], v[5]), fminf(v[6], v[7])));
-  float mx = fmaxf(fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])), fmaxf(fmaxf(v[4], v[5]), fmaxf(v[6], v[7])));
+  float mn = v[0][0], mx = v[0][0];
 #pragma unroll
-  for (int o = kC / 2; o > 0; o >>= 1) {
+  for (int c = 0; c < kCPT; ++c)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      mn = fminf(mn, v[c][j]);
+      mx = fmaxf(mx, v[c][j]);
+    }
+#pragma unroll
+  for (int o = kLanes / 2; o > 0; o >>= 1) {
     mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   }
   if (!live) return;
   const float s = __fdiv_rn(fmaxf(__fsub_rn(mx, mn), 1e-9f), 15.0f);
   const float r = __frcp_rn(s);
-  uint32_t word = 0;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int q = min(max(quant_code(__fsub_rn(v[j], mn), s, r), 0), 15);
-    word |= static_cast<uint32_t>(q) << (4 * j);
+  for (int c = 0; c < kCPT; ++c) {
+    uint32_t word = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) word |= quant_code(__fsub_rn(v[c][j], mn), s, r) << (4 * j);
+    packed[i * kCPT + c] = word;
   }
-  packed[i] = word;
-  if ((i & (kC - 1)) == 0) {
-    scale[i / kC] = s;
-    zero[i / kC] = __fadd_rn(mn, __fmul_rn(8.0f, s));
+  if ((i & (kLanes - 1)) == 0) {
+    scale[i / kLanes] = s;
+    zero[i / kLanes] = __fadd_rn(mn, __fmul_rn(8.0f, s));
   }
 }
 
@@ -151,19 +166,25 @@ int sm_count_tools() {
 
 }  // namespace
 
+template <bool kF16, int kC, int kCPT>
+void launch_cpt(const uint4* wp, int64_t chunks, uint32_t* pp, float* scale, float* zero, cudaStream_t s) {
+  const int64_t threads = chunks / kCPT;
+  const unsigned int blocks = static_cast<unsigned int>((threads + 255) / 256);
+  quantize_chunks_kernel<kF16, kC, kCPT><<<blocks, 256, 0, s>>>(wp, threads, pp, scale, zero);
+}
+
 template <bool kF16>
 cudaError_t launch_chunks(const void* w, int64_t chunks, int32_t group, uint8_t* packed, float* scale, float* zero,
                           cudaStream_t s) {
-  const unsigned int blocks = static_cast<unsigned int>((chunks + 255) / 256);
   auto wp = static_cast<const uint4*>(w);
   auto pp = reinterpret_cast<uint32_t*>(packed);
-  switch (group / 8) {
-    case 1: quantize_chunks_kernel<kF16, 1><<<blocks, 256, 0, s>>>(wp, chunks, pp, scale, zero); break;
-    case 2: quantize_chunks_kernel<kF16, 2><<<blocks, 256, 0, s>>>(wp, chunks, pp, scale, zero); break;
-    case 4: quantize_chunks_kernel<kF16, 4><<<blocks, 256, 0, s>>>(wp, chunks, pp, scale, zero); break;
-    case 8: quantize_chunks_kernel<kF16, 8><<<blocks, 256, 0, s>>>(wp, chunks, pp, scale, zero); break;
-    case 16: quantize_chunks_kernel<kF16, 16><<<blocks, 256, 0, s>>>(wp, chunks, pp, scale, zero); break;
-    default: quantize_chunks_kernel<kF16, 32><<<blocks, 256, 0, s>>>(wp, chunks, pp, scale, zero); break;
+  switch (group / 8) {   // groups of 16 or more: two chunks per thread
+    case 1: launch_cpt<kF16, 1, 1>(wp, chunks, pp, scale, zero, s); break;
+    case 2: launch_cpt<kF16, 2, 2>(wp, chunks, pp, scale, zero, s); break;
+    case 4: launch_cpt<kF16, 4, 2>(wp, chunks, pp, scale, zero, s); break;
+    case 8: launch_cpt<kF16, 8, 2>(wp, chunks, pp, scale, zero, s); break;
+    case 16: launch_cpt<kF16, 16, 2>(wp, chunks, pp, scale, zero, s); break;
+    default: launch_cpt<kF16, 32, 2>(wp, chunks, pp, scale, zero, s); break;
   }
   return cudaGetLastError();
 }
