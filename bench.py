@@ -53,10 +53,25 @@ GRAPH_CALLS = 200
 # DRAM bytes (read + write) per launch from ncu, keyed by the SHA-256 of the
 # kernel's source file at capture time; reported only while the source matches.
 TRAFFIC = {
-    # w4a16_kernel, M=1 K=4096 N=14336 g128: dram__bytes_read.sum + dram__bytes_write.sum
-    # (30,337,280 + 0), profiles/w4a16_kernel_m1_k4096_n14336_full.md
-    "w4a16": (30337280, "c7e94205b1369c60"),
+    # w4a16_kernel, M=1 K=4096 N=14336 g128, caches flushed: dram__bytes_read.sum + dram__bytes_write.sum
+    # (30,329,600 + 0), profiles/w4a16_kernel_m1_k4096_n14336_full.md
+    "w4a16": (30329600, "87d141e4bb1a5321", "w4a16.cu"),
+    # lm_head_tc_kernel, M=1 V=131072 D=2048 g128 (151,030,272 + 3,162,368),
+    # profiles/lm_head_tc_kernel_v131072_d2048_full.md
+    "lm_head": (154192640, "5faab0d70541d2ee", "embed.cu"),
+    # quantize_chunks_kernel<bf16, 16, 2>, N=14336 K=4096 g128 (117,459,456 + 7,766,016; the codes,
+    # scales and zeros are still in L2 when the kernel ends), profiles/quantize_groupwise_n14336_k4096_full.md
+    "quantize": (125225472, "cf9a6143ae4772be", "tools.cu"),
 }
+
+
+def _traffic(key):
+    """ncu DRAM bytes per launch for `key` while its source is unchanged since the capture, else None."""
+    rec = TRAFFIC.get(key)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "int4_weight_quantized_w4_gb300", "csrc", rec[2])
+    return rec[0] if rec[1] == _sha(src) else None
 
 
 def _sha(path):
@@ -259,11 +274,7 @@ def run_ours(args, rank, world, local_rank):
     e2e_s = time.perf_counter() - t0
     e2e_value = world * e2e_steps * nbytes / e2e_s / 1e9
 
-    traffic = None
-    src = os.path.join(ROOT, "int4_weight_quantized_w4_gb300", "csrc", "w4a16.cu")
-    rec = TRAFFIC.get("w4a16")
-    if rec and rec[1] == _sha(src):
-        traffic = rec[0]
+    traffic = _traffic("w4a16")
 
     line = {
         "metric": METRIC,
@@ -477,8 +488,9 @@ def bench_rows(dev, stream, bf16_tf, peak_kind, hbm_peak, only=None):
             "config": {"N": Nq, "K": Kq, "group": gq, "w": "bf16"}, "value": round(qbytes / (t_q * 1e-3) / 1e9, 1),
             "unit": "GB/s", "ms_per_step": t_q,
             "roofline": {"bound": "hbm", "achieved": round(qbytes / (t_q * 1e-3) / 1e9, 1), "peak": hbm_peak,
-                         "unit": "GB/s", "frac": round(qbytes / (t_q * 1e-3) / 1e9 / hbm_peak, 4), "traffic": None,
-                         "kernel": "quantize_groupwise_kernel", "algorithmic_bytes_per_launch": qbytes},
+                         "unit": "GB/s", "frac": round(qbytes / (t_q * 1e-3) / 1e9 / hbm_peak, 4),
+                         "traffic": _traffic("quantize"),
+                         "kernel": "quantize_chunks_kernel", "algorithmic_bytes_per_launch": qbytes},
         }
     if want('lm_head_gemv'):
         # tied embedding table used as the decode output head: one token against a
@@ -507,8 +519,9 @@ def bench_rows(dev, stream, bf16_tf, peak_kind, hbm_peak, only=None):
             "config": {"M": 1, "V": V, "D": D, "group": gh, "scale_zero": "f32", "l2": "4 rotating tables (604 MB)"},
             "value": round(hbytes / (t_h * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": t_h,
             "roofline": {"bound": "hbm", "achieved": round(hbytes / (t_h * 1e-3) / 1e9, 1), "peak": hbm_peak,
-                         "unit": "GB/s", "frac": round(hbytes / (t_h * 1e-3) / 1e9 / hbm_peak, 4), "traffic": None,
-                         "kernel": "lm_head_kernel", "algorithmic_bytes_per_launch": hbytes},
+                         "unit": "GB/s", "frac": round(hbytes / (t_h * 1e-3) / 1e9 / hbm_peak, 4),
+                         "traffic": _traffic("lm_head"),
+                         "kernel": "lm_head_tc_kernel", "algorithmic_bytes_per_launch": hbytes},
         }
     if want('s4_repack_uint4b8'):
         # weight-side tool (load time): the XOR 0x88 repack of a 64-expert [E, N, K/2] int4 tensor
