@@ -404,6 +404,75 @@ def bench_rows(dev, stream, bf16_tf, peak_kind, hbm_peak, only=None):
     if want("w4a8_diffusion"):
         dense("w4a8_diffusion", 16384, 3072, 3072, -1, 0.0)
 
+    if want("w4a8_prefill_sweep"):
+        # the prefill sweep M x N at K = 4096, g128, 1% outlier channels; weight
+        # copies rotate so that every point's working set exceeds L2
+        K = 4096
+        xs_all = bf16(S.activations_bf16(4096, K, seed=0, outlier_frac=0.01))
+        points = {}
+        for N in (4096, 11008):
+            wbytes = K * N // 2 + (K // 128) * N * 2
+            copies = max(2, -(-256 * 2**20 // wbytes))
+            qws = [on(S.random_words((K // 8, N), seed=1, tag=20 + c)) for c in range(copies)]
+            sws = [on(S.scales_f16((K // 128, N), seed=2, tag=30 + c)) for c in range(copies)]
+            for M in (512, 1024, 2048, 4096):
+                x = xs_all[:M]
+                y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+                sx = torch.empty((M,), dtype=torch.float32, device=dev)
+                ws = torch.empty((w4.w4_workspace_bytes(w4.W4_OP_W4A8, M, N, K, 128),), dtype=torch.uint8,
+                                 device=dev)
+                it = [0]
+
+                def call(x=x, y=y, sx=sx, ws=ws, it=it, qws=qws, sws=sws):
+                    c = it[0] % len(qws)
+                    it[0] += 1
+                    w4.w4a8_gemm_bf16in(x, qws[c], sws[c], 128, y=y, x_scale=sx, workspace=ws, stream=stream)
+
+                t = _time_graph(torch, stream, call, copies, 3)
+                tops = 2.0 * M * N * K / (t * 1e-3) / 1e12
+                points[f"M{M}_N{N}"] = {"ms": round(t, 5), "tops": round(tops, 1), "frac": round(tops / bf16_tf, 4)}
+            del qws, sws
+        rows["w4a8_prefill_sweep"] = {
+            "config": {"M": [512, 1024, 2048, 4096], "N": [4096, 11008], "K": K, "group": 128,
+                       "outlier_channels": 0.01},
+            "unit": "TOPS", "step": "w4a8_gemm_bf16in", "points": points,
+            "peak": bf16_tf, "peak_source": f"{peak_kind} bf16_tflops",
+            "l2": "weight copies rotate: at least 256 MB of distinct weights per point",
+        }
+    if want("w4a16_sweep"):
+        # decode at M = 1, 4, 8: symmetric fp16 scales, symmetric bf16 scales, and
+        # the asymmetric variant with bf16 zeros; 16 rotating weight copies (> L2)
+        K, N, g = DEC_K, DEC_N, DEC_G
+        qws = [on(S.random_words((K // 8, N), seed=1, tag=20 + c)) for c in range(N_COPIES)]
+        sfs = [on(S.scales_f16((K // g, N), seed=2, tag=30 + c)) for c in range(N_COPIES)]
+        sbs = [bf16(S.to_bf16_bits(S.scales_f16((K // g, N), seed=2, tag=30 + c).astype(np.float32)))
+               for c in range(N_COPIES)]
+        zs = [bf16(S.to_bf16_bits(0.01 * S.normal(3, 40 + c, (K // g) * N).reshape(K // g, N)))
+              for c in range(N_COPIES)]
+        points = {}
+        for M in (1, 4, 8):
+            x = bf16(S.activations_bf16(M, K, seed=0))
+            y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            for variant in ("sym_fp16", "sym_bf16", "asym_fp16_zeros"):
+                sc = sbs if variant == "sym_bf16" else sfs
+                zz = zs if variant.startswith("asym") else None
+                it = [0]
+
+                def call(x=x, y=y, sc=sc, zz=zz, it=it):
+                    c = it[0] % N_COPIES
+                    it[0] += 1
+                    w4.w4a16_gemm(x, qws[c], sc[c], g, zeros=None if zz is None else zz[c], y=y, stream=stream)
+
+                t = _time_graph(torch, stream, call, 4 * N_COPIES, 20)
+                nbytes = K * N // 2 + (K // g) * N * 2 * (2 if zz is not None else 1) + M * K * 2 + M * N * 2
+                gbs = nbytes / (t * 1e-3) / 1e9
+                points[f"M{M}_{variant}"] = {"ms": round(t, 5), "gbs": round(gbs, 1), "frac": round(gbs / hbm_peak, 4)}
+        rows["w4a16_sweep"] = {
+            "config": {"M": [1, 4, 8], "K": K, "N": N, "group": g,
+                       "variants": ["sym_fp16", "sym_bf16", "asym_fp16_zeros"]},
+            "unit": "GB/s", "step": "w4a16_gemm (prefetch grid + GEMV grid)", "points": points,
+            "peak": hbm_peak, "l2": f"{N_COPIES} rotating weight copies",
+        }
     if want('w4afp8_moe'):
         # the routed MoE layer: 4096 tokens, hidden 2048, 64 experts, top-8,
         # intermediate 1408 (gate_up N = 2816, down K = 1408)
