@@ -91,7 +91,8 @@ size_t w4_workspace_bytes(int32_t op, int64_t M, int64_t N, int64_t K, int32_t g
  * symmetric, 8 bits) for int8; [FP8] W4AFP8Config.__init__ (input_quant: 8-bit
  * float, symmetric, per token, dynamic) for e4m3.
  *
- *   x      [M, K] bf16 (x_dtype must be W4_BF16)
+ *   x      [M, K] bf16 or fp16 (x_dtype W4_BF16 / W4_FP16; [INC] class
+ *          docstring: the activations may be bf16 or fp16)
  *   q      [M, K] int8 (q_dtype W4_INT8) or e4m3fn codes (q_dtype W4_FP8_E4M3)
  *   scale  [M] fp32
  * Per row: amax = max_k |x|; s = amax / Q in fp32 with Q = 127 (int8) or 448

@@ -21,7 +21,7 @@ __all__ = [
     "w4_embedding_gather", "w4_lm_head_gemv",
     "w4_moe_route", "w4_moe_gather_quant_fp8", "w4afp8_moe_gemm_bf16in", "w4_moe_silu_mul_quant_fp8",
     "w4_moe_combine",
-    "w4_device_status", "w4_selftest_bounded_wait",
+    "w4_device_status", "w4_selftest_bounded_wait", "apply_weights", "MIN_TOKENS_FOR_INT8",
     "W4_OK", "W4_ERR_NULL", "W4_ERR_ALIGN", "W4_ERR_GROUP", "W4_ERR_DTYPE",
     "W4_ERR_UNSUPPORTED", "W4_ERR_SHAPE", "W4_ERR_CUDA", "W4_ERR_TIMEOUT", "W4_ERR_WORKSPACE",
     "W4_OP_W4A8", "W4_OP_W4AFP8_MOE", "W4_OP_MOE_ROUTE", "w4_workspace_bytes", "EXPORTED_SYMBOLS",
@@ -128,9 +128,10 @@ def _workspace(ws, op, M, N, K, group, device):
 
 
 def w4_quant_act_per_token(x, q_dtype: str = "int8", q=None, scale=None, stream=None):
-    """Per-token symmetric quantization of bf16 ``x [M, K]``; returns ``(q, scale)``
-    with q int8 (``q_dtype="int8"``) or float8_e4m3fn (``"fp8"``) and fp32 scales."""
-    _cuda2d(x, "x", (torch.bfloat16,))
+    """Per-token symmetric quantization of bf16 or fp16 ``x [M, K]``; returns
+    ``(q, scale)`` with q int8 (``q_dtype="int8"``) or float8_e4m3fn (``"fp8"``)
+    and fp32 scales."""
+    _cuda2d(x, "x", (torch.bfloat16, torch.float16))
     M, K = x.shape
     if q_dtype == "int8":
         qd, tdt = W4_INT8, torch.int8
@@ -142,7 +143,8 @@ def w4_quant_act_per_token(x, q_dtype: str = "int8", q=None, scale=None, stream=
     scale = torch.empty((M,), dtype=torch.float32, device=x.device) if scale is None else scale
     if q.shape != (M, K) or scale.shape != (M,):
         raise ValueError("output shapes do not match x")
-    _check(load().w4_quant_act_per_token(_ptr(x), W4_BF16, M, K, qd, _ptr(q), _ptr(scale),
+    xd = W4_FP16 if x.dtype == torch.float16 else W4_BF16
+    _check(load().w4_quant_act_per_token(_ptr(x), xd, M, K, qd, _ptr(q), _ptr(scale),
                                          _stream(stream, x.device)), "w4_quant_act_per_token")
     return q, scale
 
@@ -391,6 +393,40 @@ def w4_lm_head_gemv(h, table, scale, zero, group: int, y=None, stream=None):
     _check(load().w4_lm_head_gemv(_ptr(h), M, _ptr(table), _ptr(scale), _ptr(zero), V, D, group, _ptr(y),
                                   _stream(stream, h.device)), "w4_lm_head_gemv")
     return y
+
+
+# [INC] INCXPUW4A8LinearMethod._MIN_TOKENS_FOR_INT8: below this token count the
+# per-token quantization does not pay off and the call takes the W4A16 path.
+MIN_TOKENS_FOR_INT8 = 512
+
+
+def apply_weights(x, qweight, w_scale, group: int, bias=None, zeros=None, stream=None):
+    """The int4 linear layer with the per-call path choice of [INC]
+    ``INCXPUW4A8LinearMethod.apply_weights``: ``x [..., K]`` (bf16 or fp16)
+    times GPTQ ``qweight [K/8, N]``; returns bf16 ``[..., N]``.
+
+    From ``MIN_TOKENS_FOR_INT8`` tokens up, activations are quantized per token
+    to int8 and the W4A8 GEMM runs (fp16 scales, no zeros); below it, the
+    W4A16 GEMM runs on the bf16 activations. fp16 activations always take the
+    int8 path (the W4A16 kernels read bf16), so they need fp16 scales and no
+    zeros.
+    """
+    K = x.shape[-1]
+    x2 = x.reshape(-1, K)
+    M = x2.shape[0]
+    int8_path = x2.dtype == torch.float16 or (M >= MIN_TOKENS_FOR_INT8 and zeros is None
+                                              and w_scale.dtype == torch.float16)
+    if int8_path:
+        if zeros is not None:
+            raise ValueError("the W4A8 path has no zeros; asymmetric weights need bf16 activations")
+        if x2.dtype == torch.bfloat16:
+            y, _ = w4a8_gemm_bf16in(x2, qweight, w_scale, group, bias=bias, stream=stream)
+        else:
+            q, sx = w4_quant_act_per_token(x2, "int8", stream=stream)
+            y = w4a8_gemm(q, sx, qweight, w_scale, group, bias=bias, stream=stream)
+    else:
+        y = w4a16_gemm(x2, qweight, w_scale, group, zeros=zeros, bias=bias, stream=stream)
+    return y.reshape(*x.shape[:-1], y.shape[-1])
 
 
 def w4_device_status(stream=None, device=None) -> int:

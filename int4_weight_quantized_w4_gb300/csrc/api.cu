@@ -104,7 +104,7 @@ const char* w4_status_string(int32_t st) {
 w4_status w4_quant_act_per_token(const void* x, int32_t x_dtype, int64_t M, int64_t K, int32_t q_dtype,
                                  void* q, float* scale, void* stream) {
   if (M < 0 || K <= 0) return fail(W4_ERR_SHAPE, "sizes must be M >= 0, K > 0 (M=%lld K=%lld)", (long long)M, (long long)K);
-  if (x_dtype != W4_BF16) return fail(W4_ERR_DTYPE, "x_dtype must be W4_BF16");
+  if (x_dtype != W4_BF16 && x_dtype != W4_FP16) return fail(W4_ERR_DTYPE, "x_dtype must be W4_BF16 or W4_FP16");
   if (q_dtype != W4_INT8 && q_dtype != W4_FP8_E4M3) return fail(W4_ERR_DTYPE, "q_dtype must be W4_INT8 or W4_FP8_E4M3");
   if (K % 8 != 0) return fail(W4_ERR_ALIGN, "K must be a multiple of 8, got %lld", (long long)K);
   if (M == 0) return ok();
@@ -112,7 +112,7 @@ w4_status w4_quant_act_per_token(const void* x, int32_t x_dtype, int64_t M, int6
   if (!aligned(x, 16) || !aligned(q, 16) || !aligned(scale, 4))
     return fail(W4_ERR_ALIGN, "x and q must be 16-byte aligned, scale 4-byte aligned");
   if (M > INT32_MAX) return fail(W4_ERR_UNSUPPORTED, "M too large");
-  return from_cuda(w4::launch_quant_per_token(x, M, K, q_dtype == W4_FP8_E4M3, q, scale,
+  return from_cuda(w4::launch_quant_per_token(x, x_dtype == W4_FP16, M, K, q_dtype == W4_FP8_E4M3, q, scale,
                                               static_cast<cudaStream_t>(stream)),
                    "w4_quant_act_per_token launch");
 }

@@ -13,7 +13,7 @@ namespace w4 {
 // Polls a bounded wait makes before it gives up (about a second of spinning).
 constexpr long long kWaitLimit = 1LL << 24;
 
-cudaError_t launch_quant_per_token(const void* x, int64_t M, int64_t K, bool fp8, void* q,
+cudaError_t launch_quant_per_token(const void* x, bool x_f16, int64_t M, int64_t K, bool fp8, void* q,
                                    float* scale, cudaStream_t s);
 
 struct W4A16Args {

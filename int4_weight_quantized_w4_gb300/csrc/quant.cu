@@ -5,6 +5,7 @@
 // W4A8 GEMM. vLLM API docs, quantization.w4afp8, W4AFP8Config.__init__: the
 // expert activations are 8-bit float, symmetric, per token, dynamic.
 //
+// The activations may be bf16 or fp16 (the INC class docstring allows both).
 // Per row: amax = max |x|; s = amax / Q (IEEE fp32 divide; s = 1 if amax = 0);
 // int8: q = clamp(rne(x / s), -127, 127); e4m3: q = satfinite-rne(x / s).
 //
@@ -37,11 +38,22 @@ W4_DEV float row_max(float v, float* red) {
   return m;
 }
 
+// The two 16-bit activations of a word as fp32 (exact): bf16, or fp16 (kF16).
+template <bool kF16>
+W4_DEV float act_lo(uint32_t w) {
+  return kF16 ? half_bits_to_f32(w & 0xFFFFu) : bf16_lo(w);
+}
+template <bool kF16>
+W4_DEV float act_hi(uint32_t w) {
+  return kF16 ? half_bits_to_f32(w >> 16) : bf16_hi(w);
+}
+
+template <bool kF16>
 W4_DEV float chunk_absmax(const uint4& v) {
-  float m = fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x)));
-  m = fmaxf(m, fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y))));
-  m = fmaxf(m, fmaxf(fabsf(bf16_lo(v.z)), fabsf(bf16_hi(v.z))));
-  m = fmaxf(m, fmaxf(fabsf(bf16_lo(v.w)), fabsf(bf16_hi(v.w))));
+  float m = fmaxf(fabsf(act_lo<kF16>(v.x)), fabsf(act_hi<kF16>(v.x)));
+  m = fmaxf(m, fmaxf(fabsf(act_lo<kF16>(v.y)), fabsf(act_hi<kF16>(v.y))));
+  m = fmaxf(m, fmaxf(fabsf(act_lo<kF16>(v.z)), fabsf(act_hi<kF16>(v.z))));
+  m = fmaxf(m, fmaxf(fabsf(act_lo<kF16>(v.w)), fabsf(act_hi<kF16>(v.w))));
   return m;
 }
 
@@ -51,37 +63,39 @@ W4_DEV uint32_t q_int8(float x, float s) {
   return static_cast<uint32_t>(q) & 0xFFu;
 }
 
-// Two int8 codes from one bf16x2 word, low element in the low byte.
+// Two int8 codes from one word of two activations, low element in the low byte.
+template <bool kF16>
 W4_DEV uint32_t q_int8_pair(uint32_t w, float s) {
-  return q_int8(bf16_lo(w), s) | (q_int8(bf16_hi(w), s) << 8);
+  return q_int8(act_lo<kF16>(w), s) | (q_int8(act_hi<kF16>(w), s) << 8);
 }
 
-// Two e4m3 codes from one bf16x2 word, low element in the low byte.
+// Two e4m3 codes from one word of two activations, low element in the low byte.
+template <bool kF16>
 W4_DEV uint32_t q_e4m3_pair(uint32_t w, float s) {
-  const float lo = __fdiv_rn(bf16_lo(w), s), hi = __fdiv_rn(bf16_hi(w), s);
+  const float lo = __fdiv_rn(act_lo<kF16>(w), s), hi = __fdiv_rn(act_hi<kF16>(w), s);
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
 }
 
-template <bool FP8>
+template <bool FP8, bool kF16>
 W4_DEV uint2 quant_chunk(const uint4& v, float s) {
   uint2 o;
   if (FP8) {
-    o.x = q_e4m3_pair(v.x, s) | (q_e4m3_pair(v.y, s) << 16);
-    o.y = q_e4m3_pair(v.z, s) | (q_e4m3_pair(v.w, s) << 16);
+    o.x = q_e4m3_pair<kF16>(v.x, s) | (q_e4m3_pair<kF16>(v.y, s) << 16);
+    o.y = q_e4m3_pair<kF16>(v.z, s) | (q_e4m3_pair<kF16>(v.w, s) << 16);
   } else {
-    o.x = q_int8_pair(v.x, s) | (q_int8_pair(v.y, s) << 16);
-    o.y = q_int8_pair(v.z, s) | (q_int8_pair(v.w, s) << 16);
+    o.x = q_int8_pair<kF16>(v.x, s) | (q_int8_pair<kF16>(v.y, s) << 16);
+    o.y = q_int8_pair<kF16>(v.z, s) | (q_int8_pair<kF16>(v.w, s) << 16);
   }
   return o;
 }
 
 // The codes of one 8-chunk as stored: 8 bytes, or (kWiden) the exact fp16
 // values of the codes in the W4A8 operand order (16 bytes).
-template <bool FP8, bool kWiden>
+template <bool FP8, bool kWiden, bool kF16>
 W4_DEV void store_chunk(void* q, size_t i, const uint4& v, float s) {
-  const uint2 c = quant_chunk<FP8>(v, s);
+  const uint2 c = quant_chunk<FP8, kF16>(v, s);
   if (kWiden)
     static_cast<uint4*>(q)[i] = FP8 ? widen_e4m3(c.x, c.y) : widen_i8(c.x, c.y);
   else
@@ -92,7 +106,7 @@ W4_DEV void store_chunk(void* q, size_t i, const uint4& v, float s) {
 // NCH == 0: long rows, read twice (the second read mostly hits L2).
 // gather (may be null): source row of each output row, checked against T; an
 // id outside [0, T) gives a zero row with scale 1 and W4_ERR_SHAPE in status.
-template <int NCH, bool FP8, bool kWiden>
+template <int NCH, bool FP8, bool kWiden, bool kF16>
 __global__ void __launch_bounds__(kMaxThreads) quant_rows(const uint4* __restrict__ x, int K8,
                                                           void* __restrict__ q, float* __restrict__ scale,
                                                           const int32_t* __restrict__ gather, int64_t T,
@@ -127,27 +141,28 @@ __global__ void __launch_bounds__(kMaxThreads) quant_rows(const uint4* __restric
     for (int c = 0; c < NCH; ++c) {
       const int i = threadIdx.x + c * blockDim.x;
       v[c] = (i < K8) ? ld_stream_v4(xr + i) : make_uint4(0, 0, 0, 0);
-      m = fmaxf(m, chunk_absmax(v[c]));
+      m = fmaxf(m, chunk_absmax<kF16>(v[c]));
     }
     const float amax = row_max(m, red);
     const float s = (amax == 0.f) ? 1.f : __fdiv_rn(amax, kQ);
 #pragma unroll
     for (int c = 0; c < NCH; ++c) {
       const int i = threadIdx.x + c * blockDim.x;
-      if (i < K8) store_chunk<FP8, kWiden>(q, q0 + i, v[c], s);
+      if (i < K8) store_chunk<FP8, kWiden, kF16>(q, q0 + i, v[c], s);
     }
     if (threadIdx.x == 0) scale[row] = s;
   } else {
     float m = 0.f;
-    for (int i = threadIdx.x; i < K8; i += blockDim.x) m = fmaxf(m, chunk_absmax(ld_nc_v4(xr + i)));
+    for (int i = threadIdx.x; i < K8; i += blockDim.x) m = fmaxf(m, chunk_absmax<kF16>(ld_nc_v4(xr + i)));
     const float amax = row_max(m, red);
     const float s = (amax == 0.f) ? 1.f : __fdiv_rn(amax, kQ);
-    for (int i = threadIdx.x; i < K8; i += blockDim.x) store_chunk<FP8, kWiden>(q, q0 + i, ld_stream_v4(xr + i), s);
+    for (int i = threadIdx.x; i < K8; i += blockDim.x)
+      store_chunk<FP8, kWiden, kF16>(q, q0 + i, ld_stream_v4(xr + i), s);
     if (threadIdx.x == 0) scale[row] = s;
   }
 }
 
-template <bool FP8, bool kWiden>
+template <bool FP8, bool kWiden, bool kF16 = false>
 cudaError_t launch(const void* x, int64_t M, int64_t K, void* q, float* scale, cudaStream_t s,
                    const int32_t* gather = nullptr, int64_t T = 0, unsigned int* status = nullptr) {
   const int K8 = static_cast<int>(K / 8);
@@ -157,20 +172,22 @@ cudaError_t launch(const void* x, int64_t M, int64_t K, void* q, float* scale, c
   const dim3 grid(static_cast<unsigned>(M));
   auto xp = static_cast<const uint4*>(x);
   switch (nch) {
-    case 1: quant_rows<1, FP8, kWiden><<<grid, threads, 0, s>>>(xp, K8, q, scale, gather, T, status); break;
-    case 2: quant_rows<2, FP8, kWiden><<<grid, threads, 0, s>>>(xp, K8, q, scale, gather, T, status); break;
-    case 3: quant_rows<3, FP8, kWiden><<<grid, threads, 0, s>>>(xp, K8, q, scale, gather, T, status); break;
-    case 4: quant_rows<4, FP8, kWiden><<<grid, threads, 0, s>>>(xp, K8, q, scale, gather, T, status); break;
-    default: quant_rows<0, FP8, kWiden><<<grid, threads, 0, s>>>(xp, K8, q, scale, gather, T, status); break;
+    case 1: quant_rows<1, FP8, kWiden, kF16><<<grid, threads, 0, s>>>(xp, K8, q, scale, gather, T, status); break;
+    case 2: quant_rows<2, FP8, kWiden, kF16><<<grid, threads, 0, s>>>(xp, K8, q, scale, gather, T, status); break;
+    case 3: quant_rows<3, FP8, kWiden, kF16><<<grid, threads, 0, s>>>(xp, K8, q, scale, gather, T, status); break;
+    case 4: quant_rows<4, FP8, kWiden, kF16><<<grid, threads, 0, s>>>(xp, K8, q, scale, gather, T, status); break;
+    default: quant_rows<0, FP8, kWiden, kF16><<<grid, threads, 0, s>>>(xp, K8, q, scale, gather, T, status); break;
   }
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_quant_per_token(const void* x, int64_t M, int64_t K, bool fp8, void* q, float* scale,
+cudaError_t launch_quant_per_token(const void* x, bool x_f16, int64_t M, int64_t K, bool fp8, void* q, float* scale,
                                    cudaStream_t s) {
   if (K / 8 > INT32_MAX) return cudaErrorInvalidValue;
+  if (x_f16)
+    return fp8 ? launch<true, false, true>(x, M, K, q, scale, s) : launch<false, false, true>(x, M, K, q, scale, s);
   return fp8 ? launch<true, false>(x, M, K, q, scale, s) : launch<false, false>(x, M, K, q, scale, s);
 }
 

@@ -198,15 +198,26 @@ def repack_signed_int4_to_uint4b8(packed_s4: np.ndarray) -> np.ndarray:
 # per-token activation quantization
 # ---------------------------------------------------------------------------
 
+def _activations_f32(x) -> np.ndarray:
+    """Activations as float32 (exact): bf16 bit patterns (uint16), or fp16
+    values (float16; [INC] class docstring: the activations may be bf16 or
+    fp16)."""
+    x = np.asarray(x)
+    if x.dtype == np.float16:
+        return x.astype(np.float32)
+    return bf16_bits_to_f32(x)
+
+
 def quant_int8_per_token(x_bits: np.ndarray):
     """Dynamic per-token symmetric int8 ([INC] class docstring and
     ``apply_weights``: ``dynamic_per_token_int8_quant_ref(x, True, 8)``).
 
     Returns ``(q int8 [M,K], s float32 [M])`` with, per row,
     ``s = fp32(amax / 127)`` (1 if amax is 0) and
-    ``q = clamp(rne(fp32(x / s)), -127, 127)``.
+    ``q = clamp(rne(fp32(x / s)), -127, 127)``. ``x_bits``: bf16 bit
+    patterns, or a float16 array for fp16 activations.
     """
-    x = bf16_bits_to_f32(x_bits)
+    x = _activations_f32(x_bits)
     amax = np.max(np.abs(x), axis=1) if x.shape[1] else np.zeros(x.shape[0], np.float32)
     s = (amax / np.float32(127.0)).astype(np.float32)
     s = np.where(amax == 0, np.float32(1.0), s).astype(np.float32)
@@ -221,8 +232,9 @@ def quant_fp8_per_token(x_bits: np.ndarray):
 
     Returns ``(q uint8 e4m3fn codes [M,K], s float32 [M])``:
     ``s = fp32(amax / 448)`` (1 if amax is 0), ``q = e4m3(fp32(x / s))``.
+    ``x_bits``: bf16 bit patterns, or a float16 array for fp16 activations.
     """
-    x = bf16_bits_to_f32(x_bits)
+    x = _activations_f32(x_bits)
     amax = np.max(np.abs(x), axis=1) if x.shape[1] else np.zeros(x.shape[0], np.float32)
     s = (amax / np.float32(448.0)).astype(np.float32)
     s = np.where(amax == 0, np.float32(1.0), s).astype(np.float32)

@@ -110,7 +110,8 @@ def test_quant_validation(lib):
         a = dict(x=FAKE, xdt=w4.W4_BF16, M=4, K=256, qdt=w4.W4_INT8, q=FAKE, s=FAKE)
         a.update(kw)
         return lib.w4_quant_act_per_token(a["x"], a["xdt"], a["M"], a["K"], a["qdt"], a["q"], a["s"], None)
-    assert call(xdt=w4.W4_FP16) == w4.W4_ERR_DTYPE
+    assert call(xdt=w4.W4_INT8) == w4.W4_ERR_DTYPE
+    assert call(xdt=w4.W4_FP16, M=0) == w4.W4_OK               # fp16 activations are accepted
     assert call(qdt=w4.W4_BF16) == w4.W4_ERR_DTYPE
     assert call(K=12) == w4.W4_ERR_ALIGN
     assert call(K=0) == w4.W4_ERR_SHAPE

@@ -226,6 +226,26 @@ def test_quant_fp8_invariants():
     assert np.all(np.abs(dq - xf)[big] <= np.abs(xf)[big] * 2.0 ** -4 * (1 + 1e-6))
 
 
+def test_quant_fp16_activations():
+    """fp16 activations ([INC] class docstring: bf16 or fp16): values that both
+    formats hold exactly quantize identically either way; the fp16 extremes
+    (65504, the smallest subnormal) quantize by the same rules, 65504 giving
+    the row's +-127 / +-448 codes."""
+    vals = np.array([[0.5, -3.25, 7.0, 0.0, 1.5, -0.125, 2.0, 96.0]], np.float32)
+    for fn in (O.quant_int8_per_token, O.quant_fp8_per_token):
+        qa, sa = fn(S.to_bf16_bits(vals))
+        qb, sb = fn(vals.astype(np.float16))
+        np.testing.assert_array_equal(qa, qb)
+        np.testing.assert_array_equal(sa, sb)
+    x = np.array([[65504.0, -65504.0, 2.0 ** -24, 1.0, 0, 0, 0, 0]], np.float16)
+    q, s = O.quant_int8_per_token(x)
+    assert s[0] == np.float32(65504.0) / np.float32(127.0)
+    np.testing.assert_array_equal(q[0, :4], [127, -127, 0, 0])
+    q8, s8 = O.quant_fp8_per_token(x)
+    assert s8[0] == np.float32(65504.0) / np.float32(448.0)
+    assert O.e4m3_decode(q8[:, :2]).tolist() == [[448.0, -448.0]]
+
+
 # ---------------------------------------------------------------------------
 # W4A8 layer
 # ---------------------------------------------------------------------------

@@ -64,3 +64,25 @@ def test_quant_moe_rows_full_size():
 def test_quant_empty():
     q, s = w4.w4_quant_act_per_token(torch.empty((0, 64), dtype=torch.bfloat16, device="cuda"), "int8")
     assert q.shape == (0, 64) and s.shape == (0,)
+
+
+def _check_f16(xh, kind):
+    q, s = w4.w4_quant_act_per_token(torch.from_numpy(xh).cuda(), kind)
+    torch.cuda.synchronize()
+    q = q.cpu()
+    q = q.view(torch.uint8).numpy() if kind == "fp8" else q.numpy()
+    qr, sr = (O.quant_fp8_per_token if kind == "fp8" else O.quant_int8_per_token)(xh)
+    np.testing.assert_array_equal(s.cpu().numpy().view(np.uint32), sr.view(np.uint32))
+    np.testing.assert_array_equal(q, qr)
+
+
+@pytest.mark.parametrize("kind", ["int8", "fp8"])
+@pytest.mark.parametrize("M,K", [(3, 256), (33, 2048), (5, 4096), (9, 8200)])
+def test_quant_fp16_activations(kind, M, K):
+    """fp16 activations ([INC] class docstring: bf16 or fp16), with the fp16
+    extremes in one row: 65504, subnormals, and zeros."""
+    x = S.bf16_bits_to_f32(S.activations_bf16(M, K, seed=M + K, outlier_frac=0.01)).astype(np.float16)
+    x[0, :4] = [65504.0, -65504.0, 2.0 ** -24, -(2.0 ** -20)]
+    if M > 1:
+        x[1] = 0
+    _check_f16(x, kind)
