@@ -84,7 +84,6 @@ struct Params {
   void* out;               // bf16 [rows, N] or int32 [rows, G, N]
   const int32_t* offsets;  // [E + 1] (experts)
   int E, M, N, K, group, mode;
-  int cl;                  // CTAs per cluster along N; they share each activation tile
   int raw_rows;            // word rows (k / 8) per packed-word copy: min(RAW_PER * BK / 8, K / 8)
   unsigned int* status;
 };
@@ -106,33 +105,49 @@ W4_DEV uint4 nibbles_to_f16(uint32_t w) {
 
 W4_DEV void bar_sync_epilogue() { asm volatile("bar.sync 1, %0;" :: "n"(kEpiWarps * 32) : "memory"); }
 
-__global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_constant__ Params p) {
-  extern __shared__ uint8_t smem_dyn[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
-
-  // ---- which tile ----
-  const int n0 = blockIdx.x * BM;
-  int row0 = 0, row_end = 0, expert = 0;
+// Output tile `tid` of the grid of tiles (N tiles fastest): outputs n0 .. n0 +
+// BM, rows row0 .. row_end (of one expert's segment in expert mode). False if
+// the tile holds no rows. Every role decodes the same tiles the same way.
+struct Tile {
+  int n0, row0, row_end, expert;
+};
+W4_DEV bool decode_tile(const Params& p, int tid, int n_tiles, Tile& t) {
+  const int nx = tid % n_tiles;
+  int yt = tid / n_tiles;
+  t.n0 = nx * BM;
+  t.expert = 0;
+  t.row0 = 0;
+  t.row_end = 0;
   if (p.mode == kExperts) {
-    int t = blockIdx.y;
     for (int e = 0; e < p.E; ++e) {
       const int a = p.offsets[e], b = p.offsets[e + 1];
       const int nt = b > a ? (b - a + BN - 1) / BN : 0;
-      if (t < nt) {
-        expert = e;
-        row0 = a + t * BN;
-        row_end = min(row0 + BN, b);
+      if (yt < nt) {
+        t.expert = e;
+        t.row0 = a + yt * BN;
+        t.row_end = min(t.row0 + BN, b);
         break;
       }
-      t -= nt;
+      yt -= nt;
     }
-    row0 = max(row0, 0);
-    row_end = min(row_end, p.M);
+    t.row0 = max(t.row0, 0);
+    t.row_end = min(t.row_end, p.M);
   } else {
-    row0 = blockIdx.y * BN;
-    row_end = min(row0 + BN, p.M);
+    t.row0 = yt * BN;
+    t.row_end = min(t.row0 + BN, p.M);
   }
-  if (row0 >= row_end) return;  // no tile for this CTA (uniform across the CTA)
+  return t.row0 < t.row_end;
+}
+
+// Persistent: one CTA per SM takes tiles blockIdx.x, blockIdx.x + gridDim.x,
+// ... of the n_tiles x y_tiles grid. Every ring (packed words, operand A,
+// operand B, the two TMEM accumulators) keeps counting across tiles, so the
+// copies and conversions of the next tile run while this tile's last groups
+// are multiplied and its output is written.
+__global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_constant__ Params p, int n_tiles,
+                                                              int y_tiles) {
+  extern __shared__ uint8_t smem_dyn[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
 
   uint8_t* b_base = smem;                                  // 1024-aligned
   uint8_t* a_base = b_base + B_STAGES * B_BYTES;           // 1024-aligned
@@ -162,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
     }
     for (int i = 0; i < B_STAGES; ++i) {
       mbar_init(&b_full[i], 1);
-      mbar_init(&b_empty[i], p.cl);   // every CTA of the cluster must be done with the slot
+      mbar_init(&b_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
@@ -180,14 +195,12 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_holder;
-  // peers multicast into this CTA's shared memory: their barriers must be live
-  const uint32_t crank = p.cl > 1 ? tc::cluster_ctarank() : 0;
-  const uint16_t cmask = static_cast<uint16_t>((1u << p.cl) - 1u);
-  if (p.cl > 1) tc::cluster_sync();
 
   const int K = p.K;
   const int nst = (K + BK - 1) / BK;
+  const int nraw = (nst + RAW_PER - 1) / RAW_PER;
   const int group = p.group;
+  const int total_tiles = n_tiles * y_tiles;
 
   if (warp >= kEpiWarps) {
   // producer warpgroups give registers to the epilogue warpgroups
@@ -195,130 +208,151 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
   if (warp == kWarpLoadW) {
     // ---- raw packed weight words -> ring ----
     if (lane == 0) {
-      const int nraw = (nst + RAW_PER - 1) / RAW_PER;
-      for (int ri = 0; ri < nraw; ++ri) {
-        const int r = ri % RAW_STAGES;
-        if (!tc::wait(&raw_empty[r], ((ri / RAW_STAGES) & 1) ^ 1, abort_flag, p.status, kWaitNs)) break;
-        mbar_arrive_expect_tx(&raw_full[r], static_cast<uint32_t>(p.raw_rows * BM * 4));
-        if (p.mode == kExperts)
-          tc::tma_load_3d(raw_base + r * RAW_BYTES, &p.tm_w, &raw_full[r], ri * RAW_PER * (BK / 8), n0, expert);
-        else
-          tc::tma_load_2d(raw_base + r * RAW_BYTES, &p.tm_w, &raw_full[r], n0, ri * RAW_PER * (BK / 8));
+      int rg = 0;   // copies issued so far (all tiles)
+      bool ok = true;
+      for (int tid = blockIdx.x; tid < total_tiles && ok; tid += gridDim.x) {
+        Tile t;
+        if (!decode_tile(p, tid, n_tiles, t)) continue;
+        for (int ri = 0; ri < nraw; ++ri, ++rg) {
+          const int r = rg % RAW_STAGES;
+          if (!tc::wait(&raw_empty[r], ((rg / RAW_STAGES) & 1) ^ 1, abort_flag, p.status, kWaitNs)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&raw_full[r], static_cast<uint32_t>(p.raw_rows * BM * 4));
+          if (p.mode == kExperts)
+            tc::tma_load_3d(raw_base + r * RAW_BYTES, &p.tm_w, &raw_full[r], ri * RAW_PER * (BK / 8), t.n0,
+                            t.expert);
+          else
+            tc::tma_load_2d(raw_base + r * RAW_BYTES, &p.tm_w, &raw_full[r], t.n0, ri * RAW_PER * (BK / 8));
+        }
       }
     }
   } else if (warp == kWarpLoadB || warp == kWarpLoadB2) {
-    // ---- widened activations -> ring; with a cluster, each CTA loads 1/cl of
-    // the rows and multicasts them to every CTA of the cluster ----
+    // ---- widened activations -> ring; the two warps take alternate stages
+    // (B_STAGES is even, so each keeps its own slots) ----
     if (lane == 0) {
-      const int rows = BN / p.cl;
-      const int first = warp == kWarpLoadB ? 0 : 1;   // B_STAGES is even: a warp keeps its slots
+      const int mine = warp == kWarpLoadB ? 0 : 1;
+      int sg = 0;   // stages so far (all tiles)
       bool ok = true;
-      for (int s = first; s < nst; s += 2) {
-        const int b = s % B_STAGES;
-        if (!tc::wait(&b_empty[b], ((s / B_STAGES) & 1) ^ 1, abort_flag, p.status, kWaitNs)) {
-          ok = false;
-          break;
+      for (int tid = blockIdx.x; tid < total_tiles && ok; tid += gridDim.x) {
+        Tile t;
+        if (!decode_tile(p, tid, n_tiles, t)) continue;
+        for (int s = 0; s < nst; ++s, ++sg) {
+          if ((sg & 1) != mine) continue;
+          const int b = sg % B_STAGES;
+          if (!tc::wait(&b_empty[b], ((sg / B_STAGES) & 1) ^ 1, abort_flag, p.status, kWaitNs)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&b_full[b], B_BYTES);
+          tc::tma_load_2d(b_base + b * B_BYTES, &p.tm_act, &b_full[b], s * BK, t.row0);
         }
-        mbar_arrive_expect_tx(&b_full[b], B_BYTES);
-        if (p.cl > 1)
-          tc::tma_load_2d_multicast(b_base + b * B_BYTES + crank * rows * 128, &p.tm_act, &b_full[b], s * BK,
-                                    row0 + crank * rows, cmask);
-        else
-          tc::tma_load_2d(b_base + b * B_BYTES, &p.tm_act, &b_full[b], s * BK, row0);
-      }
-      // every CTA of the cluster releases every slot before anyone leaves:
-      // no peer commit may still be on its way to this CTA's barriers
-      for (int b = first; ok && b < B_STAGES && b < nst; b += 2) {
-        const int uses = (nst - b + B_STAGES - 1) / B_STAGES;
-        ok = tc::wait(&b_empty[b], (uses - 1) & 1, abort_flag, p.status, kWaitNs);
       }
     }
   } else if (warp >= kWarpConv0 && warp < kWarpConv0 + kConvWarps) {
     // ---- nibbles -> fp16 operand A ----
-    const int t = threadIdx.x - kWarpConv0 * 32;  // output row within the tile
-    for (int s = 0; s < nst; ++s) {
-      const int ri = s / RAW_PER, sub = s % RAW_PER;   // packed-word copy and k-stage within it
-      const int r = ri % RAW_STAGES, a = s % A_STAGES;
-      if (!tc::wait(&raw_full[r], (ri / RAW_STAGES) & 1, abort_flag, p.status, kWaitNs)) break;
-      const uint32_t* raw = reinterpret_cast<const uint32_t*>(raw_base + r * RAW_BYTES);
-      uint32_t w[8];
-      if (p.mode == kExperts) {  // box [128 outputs][raw_rows words]
-        const uint4 lo = *reinterpret_cast<const uint4*>(raw + t * p.raw_rows + sub * 8);
-        const uint4 hi = *reinterpret_cast<const uint4*>(raw + t * p.raw_rows + sub * 8 + 4);
-        w[0] = lo.x; w[1] = lo.y; w[2] = lo.z; w[3] = lo.w;
-        w[4] = hi.x; w[5] = hi.y; w[6] = hi.z; w[7] = hi.w;
-      } else {  // box [raw_rows words][128 outputs]
+    const int tr = threadIdx.x - kWarpConv0 * 32;  // output row within the tile
+    int sg = 0, rg = 0;
+    bool ok = true;
+    for (int tid = blockIdx.x; tid < total_tiles && ok; tid += gridDim.x) {
+      Tile t;
+      if (!decode_tile(p, tid, n_tiles, t)) continue;
+      for (int s = 0; s < nst; ++s, ++sg) {
+        const int sub = s % RAW_PER;   // k-stage within its packed-word copy
+        const int r = rg % RAW_STAGES, a = sg % A_STAGES;
+        if (!tc::wait(&raw_full[r], (rg / RAW_STAGES) & 1, abort_flag, p.status, kWaitNs)) {
+          ok = false;
+          break;
+        }
+        const uint32_t* raw = reinterpret_cast<const uint32_t*>(raw_base + r * RAW_BYTES);
+        uint32_t w[8];
+        if (p.mode == kExperts) {  // box [128 outputs][raw_rows words]
+          const uint4 lo = *reinterpret_cast<const uint4*>(raw + tr * p.raw_rows + sub * 8);
+          const uint4 hi = *reinterpret_cast<const uint4*>(raw + tr * p.raw_rows + sub * 8 + 4);
+          w[0] = lo.x; w[1] = lo.y; w[2] = lo.z; w[3] = lo.w;
+          w[4] = hi.x; w[5] = hi.y; w[6] = hi.z; w[7] = hi.w;
+        } else {  // box [raw_rows words][128 outputs]
 #pragma unroll
-        for (int kb = 0; kb < 8; ++kb) w[kb] = raw[(sub * 8 + kb) * BM + t];
+          for (int kb = 0; kb < 8; ++kb) w[kb] = raw[(sub * 8 + kb) * BM + tr];
+        }
+        __syncwarp();
+        // the copy's words are in registers once its last k-stage is read
+        if (sub == RAW_PER - 1 || s == nst - 1) {
+          if (lane == 0) mbar_arrive(&raw_empty[r]);
+          ++rg;
+        }
+        if (!tc::wait(&a_empty[a], ((sg / A_STAGES) & 1) ^ 1, abort_flag, p.status, kWaitNs)) {
+          ok = false;
+          break;
+        }
+        uint8_t* arow = a_base + a * A_BYTES + tr * 128;
+#pragma unroll
+        for (int kb = 0; kb < 8; ++kb)
+          *reinterpret_cast<uint4*>(arow + ((kb ^ (tr & 7)) << 4)) = nibbles_to_f16(w[kb]);
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&a_full[a]);
       }
-      __syncwarp();
-      // the copy's words are in registers once its last k-stage is read
-      if (lane == 0 && (sub == RAW_PER - 1 || s == nst - 1)) mbar_arrive(&raw_empty[r]);
-      if (!tc::wait(&a_empty[a], ((s / A_STAGES) & 1) ^ 1, abort_flag, p.status, kWaitNs)) break;
-      uint8_t* arow = a_base + a * A_BYTES + t * 128;
-#pragma unroll
-      for (int kb = 0; kb < 8; ++kb)
-        *reinterpret_cast<uint4*>(arow + ((kb ^ (t & 7)) << 4)) = nibbles_to_f16(w[kb]);
-      tc::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&a_full[a]);
     }
   } else if (warp == kWarpMma) {
     // ---- one thread issues the MMAs ----
     // Lean issue loop: one wait pair and two descriptors per stage, four MMAs
     // per stage from constant offsets; group boundaries (multiples of 16)
-    // may fall inside a stage.
+    // may fall inside a stage. Every tile opens a new accumulation.
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_f16_f32(BM, BN);
       const uint64_t adesc0 = tc::sdesc_sw128(smem_addr(a_base));
       const uint64_t bdesc0 = tc::sdesc_sw128(smem_addr(b_base));
-      int seg = 0, buf = 0;
-      int seg_end = min(min(group, SEG_MAX), K);
-      uint32_t acc = 0;
-      bool ok = tc::wait(&acc_empty[0], 1, abort_flag, p.status, kWaitNs);
-      tc::fence_after_sync();
-      int a = 0, b = 0, a_phase = 0, b_phase = 0;
-      for (int s = 0; s < nst && ok; ++s) {
-        if (!tc::wait(&b_full[b], b_phase, abort_flag, p.status, kWaitNs, 200) ||
-            !tc::wait(&a_full[a], a_phase, abort_flag, p.status, kWaitNs, 200)) {
-          ok = false;
-          break;
-        }
+      int seg = -1, buf = 0, sg = 0;
+      bool ok = true;
+      for (int tid = blockIdx.x; tid < total_tiles && ok; tid += gridDim.x) {
+        Tile t;
+        if (!decode_tile(p, tid, n_tiles, t)) continue;
+        ++seg;
+        buf = seg & 1;
+        int seg_end = min(min(group, SEG_MAX), K);
+        uint32_t acc = 0;
+        if (!tc::wait(&acc_empty[buf], ((seg >> 1) & 1) ^ 1, abort_flag, p.status, kWaitNs)) break;
         tc::fence_after_sync();
-        const uint64_t ad = adesc0 + static_cast<uint64_t>((a * A_BYTES) >> 4);
-        const uint64_t bd = bdesc0 + static_cast<uint64_t>((b * B_BYTES) >> 4);
-        const int kbase = s * BK;
-#pragma unroll
-        for (int j = 0; j < BK / UMMA_K; ++j) {
-          const int k = kbase + j * UMMA_K;
-          if (k < K) {
-            if (k == seg_end) {  // close this accumulation, open the next buffer
-              tc::commit(&acc_full[buf]);
-              ++seg;
-              buf = seg & 1;
-              const int g = k / group;
-              seg_end = min(min((g + 1) * group, k + SEG_MAX), K);
-              if (!tc::wait(&acc_empty[buf], ((seg >> 1) & 1) ^ 1, abort_flag, p.status, kWaitNs)) {
-                ok = false;
-                break;
-              }
-              tc::fence_after_sync();
-              acc = 0;
-            }
-            tc::mma_f16(tmem + buf * BN, ad + 2 * j, bd + 2 * j, idesc, acc);
-            acc = 1;
+        for (int s = 0; s < nst && ok; ++s, ++sg) {
+          const int a = sg % A_STAGES, b = sg % B_STAGES;
+          if (!tc::wait(&b_full[b], (sg / B_STAGES) & 1, abort_flag, p.status, kWaitNs, 200) ||
+              !tc::wait(&a_full[a], (sg / A_STAGES) & 1, abort_flag, p.status, kWaitNs, 200)) {
+            ok = false;
+            break;
           }
-        }
-        if (!ok) break;
-        tc::commit(&a_empty[a]);
-        if (p.cl > 1)
-          tc::commit_multicast(&b_empty[b], cmask);
-        else
+          tc::fence_after_sync();
+          const uint64_t ad = adesc0 + static_cast<uint64_t>((a * A_BYTES) >> 4);
+          const uint64_t bd = bdesc0 + static_cast<uint64_t>((b * B_BYTES) >> 4);
+          const int kbase = s * BK;
+#pragma unroll
+          for (int j = 0; j < BK / UMMA_K; ++j) {
+            const int k = kbase + j * UMMA_K;
+            if (k < K) {
+              if (k == seg_end) {  // close this accumulation, open the next buffer
+                tc::commit(&acc_full[buf]);
+                ++seg;
+                buf = seg & 1;
+                const int g = k / group;
+                seg_end = min(min((g + 1) * group, k + SEG_MAX), K);
+                if (!tc::wait(&acc_empty[buf], ((seg >> 1) & 1) ^ 1, abort_flag, p.status, kWaitNs)) {
+                  ok = false;
+                  break;
+                }
+                tc::fence_after_sync();
+                acc = 0;
+              }
+              tc::mma_f16(tmem + buf * BN, ad + 2 * j, bd + 2 * j, idesc, acc);
+              acc = 1;
+            }
+          }
+          if (!ok) break;
+          tc::commit(&a_empty[a]);
           tc::commit(&b_empty[b]);
-        if (++a == A_STAGES) { a = 0; a_phase ^= 1; }
-        if (++b == B_STAGES) { b = 0; b_phase ^= 1; }
+        }
+        if (ok) tc::commit(&acc_full[buf]);
       }
-      if (ok) tc::commit(&acc_full[buf]);
     }
     __syncwarp();
   }
@@ -326,82 +360,94 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
     asm volatile("setmaxnreg.inc.sync.aligned.u32 176;");
     // ---- epilogue: warp w owns TMEM lanes 32(w%4).. (outputs), token half w/4 ----
     const int q = warp & 3, half = warp >> 2;
-    const int n = n0 + 32 * q + lane;
-    const bool n_ok = n < p.N;
     const int N = p.N;
     const int G = K / group;
     const bool partials = p.mode == kDensePartials;
     const int c0 = half * kEpiCols;
-    if (!partials)
-      for (int j = threadIdx.x; j < BN; j += kEpiWarps * 32)
-        xs_s[j] = (row0 + j < row_end) ? p.x_scale[row0 + j] : 0.f;
-    bar_sync_epilogue();
+    int seg = 0;   // accumulations drained so far (all tiles)
+    // Every epilogue thread walks every tile and meets both named barriers of
+    // each, even after a wait has run out (ok = false then skips the work):
+    // threads that left the loop early would strand the others at bar.sync.
+    bool ok = true;
+    for (int tid = blockIdx.x; tid < total_tiles; tid += gridDim.x) {
+      Tile t;
+      if (!decode_tile(p, tid, n_tiles, t)) continue;
+      const int n = t.n0 + 32 * q + lane;
+      const bool n_ok = n < N;
+      bar_sync_epilogue();   // the previous tile's output is written: xs_s may change
+      if (!partials)
+        for (int j = threadIdx.x; j < BN; j += kEpiWarps * 32)
+          xs_s[j] = (t.row0 + j < t.row_end) ? p.x_scale[t.row0 + j] : 0.f;
+      bar_sync_epilogue();
 
-    float T[kEpiCols];
+      float T[kEpiCols];
 #pragma unroll
-    for (int j = 0; j < kEpiCols; ++j) T[j] = 0.f;
+      for (int j = 0; j < kEpiCols; ++j) T[j] = 0.f;
 
-    // the scales of this group and the next three, loaded ahead: with the TMA
-    // pipes full a plain load takes ~1-2 us, a group's MMAs ~0.5 us
-    auto ld_scale = [&](int gg) -> uint32_t {
-      if (partials || !n_ok || gg >= G) return 0u;
-      const size_t si = (p.mode == kExperts) ? ((size_t)expert * N + n) * G + gg : (size_t)gg * N + n;
-      return p.w_scale[si];
-    };
-    uint32_t sr0 = ld_scale(0), sr1 = ld_scale(1), sr2 = ld_scale(2), sr3 = ld_scale(3);
-    int cur_g = 0;
-    int seg = 0;
-    for (int k0 = 0; k0 < K; ++seg) {
-      const int g = k0 / group;
-      if (g != cur_g) {   // segments walk k in order: the group advances by one
-        sr0 = sr1;
-        sr1 = sr2;
-        sr2 = sr3;
-        sr3 = ld_scale(g + 3);
-        cur_g = g;
-      }
-      const int kend = min(min((g + 1) * group, k0 + SEG_MAX), K);
-      const int buf = seg & 1;
-      if (!tc::wait(&acc_full[buf], (seg >> 1) & 1, abort_flag, p.status, kWaitNs)) break;
-      tc::fence_after_sync();
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + buf * BN + c0;
-      if (partials) {
-        int32_t* out = static_cast<int32_t*>(p.out);
+      // the scales of this group and the next three, loaded ahead: with the TMA
+      // pipes full a plain load takes ~1-2 us, a group's MMAs ~0.5 us
+      auto ld_scale = [&](int gg) -> uint32_t {
+        if (partials || !n_ok || gg >= G) return 0u;
+        const size_t si = (p.mode == kExperts) ? ((size_t)t.expert * N + n) * G + gg : (size_t)gg * N + n;
+        return p.w_scale[si];
+      };
+      uint32_t sr0 = ld_scale(0), sr1 = ld_scale(1), sr2 = ld_scale(2), sr3 = ld_scale(3);
+      int cur_g = 0;
+      for (int k0 = 0; ok && k0 < K; ++seg) {
+        const int g = k0 / group;
+        if (g != cur_g) {   // segments walk k in order: the group advances by one
+          sr0 = sr1;
+          sr1 = sr2;
+          sr2 = sr3;
+          sr3 = ld_scale(g + 3);
+          cur_g = g;
+        }
+        const int kend = min(min((g + 1) * group, k0 + SEG_MAX), K);
+        const int buf = seg & 1;
+        if (!tc::wait(&acc_full[buf], (seg >> 1) & 1, abort_flag, p.status, kWaitNs)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + buf * BN + c0;
+        if (partials) {
+          int32_t* out = static_cast<int32_t*>(p.out);
 #pragma unroll 1
-        for (int cc = 0; cc < kEpiCols / 32; ++cc) {
-          uint32_t v[32];
-          tc::tmem_ld32(taddr + cc * 32, v);
+          for (int cc = 0; cc < kEpiCols / 32; ++cc) {
+            uint32_t v[32];
+            tc::tmem_ld32(taddr + cc * 32, v);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int row = row0 + c0 + cc * 32 + j;
-            if (n_ok && row < row_end)
-              out[((size_t)row * G + g) * N + n] = __float2int_rn(__uint_as_float(v[j]));
+            for (int j = 0; j < 32; ++j) {
+              const int row = t.row0 + c0 + cc * 32 + j;
+              if (n_ok && row < t.row_end)
+                out[((size_t)row * G + g) * N + n] = __float2int_rn(__uint_as_float(v[j]));
+            }
+          }
+        } else {
+          const float sc = half_bits_to_f32(sr0);
+#pragma unroll
+          for (int cc = 0; cc < kEpiCols / 32; ++cc) {
+            uint32_t v[32];
+            tc::tmem_ld32(taddr + cc * 32, v);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) T[cc * 32 + j] = fmaf(sc, __uint_as_float(v[j]), T[cc * 32 + j]);
           }
         }
-      } else {
-        const float s = half_bits_to_f32(sr0);
-#pragma unroll
-        for (int cc = 0; cc < kEpiCols / 32; ++cc) {
-          uint32_t v[32];
-          tc::tmem_ld32(taddr + cc * 32, v);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) T[cc * 32 + j] = fmaf(s, __uint_as_float(v[j]), T[cc * 32 + j]);
-        }
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        k0 = kend;
       }
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[buf]);
-      k0 = kend;
-    }
 
-    if (!partials && !*abort_flag) {
-      const float bsv = (p.bias != nullptr && n_ok) ? __uint_as_float(static_cast<uint32_t>(p.bias[n]) << 16) : 0.f;
-      uint16_t* y = static_cast<uint16_t*>(p.out);
+      if (ok && !partials && !*abort_flag) {
+        const float bsv = (p.bias != nullptr && n_ok) ? __uint_as_float(static_cast<uint32_t>(p.bias[n]) << 16) : 0.f;
+        uint16_t* y = static_cast<uint16_t*>(p.out);
 #pragma unroll
-      for (int j = 0; j < kEpiCols; ++j) {
-        const int row = row0 + c0 + j;
-        if (n_ok && row < row_end)
-          y[(size_t)row * N + n] = static_cast<uint16_t>(f32_to_bf16_bits(fmaf(xs_s[c0 + j], T[j], bsv)));
+        for (int j = 0; j < kEpiCols; ++j) {
+          const int row = t.row0 + c0 + j;
+          if (n_ok && row < t.row_end)
+            y[(size_t)row * N + n] = static_cast<uint16_t>(f32_to_bf16_bits(fmaf(xs_s[c0 + j], T[j], bsv)));
+        }
       }
     }
   }
@@ -415,7 +461,6 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (p.cl > 1) tc::cluster_sync();
   if (warp == kWarpMma) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
@@ -470,6 +515,16 @@ cudaError_t encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void*
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+int sm_count_w4a8() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  }
+  return n;
+}
+
 cudaError_t widen(const void* src, void* dst, int64_t rows, int64_t K, bool fp8, cudaStream_t s) {
   const size_t n16 = (size_t)rows * (size_t)K / 16;
   if (n16 == 0) return cudaSuccess;
@@ -493,13 +548,7 @@ cudaError_t run(const W4A8Args& a, int mode, cudaStream_t s) {
   cudaError_t e = a.prewidened ? cudaSuccess : widen(a.act, a.workspace, a.M, a.K, experts, s);
   if (e != cudaSuccess) return e;
 
-  // Optional cluster along N: the CTAs of a cluster share one activation
-  // tile, each loading 1/cl of it and multicasting it to the others. Measured
-  // on GB300 this did not beat one CTA per tile (the activation stream is not
-  // limited by L2 bandwidth), so the launcher uses cl = 1; the multicast path
-  // stays for shapes that are.
   const int n_tiles = static_cast<int>((a.N + BM - 1) / BM);
-  const int cl = 1;
 
   Params p;
   memset(&p, 0, sizeof(p));
@@ -509,7 +558,7 @@ cudaError_t run(const W4A8Args& a, int mode, cudaStream_t s) {
   {
     const cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.M};
     const cuuint64_t strides[1] = {(cuuint64_t)a.K * 2};
-    const cuuint32_t box[2] = {BK, static_cast<cuuint32_t>(BN / cl)};   // one CTA's slice of the tile
+    const cuuint32_t box[2] = {BK, BN};
     e = encode(&p.tm_act, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.workspace, dims, strides, box,
                CU_TENSOR_MAP_SWIZZLE_128B);
     if (e != cudaSuccess) return e;
@@ -539,23 +588,15 @@ cudaError_t run(const W4A8Args& a, int mode, cudaStream_t s) {
   p.mode = mode;
   p.status = a.status;
 
-  p.cl = cl;
-  const unsigned gx = static_cast<unsigned>((n_tiles + cl - 1) / cl * cl);
-  const long long gy = experts ? (a.M + BN - 1) / BN + a.E : (a.M + BN - 1) / BN;
-  if (gy > 65535) return cudaErrorInvalidConfiguration;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(gx, static_cast<unsigned>(gy));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cl;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, w4a8_tc_kernel, p);
+  // tile rows: dense, one per 256 rows; experts, an upper bound on the tiles
+  // of all segments together (each expert's last tile may be partial)
+  const long long y_tiles = experts ? (a.M + BN - 1) / BN + a.E : (a.M + BN - 1) / BN;
+  const long long total = y_tiles * n_tiles;
+  if (total > INT32_MAX) return cudaErrorInvalidConfiguration;
+  // persistent: one CTA per SM (the shared-memory rings fill an SM)
+  const long long grid = total < sm_count_w4a8() ? total : sm_count_w4a8();
+  w4a8_tc_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, s>>>(p, n_tiles, static_cast<int>(y_tiles));
+  return cudaGetLastError();
 }
 
 }  // namespace
