@@ -62,6 +62,9 @@ TRAFFIC = {
     # quantize_chunks_kernel<bf16, 16, 2>, N=14336 K=4096 g128 (117,459,456 + 7,766,016; the codes,
     # scales and zeros are still in L2 when the kernel ends), profiles/quantize_groupwise_n14336_k4096_full.md
     "quantize": (125225472, "cf9a6143ae4772be", "tools.cu"),
+    # w4a8_tc_kernel, W4A8 diffusion M=16384 K=N=3072 g=-1 (105,705,216 + 62,773,504),
+    # profiles/w4a8_tc_kernel_diffusion_m16384_k3072_n3072_full.md
+    "w4a8_diffusion": (168478720, "9171a7dfc2523964", "w4a8.cu"),
 }
 
 
@@ -392,7 +395,7 @@ def bench_rows(dev, stream, bf16_tf, peak_kind, hbm_peak, only=None):
             "gemm_ms": t_gemm, "gemm_tops": round(tops_gemm, 1),
             "quant_ms": t_quant, "quant_gbs": round(3.0 * M * K / (t_quant * 1e-3) / 1e9, 1),
             "roofline": {"bound": "tensor", "achieved": round(tops_gemm, 1), "peak": bf16_tf, "unit": "TFLOP/s",
-                         "frac": round(tops_gemm / bf16_tf, 4), "traffic": None,
+                         "frac": round(tops_gemm / bf16_tf, 4), "traffic": _traffic(name),
                          "peak_source": f"{peak_kind} bf16_tflops (the exact int8 x int4 products run on the "
                                         "fp16 tensor datapath; sm_103a has no int8 tcgen05 MMA)",
                          "kernel": "w4a8_gemm call = widen_kernel + w4a8_tc_kernel"},
