@@ -83,26 +83,6 @@ W4_DEV void tma_prefetch_l2_2d(const void* tmap, int c0, int c1) {
                :: "l"(tmap), "r"(c0), "r"(c1) : "memory");
 }
 
-// The same tile slice lands at the same shared-memory offset in every CTA of
-// the cluster named in `cta_mask`, and completes tx bytes on the mbarrier at
-// `bar`'s offset in each of them.
-W4_DEV void tma_load_2d_multicast(void* smem_dst, const void* tmap, uint64_t* bar, int c0, int c1, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster "
-      "[%0], [%1, {%3, %4}], [%2], %5;"
-      :: "r"(smem_addr(smem_dst)), "l"(tmap), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "h"(cta_mask) : "memory");
-}
-
-W4_DEV uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-W4_DEV void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 // Makes this thread's generic-proxy shared-memory writes visible to the async
 // proxy (the tensor core reads its operands through it).
 W4_DEV void fence_proxy_async_smem() {
@@ -161,13 +141,6 @@ W4_DEV void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t 
 W4_DEV void commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                :: "r"(smem_addr(bar)) : "memory");
-}
-
-// Arrive (once) on the mbarrier at `bar`'s offset in every CTA of `cta_mask`
-// when every tcgen05 op this thread issued so far is done.
-W4_DEV void commit_multicast(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-               :: "r"(smem_addr(bar)), "h"(cta_mask) : "memory");
 }
 
 // Warp-wide: 32 lanes x 32 consecutive 32-bit columns from TMEM. The wait is
