@@ -209,6 +209,20 @@ w4_status w4a16_gemm(const void* x, const void* qweight, const void* w_scale, in
                      int64_t M, int64_t N, int64_t K, void* stream);
 
 /*
+ * w4a16_gemm from and to host memory, for a caller whose activations and
+ * results live on the host: one call queues on `stream` the copy of x_host
+ * [M, K] bf16 into x_dev, the w4a16_gemm of x_dev into y_dev, and the copy of
+ * y_dev [M, N] into y_host (each copy one cudaMemcpyAsync). x_dev and y_dev are
+ * caller-owned device buffers (16- and 8-byte aligned). For the copies to run
+ * asynchronously x_host and y_host must be page-locked; y_host holds the
+ * result once `stream` has been synchronized. Other arguments and errors as
+ * w4a16_gemm; nothing is queued when validation fails.
+ */
+w4_status w4a16_gemm_host(const void* x_host, void* x_dev, const void* qweight, const void* w_scale,
+                          int32_t w_scale_dtype, const void* zeros, int32_t group, const void* bias, void* y_dev,
+                          void* y_host, int64_t M, int64_t N, int64_t K, void* stream);
+
+/*
  * W4AFP8 grouped expert linear ([FP8] W4AFP8Config: int4 group-128 routed
  * experts, symmetric, fp8 per-token dynamic activations; get_checkpoint_weight_mapper:
  * compressed-tensors "weight_packed" / "weight_scale" layout).

@@ -17,7 +17,7 @@ import torch
 __all__ = [
     "W4Error", "load", "library_path",
     "w4_quant_act_per_token", "w4a8_gemm", "w4a8_gemm_bf16in", "w4a8_gemm_noalloc", "w4a8_group_partials", "w4a16_gemm",
-    "w4afp8_moe_grouped_gemm", "w4_quantize_groupwise", "w4_repack_s4_to_uint4b8",
+    "w4a16_gemm_host", "w4afp8_moe_grouped_gemm", "w4_quantize_groupwise", "w4_repack_s4_to_uint4b8",
     "w4_embedding_gather", "w4_lm_head_gemv",
     "w4_moe_route", "w4_moe_gather_quant_fp8", "w4afp8_moe_gemm_bf16in", "w4_moe_silu_mul_quant_fp8",
     "w4_moe_combine",
@@ -45,6 +45,7 @@ _SIGNATURES = {
     "w4a8_gemm_bf16in": (_I32, [_P, _P, _P, _I32, _I32, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
     "w4a8_gemm_noalloc": (_I32, [_P, _P, _P, _P, _I32, _I32, _P, _P, _I64, _I64, _I64, _P]),
     "w4a16_gemm": (_I32, [_P, _P, _P, _I32, _P, _I32, _P, _P, _I64, _I64, _I64, _P]),
+    "w4a16_gemm_host": (_I32, [_P, _P, _P, _P, _I32, _P, _I32, _P, _P, _P, _I64, _I64, _I64, _P]),
     "w4afp8_moe_grouped_gemm": (_I32, [_P, _P, _P, _I32, _P, _P, _I32, _I32, _P, _I64, _I64, _I64, _P, _SZ, _P]),
     "w4_quantize_groupwise": (_I32, [_P, _I32, _I64, _I64, _I32, _P, _P, _P, _P]),
     "w4_repack_s4_to_uint4b8": (_I32, [_P, _P, _I64, _P]),
@@ -230,6 +231,24 @@ def w4a16_gemm(x, qweight, w_scale, group: int, zeros=None, bias=None, y=None, s
     _check(load().w4a16_gemm(_ptr(x), _ptr(qweight), _ptr(w_scale), _scale_dtype(w_scale), _ptr(zeros), group,
                              _ptr(bias), _ptr(y), M, N, K, _stream(stream, x.device)), "w4a16_gemm")
     return y
+
+
+def w4a16_gemm_host(x_host, x_dev, qweight, w_scale, group: int, y_dev, y_host, zeros=None, bias=None, stream=None):
+    """``w4a16_gemm`` from and to host memory: copies ``x_host`` (page-locked bf16
+    ``[M, K]`` CPU tensor) into ``x_dev``, runs the GEMM into ``y_dev`` and copies
+    it into ``y_host`` (page-locked bf16 ``[M, N]``), all queued on the stream;
+    ``y_host`` is valid once the stream is synchronized."""
+    if x_host.is_cuda or y_host.is_cuda or x_host.dtype != torch.bfloat16 or y_host.dtype != torch.bfloat16:
+        raise ValueError("x_host and y_host must be bf16 CPU tensors")
+    _cuda2d(x_dev, "x_dev", (torch.bfloat16,))
+    M, K = x_host.shape
+    N = qweight.shape[1]
+    if tuple(x_dev.shape) != (M, K) or tuple(y_host.shape) != (M, N) or tuple(y_dev.shape) != (M, N):
+        raise ValueError("inconsistent shapes for w4a16_gemm_host")
+    _check(load().w4a16_gemm_host(_ptr(x_host), _ptr(x_dev), _ptr(qweight), _ptr(w_scale), _scale_dtype(w_scale),
+                                  _ptr(zeros), group, _ptr(bias), _ptr(y_dev), _ptr(y_host), M, N, K,
+                                  _stream(stream, x_dev.device)), "w4a16_gemm_host")
+    return y_host
 
 
 def w4afp8_moe_grouped_gemm(qx, x_scale, expert_offsets, qweight, w_scale, group: int, y=None, workspace=None,

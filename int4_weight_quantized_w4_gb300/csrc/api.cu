@@ -206,30 +206,65 @@ w4_status w4a8_group_partials(const void* qx, const void* qweight, int32_t group
                      workspace_bytes, stream);
 }
 
-w4_status w4a16_gemm(const void* x, const void* qweight, const void* w_scale, int32_t w_scale_dtype,
-                     const void* zeros, int32_t group, const void* bias, void* y,
-                     int64_t M, int64_t N, int64_t K, void* stream) {
-  int32_t g = 0;
-  w4_status st = check_dims_group(M, N, K, group, &g);
+// The checks of w4a16_gemm; `check_ptrs` false stops after the ones that do
+// not look at the pointers (a zero-size call).
+static w4_status check_w4a16(const void* x, const void* qweight, const void* w_scale, int32_t w_scale_dtype,
+                             const void* zeros, const void* bias, const void* y, int64_t M, int64_t N, int64_t K,
+                             int32_t group, int32_t* g, bool check_ptrs) {
+  w4_status st = check_dims_group(M, N, K, group, g);
   if (st != W4_OK) return st;
   if (w_scale_dtype != W4_FP16 && w_scale_dtype != W4_BF16)
     return fail(W4_ERR_DTYPE, "w4a16_gemm scales must be W4_FP16 or W4_BF16");
-  if (K % 64 != 0 || g % 64 != 0)
+  if (K % 64 != 0 || *g % 64 != 0)
     return fail(W4_ERR_UNSUPPORTED, "w4a16 tiles need K and the group to be multiples of 64 (K=%lld group=%d)",
-                (long long)K, g);
-  if (w4::w4a16_smem_bytes(N, K, g) > 227 * 1024)
+                (long long)K, *g);
+  if (w4::w4a16_smem_bytes(N, K, *g) > 227 * 1024)
     return fail(W4_ERR_UNSUPPORTED, "w4a16 keeps a token row of x in shared memory: K=%lld is too long", (long long)K);
-  if (M == 0) return ok();
+  if (!check_ptrs) return W4_OK;
   if (!x || !qweight || !w_scale || !y) return fail(W4_ERR_NULL, "x, qweight, w_scale and y must be non-NULL");
   if (!aligned(x, 16) || !aligned(qweight, 16) || !aligned(y, 8) || !aligned(w_scale, 16) ||
       (zeros && !aligned(zeros, 16)) || (bias && !aligned(bias, 8)))
     return fail(W4_ERR_ALIGN, "x, qweight, scales and zeros must be 16-byte aligned; y and bias 8-byte aligned");
   if (M > INT32_MAX || N > INT32_MAX) return fail(W4_ERR_UNSUPPORTED, "M or N too large");
+  return W4_OK;
+}
+
+static w4_status launch_w4a16_checked(const void* x, const void* qweight, const void* w_scale, int32_t w_scale_dtype,
+                                      const void* zeros, int32_t g, const void* bias, void* y, int64_t M, int64_t N,
+                                      int64_t K, cudaStream_t s) {
   unsigned int* status = nullptr;
   cudaError_t e = status_ptr(&status);
   if (e != cudaSuccess) return from_cuda(e, "device status word");
   w4::W4A16Args a{x, qweight, w_scale, w_scale_dtype == W4_BF16, zeros, bias, y, M, N, K, g, status};
-  return from_cuda(w4::launch_w4a16(a, static_cast<cudaStream_t>(stream)), "w4a16 launch");
+  return from_cuda(w4::launch_w4a16(a, s), "w4a16 launch");
+}
+
+w4_status w4a16_gemm(const void* x, const void* qweight, const void* w_scale, int32_t w_scale_dtype,
+                     const void* zeros, int32_t group, const void* bias, void* y,
+                     int64_t M, int64_t N, int64_t K, void* stream) {
+  int32_t g = 0;
+  w4_status st = check_w4a16(x, qweight, w_scale, w_scale_dtype, zeros, bias, y, M, N, K, group, &g, M > 0);
+  if (st != W4_OK) return st;
+  if (M == 0) return ok();
+  return launch_w4a16_checked(x, qweight, w_scale, w_scale_dtype, zeros, g, bias, y, M, N, K,
+                              static_cast<cudaStream_t>(stream));
+}
+
+w4_status w4a16_gemm_host(const void* x_host, void* x_dev, const void* qweight, const void* w_scale,
+                          int32_t w_scale_dtype, const void* zeros, int32_t group, const void* bias, void* y_dev,
+                          void* y_host, int64_t M, int64_t N, int64_t K, void* stream) {
+  int32_t g = 0;
+  w4_status st = check_w4a16(x_dev, qweight, w_scale, w_scale_dtype, zeros, bias, y_dev, M, N, K, group, &g, M > 0);
+  if (st != W4_OK) return st;
+  if (M == 0) return ok();
+  if (!x_host || !y_host) return fail(W4_ERR_NULL, "x_host and y_host must be non-NULL");
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(x_dev, x_host, static_cast<size_t>(M) * K * 2, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return from_cuda(e, "copy of x to the device");
+  st = launch_w4a16_checked(x_dev, qweight, w_scale, w_scale_dtype, zeros, g, bias, y_dev, M, N, K, s);
+  if (st != W4_OK) return st;
+  return from_cuda(cudaMemcpyAsync(y_host, y_dev, static_cast<size_t>(M) * N * 2, cudaMemcpyDeviceToHost, s),
+                   "copy of y to the host");
 }
 
 static w4_status check_experts(int64_t R, int64_t N, int64_t K, int32_t group, int32_t E, int32_t w_scale_dtype,

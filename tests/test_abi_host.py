@@ -248,3 +248,19 @@ def test_moe_glue_validation(lib):
     assert lib.w4_moe_combine(FAKE, 16, 16, FAKE, None, 2, 8, FAKE, None) == w4.W4_ERR_NULL
     assert lib.w4_moe_combine(FAKE, 16, 16, FAKE, FAKE, 2, 0, FAKE, None) == w4.W4_ERR_SHAPE
     assert lib.w4_moe_combine(FAKE, 16, 16, FAKE, FAKE, 0, 8, FAKE, None) == w4.W4_OK
+
+
+def test_w4a16_host_entry_validation(lib):
+    def call(**kw):
+        a = dict(xh=FAKE, xd=FAKE, qw=FAKE, ws=FAKE, wdt=w4.W4_FP16, z=None, group=128, b=None, yd=FAKE, yh=FAKE,
+                 M=1, N=256, K=256)
+        a.update(kw)
+        return lib.w4a16_gemm_host(a["xh"], a["xd"], a["qw"], a["ws"], a["wdt"], a["z"], a["group"], a["b"], a["yd"],
+                                   a["yh"], a["M"], a["N"], a["K"], None)
+    assert call(xh=None) == w4.W4_ERR_NULL
+    assert call(yh=None) == w4.W4_ERR_NULL
+    assert call(xd=None) == w4.W4_ERR_NULL
+    assert call(xd=ODD) == w4.W4_ERR_ALIGN
+    assert call(wdt=w4.W4_INT8) == w4.W4_ERR_DTYPE
+    assert call(group=96) == w4.W4_ERR_GROUP
+    assert call(M=0, xh=None, yh=None) == w4.W4_OK

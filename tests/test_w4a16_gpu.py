@@ -140,3 +140,21 @@ def test_w4a16_back_to_back_chain_reads_previous_output():
                             for c in range(0, N, 1024)], axis=1)
         check_bf16_output(yb, r, f"chain step {i}")
         prev = yb
+
+
+def test_w4a16_host_entry_matches_device_entry():
+    """w4a16_gemm_host (x and y in page-locked host memory) gives the bytes of
+    w4a16_gemm on device buffers, and matches the oracle."""
+    M, K, N, g = 3, 1024, 512, 128
+    xb = S.activations_bf16(M, K, seed=41)
+    qw_np, sw_np = S.random_words((K // 8, N), seed=1), S.scales_f16((K // g, N), seed=2)
+    qw, sw = to_dev(qw_np), to_dev(sw_np)
+    x_host = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).pin_memory()
+    y_host = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    y_dev = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    w4.w4a16_gemm_host(x_host, x_dev, qw, sw, g, y_dev, y_host)
+    y_ref = w4.w4a16_gemm(bf16(xb), qw, sw, g)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(y_host.view(torch.int16).numpy().view(np.uint16), bits(y_ref))
+    check_bf16_output(bits(y_ref), O.w4a16_linear(xb, qw_np, sw_np, g), "host entry")
