@@ -32,6 +32,16 @@ def test_w4a8_partials_bit_exact(M, N, K, group):
     np.testing.assert_array_equal(P.cpu().numpy(), O.w4a8_group_partials(qx, qw, group))
 
 
+def test_w4a8_partials_more_tiles_than_sms():
+    """2176 x 2600 at K = 384: 9 x 21 = 189 tiles of 256 x 128 for 152 SMs, so
+    some persistent CTAs take two tiles (both ragged in M and N); bit-exact."""
+    M, N, K, group = 2176, 2600, 384, 128
+    _, qx, _, qw, _ = _inputs(M, N, K, group, seed=77)
+    P = w4.w4a8_group_partials(to_dev(qx), to_dev(qw), group)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(P.cpu().numpy(), O.w4a8_group_partials(qx, qw, group))
+
+
 def test_w4a8_partials_extremes():
     """|P| = 127 * 8 * group at the extreme codes: 130048 at group 128, and the
     largest exact case, group 16384."""
