@@ -200,15 +200,22 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(int32_t* __restrict_
   if (threadIdx.x == 0) offsets[E] = carry;
 }
 
+// silu(g) = g / (1 + e^-g) in fp32 with the fast exponential and divide (a
+// few ulp; the bf16 result it feeds is what the reading fixes). Below -80,
+// where 1 + e^-g passes the fast divide's range, silu(g) = g e^g to within
+// e^-80 relative.
+W4_DEV float silu_f32(float g) {
+  return g > -80.f ? __fdividef(g, 1.f + __expf(-g)) : g * __expf(g);
+}
+
 // act = bf16(silu(g) * u) for one chunk of 8 gate and 8 up values.
 W4_DEV uint4 silu_mul_chunk(const uint4& g, const uint4& u) {
   const uint32_t gw[4] = {g.x, g.y, g.z, g.w}, uw[4] = {u.x, u.y, u.z, u.w};
   uint32_t o[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float g0 = bf16_lo(gw[i]), g1 = bf16_hi(gw[i]);
-    const float a0 = __fmul_rn(__fdiv_rn(g0, __fadd_rn(1.f, expf(-g0))), bf16_lo(uw[i]));
-    const float a1 = __fmul_rn(__fdiv_rn(g1, __fadd_rn(1.f, expf(-g1))), bf16_hi(uw[i]));
+    const float a0 = silu_f32(bf16_lo(gw[i])) * bf16_lo(uw[i]);
+    const float a1 = silu_f32(bf16_hi(gw[i])) * bf16_hi(uw[i]);
     o[i] = pack_bf16x2(a0, a1);
   }
   return make_uint4(o[0], o[1], o[2], o[3]);

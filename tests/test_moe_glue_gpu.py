@@ -139,13 +139,15 @@ def test_silu_mul_quant(R, I):
 
 def test_silu_mul_quant_edge_values():
     """Gates far below zero (silu -> -0), a zero row (scale 1, codes 0), large
-    gates (silu(g) = g)."""
+    gates (silu(g) = g), and gates from -100 to -60 (tiny activations on both
+    sides of the kernel's switch to g e^g)."""
     R, I = 4, 64
     h = S.activations_bf16(R, 2 * I, seed=3)
     gf = S.bf16_bits_to_f32(h).copy()
     gf[0, :I] = -200.0
     gf[1, :] = 0.0
     gf[2, :I] = 90.0
+    gf[3, :I] = np.linspace(-100.0, -60.0, I)   # across the switch to g e^g
     _act_check(S.to_bf16_bits(gf), "silu edges")
 
 
