@@ -99,6 +99,19 @@ def decode_bytes(M=DEC_M, K=DEC_K, N=DEC_N, G=DEC_G, zeros=False):
     return b
 
 
+def max_over_ranks(value, device, world):
+    """The largest of the ranks' values (every rank gets it), after a barrier;
+    the value itself with one rank. Replicas: no data moves between ranks
+    except this one number."""
+    if world <= 1:
+        return value
+    import torch
+    torch.distributed.barrier()
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 class ClockSampler:
     """Samples SM clocks and throttle reasons with nvidia-smi during a region."""
 
@@ -247,11 +260,7 @@ def run_ours(args, rank, world, local_rank):
     ms = e0.elapsed_time(e1)
     clocks = clk.summary(t_begin, t_end)
     clocks["window"] = window
-    if world > 1:
-        torch.distributed.barrier()
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev, world)
     ms_per_step = ms / steps
     nbytes = decode_bytes()
     value = world * steps * nbytes / (ms * 1e-3) / 1e9
