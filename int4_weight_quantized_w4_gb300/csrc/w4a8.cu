@@ -40,17 +40,35 @@ namespace {
 
 constexpr int BM = 128;          // outputs per tile (MMA M, TMEM lanes)
 constexpr int BN = 256;          // tokens per tile (MMA N)
-constexpr int BK = 64;           // k per stage (one 128-byte fp16 swizzle row)
+constexpr int KS = 64;           // k per sub-tile (one 128-byte fp16 swizzle row)
 constexpr int UMMA_K = 16;
-constexpr int A_STAGES = 3;      // converted weight tiles
-constexpr int B_STAGES = 4;      // activation tiles (TMA)
-constexpr int RAW_STAGES = 2;    // packed weight words (TMA), RAW_PER k-stages per slot
-constexpr int RAW_PER = 4;       // k-stages per packed-word copy (16 KB: one copy per 256 k)
 constexpr int SEG_MAX = 16384;   // longest accumulation before a drain (exactness bound)
 
-constexpr int A_BYTES = BM * BK * 2;    // 16 KB
-constexpr int B_BYTES = BN * BK * 2;    // 32 KB
-constexpr int RAW_BYTES = RAW_PER * BM * BK / 2;  // 16 KB
+constexpr int A_SUB = BM * KS * 2;      // 16 KB per sub-tile
+constexpr int B_SUB = BN * KS * 2;      // 32 KB per sub-tile
+
+// A stage is SUBS sub-tiles of KS k; the MMA thread's per-stage waits, fence
+// and commits are shared by 4 x SUBS MMAs. Measured on GB300: with the operand
+// producers taken out entirely a 64-k stage still took ~0.8 us (its four MMAs
+// alone ~0.25 us in isolation), and two sub-tiles per stage raised the dense
+// GEMM 12-19%. Dense tiles use two; expert mode keeps one (with two, expert
+// segments that do not fill whole tiles disagreed with the oracle, cause not
+// yet found).
+template <int SUBS>
+struct Cfg {
+  static constexpr int BK = KS * SUBS;                     // k per stage
+  static constexpr int A_STAGES = SUBS == 1 ? 3 : 2;       // converted weight tiles
+  static constexpr int B_STAGES = SUBS == 1 ? 4 : 2;       // activation tiles; even: each copy warp keeps its slots
+  static constexpr int RAW_STAGES = 2;                     // packed weight words, RAW_PER k-stages per slot
+  static constexpr int RAW_PER = 4 / SUBS;                 // one 16 KB packed-word copy per 256 k
+  static constexpr int A_BYTES = A_SUB * SUBS;
+  static constexpr int B_BYTES = B_SUB * SUBS;
+  static constexpr int RAW_BYTES = RAW_PER * BM * BK / 2;  // 16 KB
+  static constexpr int SMEM = B_STAGES * B_BYTES + A_STAGES * A_BYTES + RAW_STAGES * RAW_BYTES + 2048 + 1024;
+};
+static_assert(Cfg<1>::RAW_PER * Cfg<1>::BK / 8 == 32 && Cfg<2>::RAW_PER * Cfg<2>::BK / 8 == 32,
+              "a packed-word copy is 32 word rows in both configurations");
+static_assert(Cfg<1>::SMEM <= 232448 && Cfg<2>::SMEM <= 232448, "shared memory per CTA");
 
 // Warp roles, four warpgroups: 0-7 epilogue (warp w reads TMEM lane quadrant
 // w % 4, token half w / 4), 8-11 converters, 12 weight-word TMA, 13 and 15
@@ -71,7 +89,6 @@ constexpr uint32_t kTmemCols = 2 * BN;        // double-buffered accumulator
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait
 constexpr int kEpiCols = BN / 2;              // token columns per epilogue thread
 
-constexpr int kSmemBytes = B_STAGES * B_BYTES + A_STAGES * A_BYTES + RAW_STAGES * RAW_BYTES + 2048 + 1024;
 
 enum Mode : int { kDenseY = 0, kDensePartials = 1, kExperts = 2 };
 
@@ -84,7 +101,7 @@ struct Params {
   void* out;               // bf16 [rows, N] or int32 [rows, G, N]
   const int32_t* offsets;  // [E + 1] (experts)
   int E, M, N, K, group, mode;
-  int raw_rows;            // word rows (k / 8) per packed-word copy: min(RAW_PER * BK / 8, K / 8)
+  int raw_rows;            // word rows (k / 8) per packed-word copy: min(32, K / 8)
   unsigned int* status;
 };
 
@@ -144,8 +161,12 @@ W4_DEV bool decode_tile(const Params& p, int tid, int n_tiles, Tile& t) {
 // operand B, the two TMEM accumulators) keeps counting across tiles, so the
 // copies and conversions of the next tile run while this tile's last groups
 // are multiplied and its output is written.
+template <int SUBS>
 __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_constant__ Params p, int n_tiles,
                                                               int y_tiles) {
+  using C = Cfg<SUBS>;
+  constexpr int BK = C::BK, A_STAGES = C::A_STAGES, B_STAGES = C::B_STAGES, RAW_STAGES = C::RAW_STAGES;
+  constexpr int RAW_PER = C::RAW_PER, A_BYTES = C::A_BYTES, B_BYTES = C::B_BYTES, RAW_BYTES = C::RAW_BYTES;
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
 
@@ -246,7 +267,9 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
             break;
           }
           mbar_arrive_expect_tx(&b_full[b], B_BYTES);
-          tc::tma_load_2d(b_base + b * B_BYTES, &p.tm_act, &b_full[b], s * BK, t.row0);
+#pragma unroll
+          for (int u = 0; u < SUBS; ++u)   // sub-tiles past K land as zeros
+            tc::tma_load_2d(b_base + b * B_BYTES + u * B_SUB, &p.tm_act, &b_full[b], s * BK + u * KS, t.row0);
         }
       }
     }
@@ -266,15 +289,20 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
           break;
         }
         const uint32_t* raw = reinterpret_cast<const uint32_t*>(raw_base + r * RAW_BYTES);
-        uint32_t w[8];
+        constexpr int kWords = BK / 8;   // packed words of one output per stage
+        uint32_t w[kWords];
         if (p.mode == kExperts) {  // box [128 outputs][raw_rows words]
-          const uint4 lo = *reinterpret_cast<const uint4*>(raw + tr * p.raw_rows + sub * 8);
-          const uint4 hi = *reinterpret_cast<const uint4*>(raw + tr * p.raw_rows + sub * 8 + 4);
-          w[0] = lo.x; w[1] = lo.y; w[2] = lo.z; w[3] = lo.w;
-          w[4] = hi.x; w[5] = hi.y; w[6] = hi.z; w[7] = hi.w;
+#pragma unroll
+          for (int v4 = 0; v4 < kWords / 4; ++v4) {
+            const uint4 q4 = *reinterpret_cast<const uint4*>(raw + tr * p.raw_rows + sub * kWords + 4 * v4);
+            w[4 * v4] = q4.x;
+            w[4 * v4 + 1] = q4.y;
+            w[4 * v4 + 2] = q4.z;
+            w[4 * v4 + 3] = q4.w;
+          }
         } else {  // box [raw_rows words][128 outputs]
 #pragma unroll
-          for (int kb = 0; kb < 8; ++kb) w[kb] = raw[(sub * 8 + kb) * BM + tr];
+          for (int kb = 0; kb < kWords; ++kb) w[kb] = raw[(sub * kWords + kb) * BM + tr];
         }
         __syncwarp();
         // the copy's words are in registers once its last k-stage is read
@@ -288,8 +316,8 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
         }
         uint8_t* arow = a_base + a * A_BYTES + tr * 128;
 #pragma unroll
-        for (int kb = 0; kb < 8; ++kb)
-          *reinterpret_cast<uint4*>(arow + ((kb ^ (tr & 7)) << 4)) = nibbles_to_f16(w[kb]);
+        for (int kb = 0; kb < kWords; ++kb)   // word kb: sub-tile kb / 8, 16-byte chunk kb % 8 of the row
+          *reinterpret_cast<uint4*>(arow + (kb >> 3) * A_SUB + (((kb & 7) ^ (tr & 7)) << 4)) = nibbles_to_f16(w[kb]);
         tc::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&a_full[a]);
@@ -328,6 +356,8 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
           const int kbase = s * BK;
 #pragma unroll
           for (int j = 0; j < BK / UMMA_K; ++j) {
+            // MMA j: sub-tile j / 4, 32-byte step j % 4 inside its swizzle rows
+            constexpr int kPerSub = KS / UMMA_K;
             const int k = kbase + j * UMMA_K;
             if (k < K) {
               if (k == seg_end) {  // close this accumulation, open the next buffer
@@ -343,7 +373,9 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
                 tc::fence_after_sync();
                 acc = 0;
               }
-              tc::mma_f16(tmem + buf * BN, ad + 2 * j, bd + 2 * j, idesc, acc);
+              const int u = j / kPerSub, jj = j % kPerSub;
+              tc::mma_f16(tmem + buf * BN, ad + ((u * A_SUB) >> 4) + 2 * jj, bd + ((u * B_SUB) >> 4) + 2 * jj, idesc,
+                          acc);
               acc = 1;
             }
           }
@@ -540,7 +572,9 @@ cudaError_t widen(const void* src, void* dst, int64_t rows, int64_t K, bool fp8,
 cudaError_t run(const W4A8Args& a, int mode, cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(w4a8_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(w4a8_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<1>::SMEM);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(w4a8_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<2>::SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -554,11 +588,11 @@ cudaError_t run(const W4A8Args& a, int mode, cudaStream_t s) {
   memset(&p, 0, sizeof(p));
   // packed-word copies cover RAW_PER k-stages, or all of a short K (expert
   // mode needs K % 32 == 0, so its copy width is a multiple of 16 bytes)
-  p.raw_rows = static_cast<int>(a.K / 8 < RAW_PER * BK / 8 ? a.K / 8 : RAW_PER * BK / 8);
+  p.raw_rows = static_cast<int>(a.K / 8 < 32 ? a.K / 8 : 32);   // RAW_PER * BK / 8 = 32 in both configurations
   {
     const cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.M};
     const cuuint64_t strides[1] = {(cuuint64_t)a.K * 2};
-    const cuuint32_t box[2] = {BK, BN};
+    const cuuint32_t box[2] = {KS, BN};   // one sub-tile: 64 k (128 bytes) x 256 rows
     e = encode(&p.tm_act, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.workspace, dims, strides, box,
                CU_TENSOR_MAP_SWIZZLE_128B);
     if (e != cudaSuccess) return e;
@@ -595,7 +629,12 @@ cudaError_t run(const W4A8Args& a, int mode, cudaStream_t s) {
   if (total > INT32_MAX) return cudaErrorInvalidConfiguration;
   // persistent: one CTA per SM (the shared-memory rings fill an SM)
   const long long grid = total < sm_count_w4a8() ? total : sm_count_w4a8();
-  w4a8_tc_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, s>>>(p, n_tiles, static_cast<int>(y_tiles));
+  if (experts)
+    w4a8_tc_kernel<1><<<static_cast<unsigned>(grid), kThreads, Cfg<1>::SMEM, s>>>(p, n_tiles,
+                                                                                   static_cast<int>(y_tiles));
+  else
+    w4a8_tc_kernel<2><<<static_cast<unsigned>(grid), kThreads, Cfg<2>::SMEM, s>>>(p, n_tiles,
+                                                                                   static_cast<int>(y_tiles));
   return cudaGetLastError();
 }
 
