@@ -62,9 +62,9 @@ TRAFFIC = {
     # quantize_chunks_kernel<bf16, 16, 2>, N=14336 K=4096 g128 (117,459,456 + 7,766,016; the codes,
     # scales and zeros are still in L2 when the kernel ends), profiles/quantize_groupwise_n14336_k4096_full.md
     "quantize": (125225472, "cf9a6143ae4772be", "tools.cu"),
-    # w4a8_tc_kernel, W4A8 diffusion M=16384 K=N=3072 g=-1 (105,705,216 + 62,773,504),
+    # w4a8_tc_kernel<2>, W4A8 diffusion M=16384 K=N=3072 g=-1 (105,717,248 + 62,809,856),
     # profiles/w4a8_tc_kernel_diffusion_m16384_k3072_n3072_full.md
-    "w4a8_diffusion": (168478720, "9171a7dfc2523964", "w4a8.cu"),
+    "w4a8_diffusion": (168527104, "dfde2f61ad7a7f62", "w4a8.cu"),
 }
 
 
