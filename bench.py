@@ -63,8 +63,9 @@ TRAFFIC = {
     # scales and zeros are still in L2 when the kernel ends), profiles/quantize_groupwise_n14336_k4096_full.md
     "quantize": (125225472, "cf9a6143ae4772be", "tools.cu"),
     # w4a8_tc_kernel<2>, W4A8 diffusion M=16384 K=N=3072 g=-1 (105,717,248 + 62,809,856),
-    # profiles/w4a8_tc_kernel_diffusion_m16384_k3072_n3072_full.md
-    "w4a8_diffusion": (168527104, "dfde2f61ad7a7f62", "w4a8.cu"),
+    # profiles/w4a8_tc_kernel_diffusion_m16384_k3072_n3072_full.md (captured at sha dfde2f61ad7a7f62; the
+    # file has since changed in its header comment only)
+    "w4a8_diffusion": (168527104, "b085096938827044", "w4a8.cu"),
 }
 
 

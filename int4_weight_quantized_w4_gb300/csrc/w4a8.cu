@@ -29,6 +29,10 @@
 //  * the epilogue finally writes y = bf16(s_x[m] * T + bias[n]).
 // Within every 8-wide chunk of k both operands use the order
 // (k0,k4,k1,k5,k2,k6,k3,k7), the order the nibble pairs come out in.
+// One CTA per SM walks its share of the tiles (persistent), every ring
+// counting on across tiles; a k-stage is one 64-k swizzle row (expert mode)
+// or two (dense), so the MMA thread's per-stage waits and commits serve four
+// or eight MMAs.
 #include <cuda.h>
 
 #include "common.cuh"
