@@ -112,6 +112,40 @@ def _cuda2d(t, name, dtypes):
         raise ValueError(f"{name} must have dtype in {dtypes}, got {t.dtype}")
 
 
+def _expect(t, name, shape, dtypes, device, optional=False):
+    """``t`` is read or written through a bare pointer, so the library cannot
+    see its size: it must be a contiguous CUDA tensor on ``device`` with this
+    exact ``shape`` (None: any) and a dtype in ``dtypes`` (None: any)."""
+    if t is None:
+        if optional:
+            return
+        raise ValueError(f"{name} is required")
+    if not (isinstance(t, torch.Tensor) and t.is_cuda and t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, the call runs on {device}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if dtypes is not None and t.dtype not in dtypes:
+        raise ValueError(f"{name} must have dtype in {dtypes}, got {t.dtype}")
+
+
+def _groups(K, group):
+    """Groups along K: 1 for ``group == -1``, ``K / group`` for a group that
+    divides K, None for any other group (the library reports it as
+    W4_ERR_GROUP, so the scale shapes are then not checked here)."""
+    if group == -1:
+        return 1
+    if group > 0 and K % group == 0:
+        return K // group
+    return None
+
+
+_F32, _I32T, _BF16T = (torch.float32,), (torch.int32,), (torch.bfloat16,)
+_SCALE_T = (torch.float16, torch.bfloat16)   # the library rejects what a path does not take
+_FP8_T = (torch.float8_e4m3fn, torch.uint8)
+
+
 def _scale_dtype(t):
     return {torch.float16: W4_FP16, torch.bfloat16: W4_BF16}.get(t.dtype, -1)
 
@@ -125,7 +159,42 @@ def _workspace(ws, op, M, N, K, group, device):
     need = w4_workspace_bytes(op, M, N, K, group)
     if ws is None:
         ws = torch.empty((max(need, 16),), dtype=torch.uint8, device=device)
+    _expect(ws, "workspace", None, None, device)   # the library checks its size in bytes
     return ws, ws.numel() * ws.element_size()
+
+
+def _dense_weight_args(what, qweight, w_scale, K, group, device, zeros=None, bias=None):
+    """GPTQ ``qweight [K/8, N]`` int32, ``w_scale [G, N]``, optional bf16
+    ``zeros [G, N]`` and ``bias [N]``; returns N."""
+    _cuda2d(qweight, "qweight", _I32T)
+    N = qweight.shape[1]
+    if qweight.shape[0] * 8 != K or not isinstance(w_scale, torch.Tensor) or w_scale.dim() != 2 \
+            or w_scale.shape[1] != N:
+        raise ValueError(f"inconsistent shapes for {what}")
+    G = _groups(K, group)
+    gshape = None if G is None else (G, N)
+    _expect(qweight, "qweight", None, None, device)
+    _expect(w_scale, "w_scale", gshape, _SCALE_T, device)
+    _expect(zeros, "zeros", gshape, _BF16T, device, optional=True)
+    _expect(bias, "bias", (N,), _BF16T, device, optional=True)
+    return N
+
+
+def _expert_weight_args(what, qweight, w_scale, expert_offsets, K, group, device):
+    """Compressed-tensors ``qweight [E, N, K/8]`` int32, ``w_scale [E, N, G]``
+    and int32 ``expert_offsets [E + 1]``; returns (E, N)."""
+    if not isinstance(qweight, torch.Tensor) or qweight.dim() != 3 or not qweight.is_contiguous() \
+            or qweight.dtype != torch.int32:
+        raise ValueError("qweight must be a contiguous int32 [E, N, K/8] tensor")
+    E, N = qweight.shape[0], qweight.shape[1]
+    if qweight.shape[2] * 8 != K or not isinstance(w_scale, torch.Tensor) or w_scale.dim() != 3 \
+            or w_scale.shape[:2] != (E, N):
+        raise ValueError(f"inconsistent shapes for {what}")
+    G = _groups(K, group)
+    _expect(qweight, "qweight", None, None, device)
+    _expect(w_scale, "w_scale", None if G is None else (E, N, G), _SCALE_T, device)
+    _expect(expert_offsets, "expert_offsets", (E + 1,), _I32T, device)
+    return E, N
 
 
 def w4_quant_act_per_token(x, q_dtype: str = "int8", q=None, scale=None, stream=None):
@@ -142,8 +211,8 @@ def w4_quant_act_per_token(x, q_dtype: str = "int8", q=None, scale=None, stream=
         raise ValueError("q_dtype must be 'int8' or 'fp8'")
     q = torch.empty((M, K), dtype=tdt, device=x.device) if q is None else q
     scale = torch.empty((M,), dtype=torch.float32, device=x.device) if scale is None else scale
-    if q.shape != (M, K) or scale.shape != (M,):
-        raise ValueError("output shapes do not match x")
+    _expect(q, "q", (M, K), (torch.int8,) if qd == W4_INT8 else _FP8_T, x.device)
+    _expect(scale, "scale", (M,), _F32, x.device)
     xd = W4_FP16 if x.dtype == torch.float16 else W4_BF16
     _check(load().w4_quant_act_per_token(_ptr(x), xd, M, K, qd, _ptr(q), _ptr(scale),
                                          _stream(stream, x.device)), "w4_quant_act_per_token")
@@ -155,12 +224,11 @@ def w4a8_gemm(qx, x_scale, qweight, w_scale, group: int, bias=None, y=None, work
     ``qweight [K/8, N]`` with fp16 ``w_scale [G, N]``; returns bf16 ``y [M, N]``.
     ``workspace`` (bytes from ``w4_workspace_bytes``) is allocated if not given."""
     _cuda2d(qx, "qx", (torch.int8,))
-    _cuda2d(qweight, "qweight", (torch.int32,))
     M, K = qx.shape
-    N = qweight.shape[1]
-    if qweight.shape[0] * 8 != K or x_scale.shape != (M,) or w_scale.dim() != 2 or w_scale.shape[1] != N:
-        raise ValueError("inconsistent shapes for w4a8_gemm")
+    N = _dense_weight_args("w4a8_gemm", qweight, w_scale, K, group, qx.device, bias=bias)
+    _expect(x_scale, "x_scale", (M,), _F32, qx.device)
     y = torch.empty((M, N), dtype=torch.bfloat16, device=qx.device) if y is None else y
+    _expect(y, "y", (M, N), _BF16T, qx.device)
     ws, wsb = _workspace(workspace, W4_OP_W4A8, M, N, K, group, qx.device)
     _check(load().w4a8_gemm(_ptr(qx), _ptr(x_scale), _ptr(qweight), _ptr(w_scale), _scale_dtype(w_scale),
                             group, _ptr(bias), _ptr(y), M, N, K, _ptr(ws), wsb, _stream(stream, qx.device)),
@@ -172,13 +240,12 @@ def w4a8_gemm_bf16in(x, qweight, w_scale, group: int, bias=None, y=None, x_scale
     """W4A8 linear from bf16 ``x [M, K]``: per-token int8 quantization fused into
     the GEMM's activation pass. Returns ``(y bf16 [M, N], x_scale f32 [M])``."""
     _cuda2d(x, "x", (torch.bfloat16,))
-    _cuda2d(qweight, "qweight", (torch.int32,))
     M, K = x.shape
-    N = qweight.shape[1]
-    if qweight.shape[0] * 8 != K or w_scale.dim() != 2 or w_scale.shape[1] != N:
-        raise ValueError("inconsistent shapes for w4a8_gemm_bf16in")
+    N = _dense_weight_args("w4a8_gemm_bf16in", qweight, w_scale, K, group, x.device, bias=bias)
     y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device) if y is None else y
     x_scale = torch.empty((M,), dtype=torch.float32, device=x.device) if x_scale is None else x_scale
+    _expect(y, "y", (M, N), _BF16T, x.device)
+    _expect(x_scale, "x_scale", (M,), _F32, x.device)
     ws, wsb = _workspace(workspace, W4_OP_W4A8, M, N, K, group, x.device)
     _check(load().w4a8_gemm_bf16in(_ptr(x), _ptr(qweight), _ptr(w_scale), _scale_dtype(w_scale), group, _ptr(bias),
                                    _ptr(y), _ptr(x_scale), M, N, K, _ptr(ws), wsb, _stream(stream, x.device)),
@@ -192,12 +259,11 @@ def w4a8_gemm_noalloc(qx, x_scale, qweight, w_scale, group: int, bias=None, y=No
     (M * K <= 16,777,216). Calls that may overlap on the GPU share that
     workspace and must be serialized by the caller."""
     _cuda2d(qx, "qx", (torch.int8,))
-    _cuda2d(qweight, "qweight", (torch.int32,))
     M, K = qx.shape
-    N = qweight.shape[1]
-    if qweight.shape[0] * 8 != K or x_scale.shape != (M,) or w_scale.dim() != 2 or w_scale.shape[1] != N:
-        raise ValueError("inconsistent shapes for w4a8_gemm_noalloc")
+    N = _dense_weight_args("w4a8_gemm_noalloc", qweight, w_scale, K, group, qx.device, bias=bias)
+    _expect(x_scale, "x_scale", (M,), _F32, qx.device)
     y = torch.empty((M, N), dtype=torch.bfloat16, device=qx.device) if y is None else y
+    _expect(y, "y", (M, N), _BF16T, qx.device)
     _check(load().w4a8_gemm_noalloc(_ptr(qx), _ptr(x_scale), _ptr(qweight), _ptr(w_scale), _scale_dtype(w_scale),
                                     group, _ptr(bias), _ptr(y), M, N, K, _stream(stream, qx.device)),
            "w4a8_gemm_noalloc")
@@ -207,11 +273,15 @@ def w4a8_gemm_noalloc(qx, x_scale, qweight, w_scale, group: int, bias=None, y=No
 def w4a8_group_partials(qx, qweight, group: int, out=None, workspace=None, stream=None):
     """Integer group partials ``P [M, G, N]`` (int32) of the W4A8 product."""
     _cuda2d(qx, "qx", (torch.int8,))
-    _cuda2d(qweight, "qweight", (torch.int32,))
+    _cuda2d(qweight, "qweight", _I32T)
     M, K = qx.shape
     N = qweight.shape[1]
-    G = 1 if group == -1 else (K // group if group > 0 else 0)
-    out = torch.empty((M, G, N), dtype=torch.int32, device=qx.device) if out is None else out
+    if qweight.shape[0] * 8 != K:
+        raise ValueError("inconsistent shapes for w4a8_group_partials")
+    _expect(qweight, "qweight", None, None, qx.device)
+    G = _groups(K, group)
+    out = torch.empty((M, G or 0, N), dtype=torch.int32, device=qx.device) if out is None else out
+    _expect(out, "out", None if G is None else (M, G, N), _I32T, qx.device)
     ws, wsb = _workspace(workspace, W4_OP_W4A8, M, N, K, group, qx.device)
     _check(load().w4a8_group_partials(_ptr(qx), _ptr(qweight), group, _ptr(out), M, N, K, _ptr(ws), wsb,
                                       _stream(stream, qx.device)), "w4a8_group_partials")
@@ -222,12 +292,10 @@ def w4a16_gemm(x, qweight, w_scale, group: int, zeros=None, bias=None, y=None, s
     """W4A16 linear: bf16 ``x [M, K]`` times GPTQ ``qweight [K/8, N]`` with fp16
     or bf16 ``w_scale [G, N]`` and optional bf16 ``zeros [G, N]``."""
     _cuda2d(x, "x", (torch.bfloat16,))
-    _cuda2d(qweight, "qweight", (torch.int32,))
     M, K = x.shape
-    N = qweight.shape[1]
-    if qweight.shape[0] * 8 != K or w_scale.dim() != 2 or w_scale.shape[1] != N:
-        raise ValueError("inconsistent shapes for w4a16_gemm")
+    N = _dense_weight_args("w4a16_gemm", qweight, w_scale, K, group, x.device, zeros=zeros, bias=bias)
     y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device) if y is None else y
+    _expect(y, "y", (M, N), _BF16T, x.device)
     _check(load().w4a16_gemm(_ptr(x), _ptr(qweight), _ptr(w_scale), _scale_dtype(w_scale), _ptr(zeros), group,
                              _ptr(bias), _ptr(y), M, N, K, _stream(stream, x.device)), "w4a16_gemm")
     return y
@@ -238,13 +306,16 @@ def w4a16_gemm_host(x_host, x_dev, qweight, w_scale, group: int, y_dev, y_host, 
     ``[M, K]`` CPU tensor) into ``x_dev``, runs the GEMM into ``y_dev`` and copies
     it into ``y_host`` (page-locked bf16 ``[M, N]``), all queued on the stream;
     ``y_host`` is valid once the stream is synchronized."""
-    if x_host.is_cuda or y_host.is_cuda or x_host.dtype != torch.bfloat16 or y_host.dtype != torch.bfloat16:
-        raise ValueError("x_host and y_host must be bf16 CPU tensors")
+    for t, name in ((x_host, "x_host"), (y_host, "y_host")):
+        if not isinstance(t, torch.Tensor) or t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 2 \
+                or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 2-D bf16 CPU tensor")
     _cuda2d(x_dev, "x_dev", (torch.bfloat16,))
     M, K = x_host.shape
-    N = qweight.shape[1]
-    if tuple(x_dev.shape) != (M, K) or tuple(y_host.shape) != (M, N) or tuple(y_dev.shape) != (M, N):
+    N = _dense_weight_args("w4a16_gemm_host", qweight, w_scale, K, group, x_dev.device, zeros=zeros, bias=bias)
+    if tuple(x_dev.shape) != (M, K) or tuple(y_host.shape) != (M, N):
         raise ValueError("inconsistent shapes for w4a16_gemm_host")
+    _expect(y_dev, "y_dev", (M, N), _BF16T, x_dev.device)
     _check(load().w4a16_gemm_host(_ptr(x_host), _ptr(x_dev), _ptr(qweight), _ptr(w_scale), _scale_dtype(w_scale),
                                   _ptr(zeros), group, _ptr(bias), _ptr(y_dev), _ptr(y_host), M, N, K,
                                   _stream(stream, x_dev.device)), "w4a16_gemm_host")
@@ -256,15 +327,12 @@ def w4afp8_moe_grouped_gemm(qx, x_scale, expert_offsets, qweight, w_scale, group
     """Grouped expert linear: e4m3 ``qx [R, K]`` (rows grouped by expert, as
     float8_e4m3fn or uint8 codes), fp32 ``x_scale [R]``, int32 device
     ``expert_offsets [E+1]``, ``qweight [E, N, K/8]``, fp16 ``w_scale [E, N, G]``."""
-    _cuda2d(qx, "qx", (torch.float8_e4m3fn, torch.uint8))
+    _cuda2d(qx, "qx", _FP8_T)
     R, K = qx.shape
-    if qweight.dim() != 3 or not qweight.is_contiguous() or qweight.dtype != torch.int32:
-        raise ValueError("qweight must be a contiguous int32 [E, N, K/8] tensor")
-    E, N = qweight.shape[0], qweight.shape[1]
-    if qweight.shape[2] * 8 != K or expert_offsets.shape != (E + 1,) or x_scale.shape != (R,) \
-            or w_scale.dim() != 3 or w_scale.shape[:2] != (E, N):
-        raise ValueError("inconsistent shapes for w4afp8_moe_grouped_gemm")
+    E, N = _expert_weight_args("w4afp8_moe_grouped_gemm", qweight, w_scale, expert_offsets, K, group, qx.device)
+    _expect(x_scale, "x_scale", (R,), _F32, qx.device)
     y = torch.empty((R, N), dtype=torch.bfloat16, device=qx.device) if y is None else y
+    _expect(y, "y", (R, N), _BF16T, qx.device)
     ws, wsb = _workspace(workspace, W4_OP_W4AFP8_MOE, R, N, K, group, qx.device)
     _check(load().w4afp8_moe_grouped_gemm(_ptr(qx), _ptr(x_scale), _ptr(expert_offsets), E, _ptr(qweight),
                                           _ptr(w_scale), _scale_dtype(w_scale), group, _ptr(y), R, N, K,
@@ -287,6 +355,11 @@ def w4_moe_route(logits, top_k: int, renormalize: bool = False, out=None, worksp
                torch.empty((T * top_k,), dtype=torch.int32, device=dev),
                torch.empty((T, top_k), dtype=torch.int32, device=dev))
     ids, wts, off, rt, ro = out
+    _expect(ids, "topk_ids", (T, top_k), _I32T, dev)
+    _expect(wts, "topk_weights", (T, top_k), _F32, dev)
+    _expect(off, "offsets", (E + 1,), _I32T, dev)
+    _expect(rt, "row_token", (T * top_k,), _I32T, dev)
+    _expect(ro, "row_of", (T, top_k), _I32T, dev)
     ws, wsb = _workspace(workspace, W4_OP_MOE_ROUTE, T, E, 1, 0, dev)
     _check(load().w4_moe_route(_ptr(logits), int(logits.dtype == torch.float32), T, E, top_k, int(bool(renormalize)),
                                _ptr(ids), _ptr(wts), _ptr(off), _ptr(rt), _ptr(ro), _ptr(ws), wsb,
@@ -299,9 +372,12 @@ def w4_moe_gather_quant_fp8(x, row_token, q=None, scale=None, stream=None):
     returns ``(q float8_e4m3fn [R, K], scale fp32 [R])``."""
     _cuda2d(x, "x", (torch.bfloat16,))
     T, K = x.shape
+    _expect(row_token, "row_token", None, _I32T, x.device)
     R = row_token.numel()
     q = torch.empty((R, K), dtype=torch.float8_e4m3fn, device=x.device) if q is None else q
     scale = torch.empty((R,), dtype=torch.float32, device=x.device) if scale is None else scale
+    _expect(q, "q", (R, K), _FP8_T, x.device)
+    _expect(scale, "scale", (R,), _F32, x.device)
     _check(load().w4_moe_gather_quant_fp8(_ptr(x), T, K, _ptr(row_token), R, _ptr(q), _ptr(scale),
                                           _stream(stream, x.device)), "w4_moe_gather_quant_fp8")
     return q, scale
@@ -314,15 +390,13 @@ def w4afp8_moe_gemm_bf16in(x, row_token, expert_offsets, qweight, w_scale, group
     the call. Returns ``(y bf16 [R, N], x_scale fp32 [R])``."""
     _cuda2d(x, "x", (torch.bfloat16,))
     T, K = x.shape
+    _expect(row_token, "row_token", None, _I32T, x.device, optional=True)
     R = T if row_token is None else row_token.numel()
-    if qweight.dim() != 3 or not qweight.is_contiguous() or qweight.dtype != torch.int32:
-        raise ValueError("qweight must be a contiguous int32 [E, N, K/8] tensor")
-    E, N = qweight.shape[0], qweight.shape[1]
-    if qweight.shape[2] * 8 != K or expert_offsets.shape != (E + 1,) or w_scale.dim() != 3 \
-            or w_scale.shape[:2] != (E, N):
-        raise ValueError("inconsistent shapes for w4afp8_moe_gemm_bf16in")
+    E, N = _expert_weight_args("w4afp8_moe_gemm_bf16in", qweight, w_scale, expert_offsets, K, group, x.device)
     y = torch.empty((R, N), dtype=torch.bfloat16, device=x.device) if y is None else y
     x_scale = torch.empty((R,), dtype=torch.float32, device=x.device) if x_scale is None else x_scale
+    _expect(y, "y", (R, N), _BF16T, x.device)
+    _expect(x_scale, "x_scale", (R,), _F32, x.device)
     ws, wsb = _workspace(workspace, W4_OP_W4AFP8_MOE, R, N, K, group, x.device)
     _check(load().w4afp8_moe_gemm_bf16in(_ptr(x), T, _ptr(row_token), _ptr(expert_offsets), E, _ptr(qweight),
                                          _ptr(w_scale), _scale_dtype(w_scale), group, _ptr(y), _ptr(x_scale), R, N,
@@ -336,9 +410,14 @@ def w4_moe_silu_mul_quant_fp8(h, q=None, scale=None, act=None, stream=None):
     activations to ``act`` when given."""
     _cuda2d(h, "h", (torch.bfloat16,))
     R, I2 = h.shape
+    if I2 % 2:
+        raise ValueError("h must hold gate and up halves of equal width")
     I = I2 // 2
     q = torch.empty((R, I), dtype=torch.float8_e4m3fn, device=h.device) if q is None else q
     scale = torch.empty((R,), dtype=torch.float32, device=h.device) if scale is None else scale
+    _expect(q, "q", (R, I), _FP8_T, h.device)
+    _expect(scale, "scale", (R,), _F32, h.device)
+    _expect(act, "act", (R, I), _BF16T, h.device, optional=True)
     _check(load().w4_moe_silu_mul_quant_fp8(_ptr(h), R, I, _ptr(q), _ptr(scale), _ptr(act),
                                             _stream(stream, h.device)), "w4_moe_silu_mul_quant_fp8")
     return q, scale
@@ -349,8 +428,12 @@ def w4_moe_combine(y, topk_weights, row_of, out=None, stream=None):
     returns bf16 ``[T, H]``."""
     _cuda2d(y, "y", (torch.bfloat16,))
     R, H = y.shape
+    _cuda2d(row_of, "row_of", _I32T)
     T, k = row_of.shape
+    _expect(row_of, "row_of", None, None, y.device)
+    _expect(topk_weights, "topk_weights", (T, k), _F32, y.device)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=y.device) if out is None else out
+    _expect(out, "out", (T, H), _BF16T, y.device)
     _check(load().w4_moe_combine(_ptr(y), R, H, _ptr(topk_weights), _ptr(row_of), T, k, _ptr(out),
                                  _stream(stream, y.device)), "w4_moe_combine")
     return out
@@ -365,6 +448,10 @@ def w4_quantize_groupwise(w, group: int, packed=None, scale=None, zero=None, str
     packed = torch.empty((N, K // 2), dtype=torch.uint8, device=w.device) if packed is None else packed
     scale = torch.empty((N, G), dtype=torch.float32, device=w.device) if scale is None else scale
     zero = torch.empty((N, G), dtype=torch.float32, device=w.device) if zero is None else zero
+    _expect(packed, "packed", (N, K // 2), (torch.uint8,), w.device)
+    gshape = (N, G) if _groups(K, group) is not None else None
+    _expect(scale, "scale", gshape, _F32, w.device)
+    _expect(zero, "zero", gshape, _F32, w.device)
     wdt = W4_FP16 if w.dtype == torch.float16 else W4_BF16
     _check(load().w4_quantize_groupwise(_ptr(w), wdt, N, K, group, _ptr(packed), _ptr(scale), _ptr(zero),
                                         _stream(stream, w.device)), "w4_quantize_groupwise")
@@ -385,15 +472,27 @@ def w4_repack_s4_to_uint4b8(src, dst=None, stream=None):
     return dst
 
 
+def _table_args(table, scale, zero, group):
+    """The quantized vocab table: packed uint8 ``[V, D/2]`` with fp32 scale and
+    zero ``[V, G]``. A checkpoint's bf16 scale and zero are widened once with
+    ``.float()`` (exact). Returns (V, D)."""
+    _cuda2d(table, "table", (torch.uint8,))
+    V, D = table.shape[0], table.shape[1] * 2
+    G = _groups(D, group)
+    gshape = None if G is None else (V, G)
+    _expect(scale, "scale", gshape, _F32, table.device)
+    _expect(zero, "zero", gshape, _F32, table.device)
+    return V, D
+
+
 def w4_embedding_gather(ids, table, scale, zero, group: int, out=None, stream=None):
     """Rows ``ids`` (int32 [T]) of the quantized table (packed uint8 [V, D/2],
     f32 scale/zero [V, G]) dequantized to bf16 ``[T, D]``."""
-    if ids.dtype != torch.int32 or not ids.is_cuda:
-        raise ValueError("ids must be a CUDA int32 tensor")
-    _cuda2d(table, "table", (torch.uint8,))
-    V, D = table.shape[0], table.shape[1] * 2
+    V, D = _table_args(table, scale, zero, group)
+    _expect(ids, "ids", None, _I32T, table.device)
     T = ids.numel()
     out = torch.empty((T, D), dtype=torch.bfloat16, device=table.device) if out is None else out
+    _expect(out, "out", (T, D), _BF16T, table.device)
     _check(load().w4_embedding_gather(_ptr(ids), T, _ptr(table), _ptr(scale), _ptr(zero), V, D, group, _ptr(out),
                                       _stream(stream, table.device)), "w4_embedding_gather")
     return out
@@ -403,12 +502,13 @@ def w4_lm_head_gemv(h, table, scale, zero, group: int, y=None, stream=None):
     """Tied output head: bf16 ``h [M, D]`` against the quantized table
     (packed uint8 [V, D/2], f32 scale/zero [V, G]); returns bf16 ``[M, V]``."""
     _cuda2d(h, "h", (torch.bfloat16,))
-    _cuda2d(table, "table", (torch.uint8,))
     M, D = h.shape
-    V = table.shape[0]
-    if table.shape[1] * 2 != D:
+    V, Dt = _table_args(table, scale, zero, group)
+    if Dt != D:
         raise ValueError("table and h disagree on D")
+    _expect(h, "h", None, None, table.device)
     y = torch.empty((M, V), dtype=torch.bfloat16, device=h.device) if y is None else y
+    _expect(y, "y", (M, V), _BF16T, h.device)
     _check(load().w4_lm_head_gemv(_ptr(h), M, _ptr(table), _ptr(scale), _ptr(zero), V, D, group, _ptr(y),
                                   _stream(stream, h.device)), "w4_lm_head_gemv")
     return y
