@@ -511,6 +511,34 @@ def test_silu_mul_quant_round_trip():
     np.testing.assert_array_equal(sc, (am / 448.0).astype(np.float32))
 
 
+def test_moe_gather_quant_follows_row_token():
+    """Row r is token row_token[r], quantized on its own: repeated tokens give
+    identical rows, every nonzero row's largest code is +-448, codes decode to
+    within half an e4m3 step of the token, and a token doubled (exact in
+    bf16) keeps its codes with twice the scale. A gather along the wrong axis,
+    by the wrong index or with a shared scale fails one of these."""
+    T, K = 6, 48
+    x = S.activations_bf16(T, K, seed=17)
+    xf = S.bf16_bits_to_f32(x).astype(np.float64)
+    rt = np.array([4, 0, 4, 5, 2, 0, 1], dtype=np.int32)
+    q, sc = O.moe_gather_quant_fp8(x, rt)
+    assert q.shape == (len(rt), K) and sc.shape == (len(rt),)
+    np.testing.assert_array_equal(q[0], q[2])
+    np.testing.assert_array_equal(q[1], q[5])
+    assert sc[0] == sc[2] and sc[1] == sc[5]
+    d = O.e4m3_decode(q)
+    np.testing.assert_array_equal(np.abs(d).max(axis=1), 448.0)
+    xr = xf[rt]
+    assert np.all(np.abs(d * sc[:, None].astype(np.float64) - xr)
+                  <= np.abs(xr) * 2.0 ** -4 + sc[:, None] * 2.0 ** -9 + 1e-30)
+    x2 = x.copy()
+    x2[4] = S.to_bf16_bits((xf[4] * 2.0).astype(np.float32))
+    q2, sc2 = O.moe_gather_quant_fp8(x2, rt)
+    np.testing.assert_array_equal(q2, q)
+    np.testing.assert_array_equal(sc2[[0, 2]], sc[[0, 2]] * np.float32(2.0))
+    np.testing.assert_array_equal(np.delete(sc2, [0, 2]), np.delete(sc, [0, 2]))
+
+
 def test_moe_combine_bruteforce():
     """k = 1 with weight 1 copies y's rows; in general each output element is
     the k-term weighted sum, computed here one element at a time."""
