@@ -30,9 +30,8 @@
 // Within every 8-wide chunk of k both operands use the order
 // (k0,k4,k1,k5,k2,k6,k3,k7), the order the nibble pairs come out in.
 // One CTA per SM walks its share of the tiles (persistent), every ring
-// counting on across tiles; a k-stage is one 64-k swizzle row (expert mode)
-// or two (dense), so the MMA thread's per-stage waits and commits serve four
-// or eight MMAs.
+// counting on across tiles; a k-stage is two 64-k swizzle rows, so the MMA
+// thread's per-stage waits and commits serve eight MMAs.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -55,9 +54,7 @@ constexpr int B_SUB = BN * KS * 2;      // 32 KB per sub-tile
 // and commits are shared by 4 x SUBS MMAs. Measured on GB300: with the operand
 // producers taken out entirely a 64-k stage still took ~0.8 us (its four MMAs
 // alone ~0.25 us in isolation), and two sub-tiles per stage raised the dense
-// GEMM 12-19%. Dense tiles use two; expert mode keeps one (with two, expert
-// segments that do not fill whole tiles disagreed with the oracle, cause not
-// yet found).
+// GEMM 12-19%. Both modes use two (Cfg<2>).
 template <int SUBS>
 struct Cfg {
   static constexpr int BK = KS * SUBS;                     // k per stage
@@ -308,6 +305,11 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
 #pragma unroll
           for (int kb = 0; kb < kWords; ++kb) w[kb] = raw[(sub * kWords + kb) * BM + tr];
         }
+        // The next asynchronous (TMA) copy into this slot must land after
+        // these generic-proxy reads of it: the proxy fence orders them before
+        // the release below. Without it, expert tiles on two-sub-tile stages
+        // were measured to convert words of the slot's next copy.
+        tc::fence_proxy_async_smem();
         __syncwarp();
         // the copy's words are in registers once its last k-stage is read
         if (sub == RAW_PER - 1 || s == nst - 1) {
@@ -576,9 +578,8 @@ cudaError_t widen(const void* src, void* dst, int64_t rows, int64_t K, bool fp8,
 cudaError_t run(const W4A8Args& a, int mode, cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(w4a8_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<1>::SMEM);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(w4a8_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<2>::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(w4a8_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg<2>::SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -633,12 +634,8 @@ cudaError_t run(const W4A8Args& a, int mode, cudaStream_t s) {
   if (total > INT32_MAX) return cudaErrorInvalidConfiguration;
   // persistent: one CTA per SM (the shared-memory rings fill an SM)
   const long long grid = total < sm_count_w4a8() ? total : sm_count_w4a8();
-  if (experts)
-    w4a8_tc_kernel<1><<<static_cast<unsigned>(grid), kThreads, Cfg<1>::SMEM, s>>>(p, n_tiles,
-                                                                                   static_cast<int>(y_tiles));
-  else
-    w4a8_tc_kernel<2><<<static_cast<unsigned>(grid), kThreads, Cfg<2>::SMEM, s>>>(p, n_tiles,
-                                                                                   static_cast<int>(y_tiles));
+  w4a8_tc_kernel<2><<<static_cast<unsigned>(grid), kThreads, Cfg<2>::SMEM, s>>>(p, n_tiles,
+                                                                                 static_cast<int>(y_tiles));
   return cudaGetLastError();
 }
 
