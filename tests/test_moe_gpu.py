@@ -37,6 +37,19 @@ def test_moe_small(counts, N, K, group):
     check_bf16_output(y, O.moe_grouped_linear(qx8, sx, off, qw, sw, group), f"moe {counts}")
 
 
+@pytest.mark.parametrize("counts,N,K,group", [([5, 0, 40], 128, 32, 32), ([5, 0, 40], 128, 32, -1),
+                                              ([17, 3], 136, 96, 32), ([64] * 8, 192, 384, 128),
+                                              ([33, 100], 128, 384, 48), ([9, 250], 256, 1024, 16)])
+def test_moe_stage_edges(counts, N, K, group):
+    """Expert tiles against the 128-k stages: K shorter than one stage (32,
+    96: most of the stage's MMAs skipped, a packed-word copy narrower than a
+    slot), an odd stage count whose last copy is half used (384), and groups
+    that close inside a stage (48, 16)."""
+    qx8, sx, off, qw, sw = _case(counts, N, K, group, seed=len(counts) + K)
+    y = _run(qx8, sx, off, qw, sw, group)
+    check_bf16_output(y, O.moe_grouped_linear(qx8, sx, off, qw, sw, group), f"moe edges {counts} K={K} g={group}")
+
+
 def test_moe_routed_layer_from_bf16():
     """Seeded top-8 routing of 64 tokens over 16 experts; fp8 quantization on
     the GPU, then the grouped GEMM, against the oracle's quantizer and GEMM."""
