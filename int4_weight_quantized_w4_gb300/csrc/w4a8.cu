@@ -529,15 +529,17 @@ using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, 
                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 cudaError_t get_encoder(EncodeTiled* fn) {
-  static EncodeTiled cached = nullptr;
-  if (cached == nullptr) {
+  // looked up once; a function-local static is initialised once even when
+  // several host threads get here together
+  static const EncodeTiled cached = [] {
     void* f = nullptr;
     cudaDriverEntryPointQueryResult q;
-    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q);
-    if (e != cudaSuccess) return e;
-    if (q != cudaDriverEntryPointSuccess || f == nullptr) return cudaErrorNotSupported;
-    cached = reinterpret_cast<EncodeTiled>(f);
-  }
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<EncodeTiled>(f);
+  }();
+  if (cached == nullptr) return cudaErrorNotSupported;
   *fn = cached;
   return cudaSuccess;
 }
@@ -553,13 +555,13 @@ cudaError_t encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void*
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// SMs of the current device, asked on every call (cheap, and right for
+// whichever device the caller has made current)
 int sm_count_w4a8() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-  }
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      n <= 0)
+    n = 152;
   return n;
 }
 
@@ -576,15 +578,12 @@ cudaError_t widen(const void* src, void* dst, int64_t rows, int64_t K, bool fp8,
 }
 
 cudaError_t run(const W4A8Args& a, int mode, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(w4a8_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg<2>::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  // set on every call: the attribute belongs to the current device, and a
+  // once-per-process flag would race between host threads
+  cudaError_t e = cudaFuncSetAttribute(w4a8_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<2>::SMEM);
+  if (e != cudaSuccess) return e;
   const bool experts = mode == kExperts;
-  cudaError_t e = a.prewidened ? cudaSuccess : widen(a.act, a.workspace, a.M, a.K, experts, s);
+  e = a.prewidened ? cudaSuccess : widen(a.act, a.workspace, a.M, a.K, experts, s);
   if (e != cudaSuccess) return e;
 
   const int n_tiles = static_cast<int>((a.N + BM - 1) / BM);
