@@ -136,8 +136,11 @@ w4_status w4a8_gemm(const void* qx, const float* x_scale, const void* qweight,
  * the process exits. It allocates nothing itself.
  *   - M * K must be at most 16,777,216 (2 bytes of workspace per activation),
  *     else W4_ERR_UNSUPPORTED with a message in w4_last_error().
- *   - The first call on a device looks up the array's device address (with
- *     that device current); make that first call before any stream capture.
+ *   - The array's device address is looked up on the current device, the
+ *     first time the entry point runs in a CUDA context and again whenever the
+ *     current context changes (after a device reset, for instance); make the
+ *     first call on a device before any stream capture. The stream must belong
+ *     to the current device, else W4_ERR_CUDA.
  *   - Every call shares the one array and overwrites it: calls whose kernels
  *     may overlap on the GPU (other streams, other host threads) race and
  *     must be serialized by the caller. Nothing in the array needs to start

@@ -9,6 +9,7 @@ there is no fallback. If ``libw4.so`` has not been built the first call raises.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
@@ -264,9 +265,11 @@ def w4a8_gemm_noalloc(qx, x_scale, qweight, w_scale, group: int, bias=None, y=No
     _expect(x_scale, "x_scale", (M,), _F32, qx.device)
     y = torch.empty((M, N), dtype=torch.bfloat16, device=qx.device) if y is None else y
     _expect(y, "y", (M, N), _BF16T, qx.device)
-    _check(load().w4a8_gemm_noalloc(_ptr(qx), _ptr(x_scale), _ptr(qweight), _ptr(w_scale), _scale_dtype(w_scale),
-                                    group, _ptr(bias), _ptr(y), M, N, K, _stream(stream, qx.device)),
-           "w4a8_gemm_noalloc")
+    # the built-in workspace is looked up on the current device: make qx's current
+    with torch.cuda.device(qx.device) if qx.device.type == "cuda" else contextlib.nullcontext():
+        st = load().w4a8_gemm_noalloc(_ptr(qx), _ptr(x_scale), _ptr(qweight), _ptr(w_scale), _scale_dtype(w_scale),
+                                      group, _ptr(bias), _ptr(y), M, N, K, _stream(stream, qx.device))
+    _check(st, "w4a8_gemm_noalloc")
     return y
 
 

@@ -356,15 +356,7 @@ __global__ void __launch_bounds__(kTcWarps * 32) lm_head_tc_kernel(const uint16_
   }
 }
 
-int sm_count_embed() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-  }
-  return n;
-}
+int sm_count_embed() { return current_sm_count(); }
 
 template <int kM, int kCPL>
 cudaError_t launch_head(const void* h, int Mact, const void* table, const float* scale, const float* zero, int64_t V,

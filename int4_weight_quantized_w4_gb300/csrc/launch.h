@@ -10,6 +10,17 @@
 
 namespace w4 {
 
+// SMs of the current device, asked on every call: the runtime answers from its
+// own cache, the status is checked before the value is used, and the answer
+// is right for whichever device the caller has made current.
+inline int current_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      n <= 0)
+    n = 152;
+  return n;
+}
+
 // Polls a bounded wait makes before it gives up (about a second of spinning).
 constexpr long long kWaitLimit = 1LL << 24;
 

@@ -325,15 +325,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
                       pack_bf16x2(acc[6], acc[7]));
 }
 
-int sm_count_glue() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-  }
-  return n;
-}
+int sm_count_glue() { return current_sm_count(); }
 
 template <int kEPL>
 cudaError_t launch_route_k(const void* logits, bool bf16, int64_t T, int E, int k, bool renorm, int32_t* ids,

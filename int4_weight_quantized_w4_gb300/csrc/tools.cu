@@ -154,15 +154,7 @@ __global__ void __launch_bounds__(256) xor88_kernel(const uint4* src, uint4* dst
   if (blockIdx.x == 0 && static_cast<int>(threadIdx.x) < tail) dst_tail[threadIdx.x] = src_tail[threadIdx.x] ^ 0x88u;
 }
 
-int sm_count_tools() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-  }
-  return n;
-}
+int sm_count_tools() { return current_sm_count(); }
 
 }  // namespace
 

@@ -442,7 +442,11 @@ __global__ void __maxnreg__(120) w4a16_kernel(const __grid_constant__ Params p) 
       }
       // this unit of the tile is consumed; the warp that finishes the stage's
       // last unit refills the slot with stage i + R (the counter only grows:
-      // the last of the four units of round i / R reads 4 (i / R) + 3)
+      // the last of the four units of round i / R reads 4 (i / R) + 3). Every
+      // reading thread orders its generic-proxy reads of the slot before the
+      // asynchronous copy that will overwrite it, before the warp counts the
+      // unit done.
+      tc::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
         asm volatile("fence.acq_rel.cta;" ::: "memory");
@@ -483,34 +487,24 @@ __global__ void __maxnreg__(120) w4a16_kernel(const __grid_constant__ Params p) 
   }
 }
 
-int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-  }
-  return n;
-}
+int sm_count() { return current_sm_count(); }
 
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 EncodeTiled encoder(cudaError_t* err) {
-  static EncodeTiled fn = nullptr;
-  if (fn == nullptr) {
+  // looked up once; a function-local static is initialised once even when
+  // several host threads get here together
+  static const EncodeTiled fn = [] {
     void* f = nullptr;
     cudaDriverEntryPointQueryResult q;
-    *err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q);
-    if (*err != cudaSuccess) return nullptr;
-    if (q != cudaDriverEntryPointSuccess || f == nullptr) {
-      *err = cudaErrorNotSupported;
-      return nullptr;
-    }
-    fn = reinterpret_cast<EncodeTiled>(f);
-  }
-  *err = cudaSuccess;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<EncodeTiled>(f);
+  }();
+  *err = fn == nullptr ? cudaErrorNotSupported : cudaSuccess;
   return fn;
 }
 

@@ -555,15 +555,7 @@ cudaError_t encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void*
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// SMs of the current device, asked on every call (cheap, and right for
-// whichever device the caller has made current)
-int sm_count_w4a8() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-      n <= 0)
-    n = 152;
-  return n;
-}
+int sm_count_w4a8() { return current_sm_count(); }
 
 cudaError_t widen(const void* src, void* dst, int64_t rows, int64_t K, bool fp8, cudaStream_t s) {
   const size_t n16 = (size_t)rows * (size_t)K / 16;

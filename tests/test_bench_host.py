@@ -93,3 +93,26 @@ def test_traffic_reported_only_for_the_captured_source(monkeypatch):
     monkeypatch.setitem(bench.TRAFFIC, "probe", (123, sha, "w4a16.cu"))
     assert bench._traffic("probe") == 123
     assert bench._traffic("no such kernel") is None
+
+
+def test_line_order_and_summary():
+    """The per-row detail leads the line and a compact summary of every row's
+    headline figure ends it, so a reader that keeps only the end of the line
+    still sees the W4A8, MoE and sweep numbers."""
+    line = {"metric": "m", "value": 1.0, "roofline": {"achieved": 3000.0, "frac": 0.44},
+            "rows": {"w4a8_prefill": {"value": 700.0, "gemm_tops": 720.0, "quant_gbs": 4000.0,
+                                      "roofline": {"frac": 0.38}},
+                     "w4a8_prefill_sweep": {"points": {"M512_N4096": {"frac": 0.2}}},
+                     "w4afp8_moe": {"value": 400.0, "gemm_tflops": 450.0, "roofline": {"frac": 0.12}},
+                     "w4a16_sweep": {"points": {"M8_sym_fp16": {"frac": 0.36}}},
+                     "lm_head_gemv": {"value": 3700.0, "roofline": {"frac": 0.55}}},
+            "cpu_baseline": {"value": 0.2}}
+    out = bench.ordered_line(line)
+    keys = list(out)
+    assert keys[0] == "rows" and keys[-1] == "summary" and keys.index("metric") < keys.index("cpu_baseline")
+    sm = out["summary"]
+    assert sm["w4a16_M1"] == {"gbs": 3000.0, "frac": 0.44}
+    assert sm["w4a8_prefill"]["frac"] == 0.38 and sm["w4a8_sweep_frac"] == {"M512_N4096": 0.2}
+    assert sm["w4afp8_moe"]["frac_fp8"] == 0.12 and sm["w4a16_sweep_frac"]["M8_sym_fp16"] == 0.36
+    assert sm["lm_head_gemv"]["frac"] == 0.55
+    assert len(json.dumps(sm)) < 1500

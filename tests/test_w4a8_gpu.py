@@ -168,3 +168,23 @@ def test_w4a8_bf16in_equals_quant_then_gemm(M, N, K, group, outliers):
     assert np.array_equal(bits(y_f), bits(y_u))
     qr, sr = O.quant_int8_per_token(xb)
     check_bf16_output(bits(y_f), O.w4a8_linear(qr, sr, qw, sw, group, bias_bits=bb), f"bf16in M={M}")
+
+
+@pytest.mark.parametrize("M,N,K,group,outliers", [(4096, 11008, 4096, 128, 0.01), (16384, 3072, 3072, -1, 0.0)])
+def test_w4a8_bf16in_full_size(M, N, K, group, outliers):
+    """The fused quantize + GEMM entry point at the sizes the bench times: the
+    prefill shape (K=4096, group 128, 1% outlier channels x20) and the
+    diffusion shape (per-channel scales). Per-token scales bit-exact on every
+    row; outputs on sampled rows (every column) against the oracle's quantizer
+    and GEMM at the parity bar."""
+    g = K if group == -1 else group
+    xb = S.activations_bf16(M, K, seed=0, outlier_frac=outliers)
+    qw = S.random_words((K // 8, N), seed=1)
+    sw = S.scales_f16((K // g, N), seed=2)
+    y, sx = w4.w4a8_gemm_bf16in(bf16(xb), to_dev(qw), to_dev(sw), group)
+    torch.cuda.synchronize()
+    qr, sr = O.quant_int8_per_token(xb)
+    np.testing.assert_array_equal(sx.cpu().numpy().view(np.uint32), sr.view(np.uint32))
+    rows = np.unique(np.concatenate([np.arange(0, M, max(1, M // 40)), [1, M - 2, M - 1]]))
+    check_bf16_output(bits(y)[rows], O.w4a8_linear(qr[rows], sr[rows], qw, sw, group),
+                      f"bf16in full size {M}x{N}x{K}")

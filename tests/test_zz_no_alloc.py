@@ -19,7 +19,7 @@ import torch
 import int4_weight_quantized_w4_gb300 as w4
 import oracle as O
 import synthetic as S
-from _compare import bf16_bits_to_f64, check_bf16_output
+from _compare import check_bf16_output
 from _gpu import bf16, bits, requires_cuda, to_dev
 
 pytestmark = [pytest.mark.gpu, requires_cuda]
@@ -29,7 +29,7 @@ def _inputs(M, N, K, group, seed):
     g = K if group == -1 else group
     xb = S.activations_bf16(M, K, seed=seed, outlier_frac=0.01)
     qx, sx = O.quant_int8_per_token(xb)
-    return (to_dev(qx), to_dev(sx), to_dev(S.random_words((K // 8, N), seed=seed + 1)),
+    return (xb, to_dev(qx), to_dev(sx), to_dev(S.random_words((K // 8, N), seed=seed + 1)),
             to_dev(S.scales_f16((K // g, N), seed=seed + 2)), bf16(S.bias_bf16(N, seed=seed + 3)))
 
 
@@ -45,14 +45,19 @@ def _call_noalloc(lib, qx, sx, qw, sw, group, bias, y):
 def test_noalloc_matches_w4a8_gemm_twice_in_a_row():
     lib = w4.load()
     # two different problems back to back: the second reuses the workspace the
-    # first one filled, so stale contents would show up as a mismatch
+    # first one filled, so stale contents would show up as a mismatch. Both
+    # entry points run the same kernels on the same inputs, so their outputs
+    # must agree bit for bit; both are also held to the oracle's bar.
     for (M, N, K, group, seed) in [(300, 264, 1024, 128, 1), (517, 392, 3072, -1, 2)]:
-        qx, sx, qw, sw, bias = _inputs(M, N, K, group, seed)
+        xb, qx, sx, qw, sw, bias = _inputs(M, N, K, group, seed)
         y = torch.full((M, N), -7.0, dtype=torch.bfloat16, device="cuda")
         assert _call_noalloc(lib, qx, sx, qw, sw, group, bias, y) == w4.W4_OK, lib.w4_last_error()
         ref = w4.w4a8_gemm(qx, sx, qw, sw, group, bias=bias)
         torch.cuda.synchronize()
-        check_bf16_output(bits(y), bf16_bits_to_f64(bits(ref)), f"noalloc vs w4a8_gemm M={M} K={K}")
+        np.testing.assert_array_equal(bits(y), bits(ref), err_msg=f"noalloc vs w4a8_gemm M={M} K={K}")
+        r = O.w4a8_linear(qx.cpu().numpy(), sx.cpu().numpy(), qw.cpu().numpy(), sw.cpu().numpy(), group,
+                          bits(bias))
+        check_bf16_output(bits(y), r, f"noalloc vs oracle M={M} K={K}")
     assert w4.w4_device_status() == w4.W4_OK
 
 
