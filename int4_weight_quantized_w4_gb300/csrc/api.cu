@@ -299,7 +299,8 @@ w4_status w4afp8_moe_grouped_gemm(const void* qx, const float* x_scale, const in
   unsigned int* status = nullptr;
   cudaError_t e = status_ptr(&status);
   if (e != cudaSuccess) return from_cuda(e, "device status word");
-  w4::W4A8Args a{qx, x_scale, qweight, w_scale, nullptr, y, expert_offsets, E, R, N, K, g, false, status, workspace};
+  w4::W4A8Args a{qx, x_scale, qweight, w_scale, nullptr, y, expert_offsets, E, R, N, K, g, false, status, workspace,
+                 false, w4::w4afp8_fp8_path(g)};
   return from_cuda(w4::launch_w4afp8_experts(a, static_cast<cudaStream_t>(stream)), "w4afp8 experts launch");
 }
 
@@ -395,10 +396,13 @@ w4_status w4afp8_moe_gemm_bf16in(const void* x, int64_t T, const int32_t* row_to
   cudaError_t e = status_ptr(&status);
   if (e != cudaSuccess) return from_cuda(e, "device status word");
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  e = w4::launch_quant_gather(x, T, K, row_token, R, true, true, workspace, x_scale, status, s);
-  if (e != cudaSuccess) return from_cuda(e, "gather-quant-widen launch");
-  w4::W4A8Args a{nullptr, x_scale, qweight, w_scale, nullptr, y, expert_offsets, E, R, N, K, g, false, status,
-                 workspace, true};
+  // the fp8 path reads the gathered e4m3 codes from the workspace as they are;
+  // the fp16 path (groups that are not multiples of 32) their widened values
+  const bool fp8 = w4::w4afp8_fp8_path(g);
+  e = w4::launch_quant_gather(x, T, K, row_token, R, true, !fp8, workspace, x_scale, status, s);
+  if (e != cudaSuccess) return from_cuda(e, "gather-quant launch");
+  w4::W4A8Args a{fp8 ? workspace : nullptr, x_scale, qweight, w_scale, nullptr, y, expert_offsets, E, R, N, K, g,
+                 false, status, workspace, !fp8, fp8};
   return from_cuda(w4::launch_w4afp8_experts(a, s), "w4afp8 experts launch");
 }
 

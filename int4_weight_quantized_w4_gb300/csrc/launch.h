@@ -62,12 +62,16 @@ struct W4A8Args {
   unsigned int* status;
   void* workspace;        // fp16 [rows, K]: the activations widened once per call
   bool prewidened;        // the workspace already holds them (act unused)
+  bool fp8_act;           // experts: act holds e4m3 codes [R, K] that the fp8 tensor path reads directly
 };
 size_t w4a8_workspace_bytes(int64_t rows, int64_t K);
 // Sets the calling thread's w4_last_error() message and returns `st`.
 w4_status report_error(w4_status st, const char* msg);
 cudaError_t launch_w4a8_dense(const W4A8Args& a, cudaStream_t s);
 cudaError_t launch_w4afp8_experts(const W4A8Args& a, cudaStream_t s);
+// Expert GEMMs whose (effective) group is a multiple of 32 run on the fp8
+// tensor path (kind::f8f6f4, 32 k per MMA); others widen to fp16 first.
+bool w4afp8_fp8_path(int32_t group);
 
 cudaError_t launch_quantize_groupwise(const void* w, bool f16, int64_t N, int64_t K, int32_t group, uint8_t* packed,
                                       float* scale, float* zero, cudaStream_t s);

@@ -121,8 +121,9 @@ W4_DEV uint64_t sdesc_sw128(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor, kind::f16 with fp16 A and B, fp32 accumulator,
-// both operands K-major, shape M x N.
+// Instruction descriptor with fp32 accumulator, both operands K-major, shape
+// M x N, A and B format code 0: fp16 under kind::f16, e4m3 under
+// kind::f8f6f4.
 constexpr uint32_t idesc_f16_f32(int M, int N) {
   return (1u << 4)                                // D format: f32
          | (0u << 7) | (0u << 10)                 // A, B format: f16
@@ -134,6 +135,15 @@ W4_DEV void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t 
   asm volatile(
       "{.reg .pred p; setp.ne.b32 p, %4, 0; "
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;}"
+      :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+// The same MMA on 8-bit floats (kind::f8f6f4; the formats come from idesc):
+// M x N x 32 per instruction, fp32 accumulator.
+W4_DEV void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{.reg .pred p; setp.ne.b32 p, %4, 0; "
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;}"
       :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
 }
 

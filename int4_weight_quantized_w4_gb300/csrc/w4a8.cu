@@ -43,33 +43,37 @@ namespace {
 
 constexpr int BM = 128;          // outputs per tile (MMA M, TMEM lanes)
 constexpr int BN = 256;          // tokens per tile (MMA N)
-constexpr int KS = 64;           // k per sub-tile (one 128-byte fp16 swizzle row)
-constexpr int UMMA_K = 16;
 constexpr int SEG_MAX = 16384;   // longest accumulation before a drain (exactness bound)
 
-constexpr int A_SUB = BM * KS * 2;      // 16 KB per sub-tile
-constexpr int B_SUB = BN * KS * 2;      // 32 KB per sub-tile
+constexpr int A_SUB = BM * 128;         // 16 KB per sub-tile: one 128-byte swizzle row per output
+constexpr int B_SUB = BN * 128;         // 32 KB per sub-tile: one 128-byte swizzle row per token
 
-// A stage is SUBS sub-tiles of KS k; the MMA thread's per-stage waits, fence
-// and commits are shared by 4 x SUBS MMAs. Measured on GB300: with the operand
-// producers taken out entirely a 64-k stage still took ~0.8 us (its four MMAs
-// alone ~0.25 us in isolation), and two sub-tiles per stage raised the dense
-// GEMM 12-19%. Both modes use two (Cfg<2>).
-template <int SUBS>
+// A sub-tile is one 128-byte swizzle row per operand row: 64 k of fp16 or
+// 128 k of e4m3 (FP8, kind::f8f6f4). An MMA takes 32 bytes of k either way
+// (16 fp16 or 32 e4m3 values), so the descriptor steps are the same and an
+// fp8 stage covers twice the k of an fp16 stage in the same MMA time.
+// A stage is SUBS sub-tiles; the MMA thread's per-stage waits, fence and
+// commits are shared by 4 x SUBS MMAs. Measured on GB300: with the operand
+// producers taken out entirely a 64-k fp16 stage still took ~0.8 us (its four
+// MMAs alone ~0.25 us in isolation), and two sub-tiles per stage raised the
+// dense GEMM 12-19%. Every configuration uses two (Cfg<2, *>).
+template <int SUBS, bool FP8>
 struct Cfg {
+  static constexpr int KS = FP8 ? 128 : 64;               // k per sub-tile
+  static constexpr int UMMA_K = FP8 ? 32 : 16;            // k per MMA
   static constexpr int BK = KS * SUBS;                     // k per stage
   static constexpr int A_STAGES = SUBS == 1 ? 3 : 2;       // converted weight tiles
   static constexpr int B_STAGES = SUBS == 1 ? 4 : 2;       // activation tiles; even: each copy warp keeps its slots
   static constexpr int RAW_STAGES = 2;                     // packed weight words, RAW_PER k-stages per slot
-  static constexpr int RAW_PER = 4 / SUBS;                 // one 16 KB packed-word copy per 256 k
+  static constexpr int RAW_PER = 256 / BK;                 // one 16 KB packed-word copy per 256 k
   static constexpr int A_BYTES = A_SUB * SUBS;
   static constexpr int B_BYTES = B_SUB * SUBS;
-  static constexpr int RAW_BYTES = RAW_PER * BM * BK / 2;  // 16 KB
+  static constexpr int RAW_BYTES = BM * 256 / 2;           // 16 KB: 32 word rows of 128 outputs
   static constexpr int SMEM = B_STAGES * B_BYTES + A_STAGES * A_BYTES + RAW_STAGES * RAW_BYTES + 2048 + 1024;
 };
-static_assert(Cfg<1>::RAW_PER * Cfg<1>::BK / 8 == 32 && Cfg<2>::RAW_PER * Cfg<2>::BK / 8 == 32,
-              "a packed-word copy is 32 word rows in both configurations");
-static_assert(Cfg<1>::SMEM <= 232448 && Cfg<2>::SMEM <= 232448, "shared memory per CTA");
+static_assert(Cfg<2, false>::RAW_PER * Cfg<2, false>::BK == 256 && Cfg<2, true>::RAW_PER * Cfg<2, true>::BK == 256,
+              "a packed-word copy is 32 word rows in every configuration");
+static_assert(Cfg<2, false>::SMEM <= 232448 && Cfg<2, true>::SMEM <= 232448, "shared memory per CTA");
 
 // Warp roles, four warpgroups: 0-7 epilogue (warp w reads TMEM lane quadrant
 // w % 4, token half w / 4), 8-11 converters, 12 weight-word TMA, 13 and 15
@@ -121,6 +125,23 @@ W4_DEV uint4 nibbles_to_f16(uint32_t w) {
   return o;
 }
 
+// Two fp16 values -> two e4m3 codes (low half -> low byte), round to nearest
+// even, saturating; exact for the integers -8..7.
+W4_DEV uint32_t f16x2_to_e4m3x2(uint32_t h) {
+  uint32_t d;
+  asm("{.reg .b16 t; cvt.rn.satfinite.e4m3x2.f16x2 t, %1; cvt.u32.u16 %0, t;}" : "=r"(d) : "r"(h));
+  return d;
+}
+
+// 8 nibbles (k0..k7 of one output) -> the e4m3 codes of q - 8 in natural k
+// order (byte j = k j), the order the caller's e4m3 activations come in.
+W4_DEV uint2 nibbles_to_e4m3(uint32_t w) {
+  const uint4 h = nibbles_to_f16(w);                     // (k0,k4) (k1,k5) (k2,k6) (k3,k7)
+  const uint32_t p01 = prmt(f16x2_to_e4m3x2(h.x), f16x2_to_e4m3x2(h.y), 0x5140u);   // k0 k1 k4 k5
+  const uint32_t p23 = prmt(f16x2_to_e4m3x2(h.z), f16x2_to_e4m3x2(h.w), 0x5140u);   // k2 k3 k6 k7
+  return make_uint2(prmt(p01, p23, 0x5410u), prmt(p01, p23, 0x7632u));
+}
+
 W4_DEV void bar_sync_epilogue() { asm volatile("bar.sync 1, %0;" :: "n"(kEpiWarps * 32) : "memory"); }
 
 // Output tile `tid` of the grid of tiles (N tiles fastest): outputs n0 .. n0 +
@@ -162,10 +183,11 @@ W4_DEV bool decode_tile(const Params& p, int tid, int n_tiles, Tile& t) {
 // operand B, the two TMEM accumulators) keeps counting across tiles, so the
 // copies and conversions of the next tile run while this tile's last groups
 // are multiplied and its output is written.
-template <int SUBS>
+template <int SUBS, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_constant__ Params p, int n_tiles,
                                                               int y_tiles) {
-  using C = Cfg<SUBS>;
+  using C = Cfg<SUBS, FP8>;
+  constexpr int KS = C::KS, UMMA_K = C::UMMA_K;
   constexpr int BK = C::BK, A_STAGES = C::A_STAGES, B_STAGES = C::B_STAGES, RAW_STAGES = C::RAW_STAGES;
   constexpr int RAW_PER = C::RAW_PER, A_BYTES = C::A_BYTES, B_BYTES = C::B_BYTES, RAW_BYTES = C::RAW_BYTES;
   extern __shared__ uint8_t smem_dyn[];
@@ -293,9 +315,14 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
         constexpr int kWords = BK / 8;   // packed words of one output per stage
         uint32_t w[kWords];
         if (p.mode == kExperts) {  // box [128 outputs][raw_rows words]
+          // 32-word rows arrive 128-byte swizzled: 16-byte chunk c of row tr
+          // sits at chunk c ^ (tr % 8), so a quarter-warp's loads hit 8
+          // distinct bank groups
+          const int swz = p.raw_rows == 32 ? (tr & 7) : 0;
 #pragma unroll
           for (int v4 = 0; v4 < kWords / 4; ++v4) {
-            const uint4 q4 = *reinterpret_cast<const uint4*>(raw + tr * p.raw_rows + sub * kWords + 4 * v4);
+            const int c = sub * (kWords / 4) + v4;
+            const uint4 q4 = *reinterpret_cast<const uint4*>(raw + tr * p.raw_rows + 4 * (c ^ swz));
             w[4 * v4] = q4.x;
             w[4 * v4 + 1] = q4.y;
             w[4 * v4 + 2] = q4.z;
@@ -321,9 +348,18 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
           break;
         }
         uint8_t* arow = a_base + a * A_BYTES + tr * 128;
+        if constexpr (FP8) {
 #pragma unroll
-        for (int kb = 0; kb < kWords; ++kb)   // word kb: sub-tile kb / 8, 16-byte chunk kb % 8 of the row
-          *reinterpret_cast<uint4*>(arow + (kb >> 3) * A_SUB + (((kb & 7) ^ (tr & 7)) << 4)) = nibbles_to_f16(w[kb]);
+          for (int kp = 0; kp < kWords / 2; ++kp) {   // words 2kp, 2kp+1: sub-tile kp / 8, chunk kp % 8
+            const uint2 lo = nibbles_to_e4m3(w[2 * kp]), hi = nibbles_to_e4m3(w[2 * kp + 1]);
+            *reinterpret_cast<uint4*>(arow + (kp >> 3) * A_SUB + (((kp & 7) ^ (tr & 7)) << 4)) =
+                make_uint4(lo.x, lo.y, hi.x, hi.y);
+          }
+        } else {
+#pragma unroll
+          for (int kb = 0; kb < kWords; ++kb)   // word kb: sub-tile kb / 8, 16-byte chunk kb % 8 of the row
+            *reinterpret_cast<uint4*>(arow + (kb >> 3) * A_SUB + (((kb & 7) ^ (tr & 7)) << 4)) = nibbles_to_f16(w[kb]);
+        }
         tc::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&a_full[a]);
@@ -335,6 +371,8 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
     // per stage from constant offsets; group boundaries (multiples of 16)
     // may fall inside a stage. Every tile opens a new accumulation.
     if (lane == 0) {
+      // e4m3 A and B under kind::f8f6f4 take the same format code (0) that
+      // fp16 takes under kind::f16, so one instruction descriptor serves both
       constexpr uint32_t idesc = tc::idesc_f16_f32(BM, BN);
       const uint64_t adesc0 = tc::sdesc_sw128(smem_addr(a_base));
       const uint64_t bdesc0 = tc::sdesc_sw128(smem_addr(b_base));
@@ -380,8 +418,12 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
                 acc = 0;
               }
               const int u = j / kPerSub, jj = j % kPerSub;
-              tc::mma_f16(tmem + buf * BN, ad + ((u * A_SUB) >> 4) + 2 * jj, bd + ((u * B_SUB) >> 4) + 2 * jj, idesc,
-                          acc);
+              if constexpr (FP8)
+                tc::mma_f8(tmem + buf * BN, ad + ((u * A_SUB) >> 4) + 2 * jj, bd + ((u * B_SUB) >> 4) + 2 * jj, idesc,
+                           acc);
+              else
+                tc::mma_f16(tmem + buf * BN, ad + ((u * A_SUB) >> 4) + 2 * jj, bd + ((u * B_SUB) >> 4) + 2 * jj,
+                            idesc, acc);
               acc = 1;
             }
           }
@@ -569,14 +611,22 @@ cudaError_t widen(const void* src, void* dst, int64_t rows, int64_t K, bool fp8,
   return cudaGetLastError();
 }
 
-cudaError_t run(const W4A8Args& a, int mode, cudaStream_t s) {
+template <bool FP8>
+cudaError_t run_t(const W4A8Args& a, int mode, cudaStream_t s) {
+  using C = Cfg<2, FP8>;
   // set on every call: the attribute belongs to the current device, and a
   // once-per-process flag would race between host threads
-  cudaError_t e = cudaFuncSetAttribute(w4a8_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<2>::SMEM);
+  cudaError_t e = cudaFuncSetAttribute(w4a8_tc_kernel<2, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const bool experts = mode == kExperts;
-  e = a.prewidened ? cudaSuccess : widen(a.act, a.workspace, a.M, a.K, experts, s);
-  if (e != cudaSuccess) return e;
+  // the activation operand TMA reads: the e4m3 codes themselves (fp8 path),
+  // or the 8-bit codes widened once to exact fp16 in the workspace
+  const void* act = a.act;
+  if (!FP8) {
+    e = a.prewidened ? cudaSuccess : widen(a.act, a.workspace, a.M, a.K, experts, s);
+    if (e != cudaSuccess) return e;
+    act = a.workspace;
+  }
 
   const int n_tiles = static_cast<int>((a.N + BM - 1) / BM);
 
@@ -584,20 +634,24 @@ cudaError_t run(const W4A8Args& a, int mode, cudaStream_t s) {
   memset(&p, 0, sizeof(p));
   // packed-word copies cover RAW_PER k-stages, or all of a short K (expert
   // mode needs K % 32 == 0, so its copy width is a multiple of 16 bytes)
-  p.raw_rows = static_cast<int>(a.K / 8 < 32 ? a.K / 8 : 32);   // RAW_PER * BK / 8 = 32 in both configurations
+  p.raw_rows = static_cast<int>(a.K / 8 < 32 ? a.K / 8 : 32);   // RAW_PER * BK / 8 = 32 in every configuration
   {
+    // one sub-tile: 128 bytes of k (64 fp16 or 128 e4m3 values) x 256 rows
     const cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.M};
-    const cuuint64_t strides[1] = {(cuuint64_t)a.K * 2};
-    const cuuint32_t box[2] = {KS, BN};   // one sub-tile: 64 k (128 bytes) x 256 rows
-    e = encode(&p.tm_act, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.workspace, dims, strides, box,
-               CU_TENSOR_MAP_SWIZZLE_128B);
+    const cuuint64_t strides[1] = {(cuuint64_t)a.K * (FP8 ? 1 : 2)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(C::KS), BN};
+    e = encode(&p.tm_act, FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, act, dims, strides,
+               box, CU_TENSOR_MAP_SWIZZLE_128B);
     if (e != cudaSuccess) return e;
   }
   if (experts) {
+    // rows of 32 words (128 bytes) come 128-byte swizzled, so that the
+    // converter threads, one output row each, read them without bank conflicts
     const cuuint64_t dims[3] = {(cuuint64_t)a.K / 8, (cuuint64_t)a.N, (cuuint64_t)a.E};
     const cuuint64_t strides[2] = {(cuuint64_t)a.K / 8 * 4, (cuuint64_t)a.N * (a.K / 8) * 4};
     const cuuint32_t box[3] = {static_cast<cuuint32_t>(p.raw_rows), BM, 1};
-    e = encode(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_INT32, 3, a.qweight, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+    e = encode(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_INT32, 3, a.qweight, dims, strides, box,
+               p.raw_rows == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
   } else {
     const cuuint64_t dims[2] = {(cuuint64_t)a.N, (cuuint64_t)a.K / 8};
     const cuuint64_t strides[1] = {(cuuint64_t)a.N * 4};
@@ -625,9 +679,13 @@ cudaError_t run(const W4A8Args& a, int mode, cudaStream_t s) {
   if (total > INT32_MAX) return cudaErrorInvalidConfiguration;
   // persistent: one CTA per SM (the shared-memory rings fill an SM)
   const long long grid = total < sm_count_w4a8() ? total : sm_count_w4a8();
-  w4a8_tc_kernel<2><<<static_cast<unsigned>(grid), kThreads, Cfg<2>::SMEM, s>>>(p, n_tiles,
+  w4a8_tc_kernel<2, FP8><<<static_cast<unsigned>(grid), kThreads, C::SMEM, s>>>(p, n_tiles,
                                                                                  static_cast<int>(y_tiles));
   return cudaGetLastError();
+}
+
+cudaError_t run(const W4A8Args& a, int mode, cudaStream_t s) {
+  return (mode == kExperts && a.fp8_act) ? run_t<true>(a, mode, s) : run_t<false>(a, mode, s);
 }
 
 }  // namespace
@@ -639,5 +697,7 @@ cudaError_t launch_w4a8_dense(const W4A8Args& a, cudaStream_t s) {
 }
 
 cudaError_t launch_w4afp8_experts(const W4A8Args& a, cudaStream_t s) { return run(a, kExperts, s); }
+
+bool w4afp8_fp8_path(int32_t group) { return group % 32 == 0; }
 
 }  // namespace w4
