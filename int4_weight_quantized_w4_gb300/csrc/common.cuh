@@ -44,6 +44,21 @@ W4_DEV uint32_t and_xor(uint32_t a, uint32_t b, uint32_t c) {
   return d;
 }
 
+// m ? a : b, bit by bit, as one LOP3.
+W4_DEV uint32_t select_bits(uint32_t m, uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xE4;" : "=r"(d) : "r"(a), "r"(b), "r"(m));
+  return d;
+}
+
+// d0 += a * b0 and d1 += a * b1, two fp32 FMAs (round to nearest) in one
+// packed instruction.
+W4_DEV void fma2(float& d0, float& d1, float a, float b0, float b1) {
+  asm("{.reg .b64 d, x, y; mov.b64 d, {%0, %1}; mov.b64 x, {%2, %2}; mov.b64 y, {%3, %4}; "
+      "fma.rn.f32x2 d, x, y, d; mov.b64 {%0, %1}, d;}"
+      : "+f"(d0), "+f"(d1) : "f"(a), "f"(b0), "f"(b1));
+}
+
 W4_DEV float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 W4_DEV float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 

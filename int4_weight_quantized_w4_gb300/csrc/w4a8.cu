@@ -125,21 +125,22 @@ W4_DEV uint4 nibbles_to_f16(uint32_t w) {
   return o;
 }
 
-// Two fp16 values -> two e4m3 codes (low half -> low byte), round to nearest
-// even, saturating; exact for the integers -8..7.
-W4_DEV uint32_t f16x2_to_e4m3x2(uint32_t h) {
-  uint32_t d;
-  asm("{.reg .b16 t; cvt.rn.satfinite.e4m3x2.f16x2 t, %1; cvt.u32.u16 %0, t;}" : "=r"(d) : "r"(h));
-  return d;
-}
-
-// 8 nibbles (k0..k7 of one output) -> the e4m3 codes of q - 8 in natural k
-// order (byte j = k j), the order the caller's e4m3 activations come in.
+// 8 nibbles (k0..k7 of one output) -> the e4m3 codes of (q - 8) * 2^-9 in
+// natural k order (byte j = k j), the order the caller's e4m3 activations
+// come in. In the lowest binades of e4m3 the code of v * 2^-9 for an integer
+// 0 <= v <= 15 is v itself (subnormals m * 2^-9 for v < 8, then exponent
+// field 1, (8 + m) * 2^-9), so with the sign bit every weight value is one
+// byte: q >= 8 -> q - 8 = q ^ 8; q < 8 -> 0x80 | (8 - q) = 0x88 - q. The
+// epilogue multiplies the group scale by 2^9 (exact) to undo the 2^-9.
 W4_DEV uint2 nibbles_to_e4m3(uint32_t w) {
-  const uint4 h = nibbles_to_f16(w);                     // (k0,k4) (k1,k5) (k2,k6) (k3,k7)
-  const uint32_t p01 = prmt(f16x2_to_e4m3x2(h.x), f16x2_to_e4m3x2(h.y), 0x5140u);   // k0 k1 k4 k5
-  const uint32_t p23 = prmt(f16x2_to_e4m3x2(h.z), f16x2_to_e4m3x2(h.w), 0x5140u);   // k2 k3 k6 k7
-  return make_uint2(prmt(p01, p23, 0x5410u), prmt(p01, p23, 0x7632u));
+  const uint32_t e = w & 0x0F0F0F0Fu;                // k0 k2 k4 k6, one per byte
+  const uint32_t o = (w >> 4) & 0x0F0F0F0Fu;         // k1 k3 k5 k7
+  const uint32_t me = prmt(w << 4, 0u, 0xBA98u);     // 0xFF in the bytes whose q >= 8 (the nibble's bit 3)
+  const uint32_t mo = prmt(w, 0u, 0xBA98u);
+  // bytewise, with no borrow between bytes (q <= 15 < 0x88)
+  const uint32_t ce = select_bits(me, e ^ 0x08080808u, 0x88888888u - e);
+  const uint32_t co = select_bits(mo, o ^ 0x08080808u, 0x88888888u - o);
+  return make_uint2(prmt(ce, co, 0x5140u), prmt(ce, co, 0x7362u));   // k0 k1 k2 k3, k4 k5 k6 k7
 }
 
 W4_DEV void bar_sync_epilogue() { asm volatile("bar.sync 1, %0;" :: "n"(kEpiWarps * 32) : "memory"); }
@@ -150,24 +151,31 @@ W4_DEV void bar_sync_epilogue() { asm volatile("bar.sync 1, %0;" :: "n"(kEpiWarp
 struct Tile {
   int n0, row0, row_end, expert;
 };
-W4_DEV bool decode_tile(const Params& p, int tid, int n_tiles, Tile& t) {
+// Where a role's walk over the experts stands: expert e, and the row tiles of
+// the experts before it. A role visits its tiles in increasing order, so the
+// expert of its next tile is never before the current one: each role reads
+// the offsets once per expert and once per tile, not once per expert per tile.
+struct TileCursor {
+  int e = 0, base = 0;
+};
+W4_DEV bool decode_tile(const Params& p, int tid, int n_tiles, Tile& t, TileCursor& cur) {
   const int nx = tid % n_tiles;
-  int yt = tid / n_tiles;
+  const int yt = tid / n_tiles;
   t.n0 = nx * BM;
   t.expert = 0;
   t.row0 = 0;
   t.row_end = 0;
   if (p.mode == kExperts) {
-    for (int e = 0; e < p.E; ++e) {
-      const int a = p.offsets[e], b = p.offsets[e + 1];
+    for (; cur.e < p.E; ++cur.e) {
+      const int a = p.offsets[cur.e], b = p.offsets[cur.e + 1];
       const int nt = b > a ? (b - a + BN - 1) / BN : 0;
-      if (yt < nt) {
-        t.expert = e;
-        t.row0 = a + yt * BN;
+      if (yt < cur.base + nt) {
+        t.expert = cur.e;
+        t.row0 = a + (yt - cur.base) * BN;
         t.row_end = min(t.row0 + BN, b);
         break;
       }
-      yt -= nt;
+      cur.base += nt;
     }
     t.row0 = max(t.row0, 0);
     t.row_end = min(t.row_end, p.M);
@@ -248,15 +256,16 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
 
   if (warp >= kEpiWarps) {
   // producer warpgroups give registers to the epilogue warpgroups
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 80;");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 72;");
   if (warp == kWarpLoadW) {
     // ---- raw packed weight words -> ring ----
     if (lane == 0) {
       int rg = 0;   // copies issued so far (all tiles)
       bool ok = true;
+      TileCursor cur;
       for (int tid = blockIdx.x; tid < total_tiles && ok; tid += gridDim.x) {
         Tile t;
-        if (!decode_tile(p, tid, n_tiles, t)) continue;
+        if (!decode_tile(p, tid, n_tiles, t, cur)) continue;
         for (int ri = 0; ri < nraw; ++ri, ++rg) {
           const int r = rg % RAW_STAGES;
           if (!tc::wait(&raw_empty[r], ((rg / RAW_STAGES) & 1) ^ 1, abort_flag, p.status, kWaitNs)) {
@@ -279,9 +288,10 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
       const int mine = warp == kWarpLoadB ? 0 : 1;
       int sg = 0;   // stages so far (all tiles)
       bool ok = true;
+      TileCursor cur;
       for (int tid = blockIdx.x; tid < total_tiles && ok; tid += gridDim.x) {
         Tile t;
-        if (!decode_tile(p, tid, n_tiles, t)) continue;
+        if (!decode_tile(p, tid, n_tiles, t, cur)) continue;
         for (int s = 0; s < nst; ++s, ++sg) {
           if ((sg & 1) != mine) continue;
           const int b = sg % B_STAGES;
@@ -301,9 +311,10 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
     const int tr = threadIdx.x - kWarpConv0 * 32;  // output row within the tile
     int sg = 0, rg = 0;
     bool ok = true;
+    TileCursor cur;
     for (int tid = blockIdx.x; tid < total_tiles && ok; tid += gridDim.x) {
       Tile t;
-      if (!decode_tile(p, tid, n_tiles, t)) continue;
+      if (!decode_tile(p, tid, n_tiles, t, cur)) continue;
       for (int s = 0; s < nst; ++s, ++sg) {
         const int sub = s % RAW_PER;   // k-stage within its packed-word copy
         const int r = rg % RAW_STAGES, a = sg % A_STAGES;
@@ -378,9 +389,10 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
       const uint64_t bdesc0 = tc::sdesc_sw128(smem_addr(b_base));
       int seg = -1, buf = 0, sg = 0;
       bool ok = true;
+      TileCursor cur;
       for (int tid = blockIdx.x; tid < total_tiles && ok; tid += gridDim.x) {
         Tile t;
-        if (!decode_tile(p, tid, n_tiles, t)) continue;
+        if (!decode_tile(p, tid, n_tiles, t, cur)) continue;
         ++seg;
         buf = seg & 1;
         int seg_end = min(min(group, SEG_MAX), K);
@@ -437,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
     __syncwarp();
   }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 176;");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 184;");
     // ---- epilogue: warp w owns TMEM lanes 32(w%4).. (outputs), token half w/4 ----
     const int q = warp & 3, half = warp >> 2;
     const int N = p.N;
@@ -449,9 +461,10 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
     // each, even after a wait has run out (ok = false then skips the work):
     // threads that left the loop early would strand the others at bar.sync.
     bool ok = true;
+    TileCursor cur;
     for (int tid = blockIdx.x; tid < total_tiles; tid += gridDim.x) {
       Tile t;
-      if (!decode_tile(p, tid, n_tiles, t)) continue;
+      if (!decode_tile(p, tid, n_tiles, t, cur)) continue;
       const int n = t.n0 + 32 * q + lane;
       const bool n_ok = n < N;
       bar_sync_epilogue();   // the previous tile's output is written: xs_s may change
@@ -504,13 +517,15 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
             }
           }
         } else {
-          const float sc = half_bits_to_f32(sr0);
+          // the fp8 path's weights are (q - 8) 2^-9: 2^9 goes into the scale (exact)
+          const float sc = half_bits_to_f32(sr0) * (FP8 ? 512.f : 1.f);
 #pragma unroll
           for (int cc = 0; cc < kEpiCols / 32; ++cc) {
             uint32_t v[32];
             tc::tmem_ld32(taddr + cc * 32, v);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) T[cc * 32 + j] = fmaf(sc, __uint_as_float(v[j]), T[cc * 32 + j]);
+            for (int j = 0; j < 32; j += 2)
+              fma2(T[cc * 32 + j], T[cc * 32 + j + 1], sc, __uint_as_float(v[j]), __uint_as_float(v[j + 1]));
           }
         }
         tc::fence_before_sync();
@@ -520,13 +535,22 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
       }
 
       if (ok && !partials && !*abort_flag) {
+        // Lanes 2i and 2i+1 hold outputs n and n+1 of the same tokens. For each
+        // pair of tokens (j, j+1) they swap halves, so that the even lane stores
+        // (n, n+1) of token j and the odd lane (n, n+1) of token j+1: one 4-byte
+        // store per two outputs. N is even, so n + 1 < N whenever n < N.
         const float bsv = (p.bias != nullptr && n_ok) ? __uint_as_float(static_cast<uint32_t>(p.bias[n]) << 16) : 0.f;
-        uint16_t* y = static_cast<uint16_t*>(p.out);
+        const int odd = lane & 1;
+        const uint32_t sel = odd ? 0x3276u : 0x5410u;
+        const int row_b = t.row0 + c0 + odd;
+        uint32_t* yp = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) + (size_t)row_b * N + (n & ~1));
 #pragma unroll
-        for (int j = 0; j < kEpiCols; ++j) {
-          const int row = t.row0 + c0 + j;
-          if (n_ok && row < t.row_end)
-            y[(size_t)row * N + n] = static_cast<uint16_t>(f32_to_bf16_bits(fmaf(xs_s[c0 + j], T[j], bsv)));
+        for (int j = 0; j < kEpiCols; j += 2) {
+          const float2 xs2 = *reinterpret_cast<const float2*>(xs_s + c0 + j);
+          const uint32_t v = pack_bf16x2(fmaf(xs2.x, T[j], bsv), fmaf(xs2.y, T[j + 1], bsv));
+          const uint32_t o = prmt(v, __shfl_xor_sync(0xffffffffu, v, 1), sel);
+          if (n_ok && row_b + j < t.row_end) *yp = o;
+          yp += N;   // two rows on
         }
       }
     }
