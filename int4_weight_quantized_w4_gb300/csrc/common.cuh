@@ -132,6 +132,15 @@ W4_DEV uint4 ld_nc_v4(const void* p) {
   return v;
 }
 
+// 16-byte load cached in L2 only: sees data another grid wrote, even one
+// that finished while this grid was already running.
+W4_DEV uint4 ld_cg_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p) : "memory");
+  return v;
+}
+
 W4_DEV uint2 ld_nc_v2(const void* p) {
   uint2 v;
   asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));

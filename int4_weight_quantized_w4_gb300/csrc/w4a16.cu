@@ -243,36 +243,25 @@ __global__ void __maxnreg__(120) w4a16_kernel(const __grid_constant__ Params p) 
   {
     const int K = p.K, group = p.group;
     // ---- prologue, per warp over the x segments it owns (u = warp, warp + 16,
-    // ...): zero what lies past K (nothing here depends on x), then after the
-    // dependency wait copy the segments in, find each token's largest
-    // exponent field E in the segment, which fixes 2^e, e = 14 - (E - 127),
-    // and convert in place ----
-    for (int u = warp; u < nseg; u += kConsumers)
-      for (int m = 0; m < M; ++m) {
-        const int cc = u * kSegChunks + lane;
-        if (cc * 8 >= K) xs[m * xch + cc] = make_uint4(0, 0, 0, 0);
-      }
+    // ...): after the dependency wait each lane loads its 16 bytes of every
+    // token row of the segment straight from global memory (a load through
+    // L2, which sees what the previous kernel wrote; measured on GB300 it lands
+    // ~1 us sooner than a bulk copy queued behind the weight tiles), finds each
+    // token's largest exponent field E in the segment, which fixes 2^e,
+    // e = 14 - (E - 127), and converts ----
     // x (and y) may belong to the previous kernel on the stream
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (lane == 0) {
-      uint32_t bytes = 0;
-      for (int u = warp; u < nseg && u * kUnitK < K; u += kConsumers)
-        bytes += M * 2 * min(kUnitK, K - u * kUnitK);
-      if (bytes > 0) {
-        mbar_arrive_expect_tx(&xbar[warp], bytes);
-        for (int u = warp; u < nseg && u * kUnitK < K; u += kConsumers)
-          for (int m = 0; m < M; ++m)
-            tc::bulk_load(xs + m * xch + u * kSegChunks, p.x + (size_t)m * K + u * kUnitK,
-                          2 * min(kUnitK, K - u * kUnitK), &xbar[warp]);
-      } else {
-        mbar_arrive(&xbar[warp]);
-      }
-    }
-    const bool x_ok = __all_sync(0xffffffffu, tc::wait(&xbar[warp], 0, abort_flag, p.status, kWaitNs));
+    const bool x_ok = true;
     for (int u = warp; u < nseg && x_ok; u += kConsumers) {
       const int cc = u * kSegChunks + lane;
-      for (int m = 0; m < M; ++m) {
-        const uint4 v = xs[m * xch + cc];
+      uint4 xv8[kTok];   // every token's chunk in flight at once
+#pragma unroll
+      for (int m = 0; m < kTok; ++m)
+        xv8[m] = (m < M && cc * 8 < K) ? ld_cg_v4(p.x + (size_t)m * K + cc * 8) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int m = 0; m < kTok; ++m) {
+        if (m >= M) break;
+        const uint4 v = xv8[m];
         const uint32_t h = __vmaxu2(__vmaxu2(v.x & 0x7F807F80u, v.y & 0x7F807F80u),
                                     __vmaxu2(v.z & 0x7F807F80u, v.w & 0x7F807F80u));
         const uint32_t ef = __reduce_max_sync(0xffffffffu, max(h & 0xFFFFu, h >> 16));
