@@ -74,6 +74,8 @@ struct Cfg {
 static_assert(Cfg<2, false>::RAW_PER * Cfg<2, false>::BK == 256 && Cfg<2, true>::RAW_PER * Cfg<2, true>::BK == 256,
               "a packed-word copy is 32 word rows in every configuration");
 static_assert(Cfg<2, false>::SMEM <= 232448 && Cfg<2, true>::SMEM <= 232448, "shared memory per CTA");
+static_assert(Cfg<2, false>::A_STAGES == Cfg<2, false>::B_STAGES && Cfg<2, true>::A_STAGES == Cfg<2, true>::B_STAGES,
+              "one full and one empty barrier serve both operands of a stage");
 
 // Warp roles, four warpgroups: 0-7 epilogue (warp w reads TMEM lane quadrant
 // w % 4, token half w / 4), 8-11 converters, 12 weight-word TMA, 13 and 15
@@ -207,11 +209,12 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
   uint64_t* bars = reinterpret_cast<uint64_t*>(raw_base + RAW_STAGES * RAW_BYTES);
   uint64_t* raw_full = bars;
   uint64_t* raw_empty = raw_full + RAW_STAGES;
-  uint64_t* a_full = raw_empty + RAW_STAGES;
-  uint64_t* a_empty = a_full + A_STAGES;
-  uint64_t* b_full = a_empty + A_STAGES;
-  uint64_t* b_empty = b_full + B_STAGES;
-  uint64_t* acc_full = b_empty + B_STAGES;
+  // one "stage full" barrier per k-stage (the converter warps' arrivals and
+  // the activation copy's bytes) and one "stage empty" barrier (a single
+  // commit of the stage's MMAs, waited on by both producers)
+  uint64_t* st_full = raw_empty + RAW_STAGES;
+  uint64_t* st_empty = st_full + A_STAGES;
+  uint64_t* acc_full = st_empty + A_STAGES;
   uint64_t* acc_empty = acc_full + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
@@ -224,12 +227,8 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
       mbar_init(&raw_empty[i], kConvWarps);
     }
     for (int i = 0; i < A_STAGES; ++i) {
-      mbar_init(&a_full[i], kConvWarps);
-      mbar_init(&a_empty[i], 1);
-    }
-    for (int i = 0; i < B_STAGES; ++i) {
-      mbar_init(&b_full[i], 1);
-      mbar_init(&b_empty[i], 1);
+      mbar_init(&st_full[i], kConvWarps + 1);
+      mbar_init(&st_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
@@ -295,14 +294,14 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
         for (int s = 0; s < nst; ++s, ++sg) {
           if ((sg & 1) != mine) continue;
           const int b = sg % B_STAGES;
-          if (!tc::wait(&b_empty[b], ((sg / B_STAGES) & 1) ^ 1, abort_flag, p.status, kWaitNs)) {
+          if (!tc::wait(&st_empty[b], ((sg / B_STAGES) & 1) ^ 1, abort_flag, p.status, kWaitNs)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&b_full[b], B_BYTES);
+          mbar_arrive_expect_tx(&st_full[b], B_BYTES);
 #pragma unroll
           for (int u = 0; u < SUBS; ++u)   // sub-tiles past K land as zeros
-            tc::tma_load_2d(b_base + b * B_BYTES + u * B_SUB, &p.tm_act, &b_full[b], s * BK + u * KS, t.row0);
+            tc::tma_load_2d(b_base + b * B_BYTES + u * B_SUB, &p.tm_act, &st_full[b], s * BK + u * KS, t.row0);
         }
       }
     }
@@ -354,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
           if (lane == 0) mbar_arrive(&raw_empty[r]);
           ++rg;
         }
-        if (!tc::wait(&a_empty[a], ((sg / A_STAGES) & 1) ^ 1, abort_flag, p.status, kWaitNs)) {
+        if (!tc::wait(&st_empty[a], ((sg / A_STAGES) & 1) ^ 1, abort_flag, p.status, kWaitNs)) {
           ok = false;
           break;
         }
@@ -373,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
         }
         tc::fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&a_full[a]);
+        if (lane == 0) mbar_arrive(&st_full[a]);
       }
     }
   } else if (warp == kWarpMma) {
@@ -401,8 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
         tc::fence_after_sync();
         for (int s = 0; s < nst && ok; ++s, ++sg) {
           const int a = sg % A_STAGES, b = sg % B_STAGES;
-          if (!tc::wait(&b_full[b], (sg / B_STAGES) & 1, abort_flag, p.status, kWaitNs, 200) ||
-              !tc::wait(&a_full[a], (sg / A_STAGES) & 1, abort_flag, p.status, kWaitNs, 200)) {
+          if (!tc::wait(&st_full[a], (sg / A_STAGES) & 1, abort_flag, p.status, kWaitNs, 200)) {
             ok = false;
             break;
           }
@@ -440,8 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
             }
           }
           if (!ok) break;
-          tc::commit(&a_empty[a]);
-          tc::commit(&b_empty[b]);
+          tc::commit(&st_empty[a]);
         }
         if (ok) tc::commit(&acc_full[buf]);
       }
