@@ -114,6 +114,31 @@ W4_DEV uint4 widen_e4m3(uint32_t u0, uint32_t u1) {
 }
 
 // ---------------------------------------------------------------------------
+// per-token quantization: the codes of the IEEE quotient fl(x / s)
+// ---------------------------------------------------------------------------
+
+W4_DEV uint32_t e4m3x2_rn(float lo, float hi) {
+  uint16_t c;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c) : "f"(hi), "f"(lo));
+  return c;
+}
+
+// The e4m3 codes (satfinite, round to nearest even) of fl(xl / s) and
+// fl(xh / s), lo in the low byte, given r = fl(1 / s). y = x r differs from
+// x / s by at most |x / s| (2^-23 + 2^-48) and fl(x / s) from x / s by at most
+// |x / s| 2^-24, so fl(x / s) lies inside [y (1 - 2^-20), y (1 + 2^-20)], even
+// with both ends rounded to fp32. e4m3 rounding is monotone: when both ends of
+// the bracket give the same code, that is the code of fl(x / s); otherwise the
+// IEEE divide decides (values within about 2^-20 of a rounding boundary).
+W4_DEV uint32_t e4m3x2_of_quotient(float xl, float xh, float s, float r) {
+  const float yl = xl * r, yh = xh * r;
+  const uint32_t a = e4m3x2_rn(yl * 0.99999904632568359375f, yh * 0.99999904632568359375f);
+  const uint32_t b = e4m3x2_rn(yl * 1.00000095367431640625f, yh * 1.00000095367431640625f);
+  if (a == b) return a;
+  return e4m3x2_rn(__fdiv_rn(xl, s), __fdiv_rn(xh, s));
+}
+
+// ---------------------------------------------------------------------------
 // global memory access
 // ---------------------------------------------------------------------------
 

@@ -229,11 +229,9 @@ W4_DEV float chunk_absmax_bf16(const uint4& v) {
   return m;
 }
 
-W4_DEV uint32_t e4m3_pair(uint32_t w, float s) {
-  const float lo = __fdiv_rn(bf16_lo(w), s), hi = __fdiv_rn(bf16_hi(w), s);
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
+// The e4m3 codes of fl(x / s) for the two activations of a word (r = fl(1 / s)).
+W4_DEV uint32_t e4m3_pair(uint32_t w, float s, float r) {
+  return e4m3x2_of_quotient(bf16_lo(w), bf16_hi(w), s, r);
 }
 
 // One CTA per row; NCH chunks of 8 per thread kept in registers (NCH == 0:
@@ -257,9 +255,10 @@ __global__ void __launch_bounds__(kActThreads) silu_mul_quant_kernel(const uint4
     return r;
   };
   auto store = [&](size_t i, const uint4& a, float s) {
+    const float r = __frcp_rn(s);
     uint2 c;
-    c.x = e4m3_pair(a.x, s) | (e4m3_pair(a.y, s) << 16);
-    c.y = e4m3_pair(a.z, s) | (e4m3_pair(a.w, s) << 16);
+    c.x = e4m3_pair(a.x, s, r) | (e4m3_pair(a.y, s, r) << 16);
+    c.y = e4m3_pair(a.z, s, r) | (e4m3_pair(a.w, s, r) << 16);
     q[o0 + i] = c;
     if (act != nullptr) act[o0 + i] = a;
   };

@@ -57,36 +57,44 @@ W4_DEV float chunk_absmax(const uint4& v) {
   return m;
 }
 
-W4_DEV uint32_t q_int8(float x, float s) {
-  int q = __float2int_rn(__fdiv_rn(x, s));
-  q = max(-127, min(127, q));
-  return static_cast<uint32_t>(q) & 0xFFu;
+// The codes are those of the IEEE quotient fl(x / s), taken from y = x * r
+// with r = fl(1 / s), the correctly rounded reciprocal. y and x / s differ by
+// at most |x / s| (2^-23 + 2^-48) and fl(x / s) is within |x / s| 2^-24 of
+// x / s, so for |x / s| <= 127.0001 (int8: |x| <= amax, s = fl(amax / 127))
+// |y - fl(x / s)| <= 2.3e-5 < 2^-15. Where y is more than 2^-15 from every
+// half-integer, y and fl(x / s) round to the same integer; nearer than that
+// the quotient is formed with the IEEE divide itself (a few elements per row
+// at most).
+W4_DEV uint32_t q_int8(float x, float s, float r) {
+  const float y = x * r;
+  float q = rintf(y);
+  if (fabsf(0.5f - fabsf(y - q)) < 3.0517578125e-5f) q = rintf(__fdiv_rn(x, s));
+  q = fmaxf(-127.f, fminf(127.f, q));
+  return static_cast<uint32_t>(static_cast<int>(q)) & 0xFFu;
 }
 
 // Two int8 codes from one word of two activations, low element in the low byte.
 template <bool kF16>
-W4_DEV uint32_t q_int8_pair(uint32_t w, float s) {
-  return q_int8(act_lo<kF16>(w), s) | (q_int8(act_hi<kF16>(w), s) << 8);
+W4_DEV uint32_t q_int8_pair(uint32_t w, float s, float r) {
+  return q_int8(act_lo<kF16>(w), s, r) | (q_int8(act_hi<kF16>(w), s, r) << 8);
 }
 
-// Two e4m3 codes from one word of two activations, low element in the low byte.
+// Two e4m3 codes from one word of two activations, low element in the low
+// byte: the codes of fl(x / s) (e4m3x2_of_quotient).
 template <bool kF16>
-W4_DEV uint32_t q_e4m3_pair(uint32_t w, float s) {
-  const float lo = __fdiv_rn(act_lo<kF16>(w), s), hi = __fdiv_rn(act_hi<kF16>(w), s);
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
+W4_DEV uint32_t q_e4m3_pair(uint32_t w, float s, float r) {
+  return e4m3x2_of_quotient(act_lo<kF16>(w), act_hi<kF16>(w), s, r);
 }
 
 template <bool FP8, bool kF16>
-W4_DEV uint2 quant_chunk(const uint4& v, float s) {
+W4_DEV uint2 quant_chunk(const uint4& v, float s, float r) {
   uint2 o;
   if (FP8) {
-    o.x = q_e4m3_pair<kF16>(v.x, s) | (q_e4m3_pair<kF16>(v.y, s) << 16);
-    o.y = q_e4m3_pair<kF16>(v.z, s) | (q_e4m3_pair<kF16>(v.w, s) << 16);
+    o.x = q_e4m3_pair<kF16>(v.x, s, r) | (q_e4m3_pair<kF16>(v.y, s, r) << 16);
+    o.y = q_e4m3_pair<kF16>(v.z, s, r) | (q_e4m3_pair<kF16>(v.w, s, r) << 16);
   } else {
-    o.x = q_int8_pair<kF16>(v.x, s) | (q_int8_pair<kF16>(v.y, s) << 16);
-    o.y = q_int8_pair<kF16>(v.z, s) | (q_int8_pair<kF16>(v.w, s) << 16);
+    o.x = q_int8_pair<kF16>(v.x, s, r) | (q_int8_pair<kF16>(v.y, s, r) << 16);
+    o.y = q_int8_pair<kF16>(v.z, s, r) | (q_int8_pair<kF16>(v.w, s, r) << 16);
   }
   return o;
 }
@@ -94,8 +102,8 @@ W4_DEV uint2 quant_chunk(const uint4& v, float s) {
 // The codes of one 8-chunk as stored: 8 bytes, or (kWiden) the exact fp16
 // values of the codes in the W4A8 operand order (16 bytes).
 template <bool FP8, bool kWiden, bool kF16>
-W4_DEV void store_chunk(void* q, size_t i, const uint4& v, float s) {
-  const uint2 c = quant_chunk<FP8, kF16>(v, s);
+W4_DEV void store_chunk(void* q, size_t i, const uint4& v, float s, float r) {
+  const uint2 c = quant_chunk<FP8, kF16>(v, s, r);
   if (kWiden)
     static_cast<uint4*>(q)[i] = FP8 ? widen_e4m3(c.x, c.y) : widen_i8(c.x, c.y);
   else
@@ -145,10 +153,11 @@ __global__ void __launch_bounds__(kMaxThreads) quant_rows(const uint4* __restric
     }
     const float amax = row_max(m, red);
     const float s = (amax == 0.f) ? 1.f : __fdiv_rn(amax, kQ);
+    const float r = __frcp_rn(s);
 #pragma unroll
     for (int c = 0; c < NCH; ++c) {
       const int i = threadIdx.x + c * blockDim.x;
-      if (i < K8) store_chunk<FP8, kWiden, kF16>(q, q0 + i, v[c], s);
+      if (i < K8) store_chunk<FP8, kWiden, kF16>(q, q0 + i, v[c], s, r);
     }
     if (threadIdx.x == 0) scale[row] = s;
   } else {
@@ -156,8 +165,9 @@ __global__ void __launch_bounds__(kMaxThreads) quant_rows(const uint4* __restric
     for (int i = threadIdx.x; i < K8; i += blockDim.x) m = fmaxf(m, chunk_absmax<kF16>(ld_nc_v4(xr + i)));
     const float amax = row_max(m, red);
     const float s = (amax == 0.f) ? 1.f : __fdiv_rn(amax, kQ);
+    const float r = __frcp_rn(s);
     for (int i = threadIdx.x; i < K8; i += blockDim.x)
-      store_chunk<FP8, kWiden, kF16>(q, q0 + i, ld_stream_v4(xr + i), s);
+      store_chunk<FP8, kWiden, kF16>(q, q0 + i, ld_stream_v4(xr + i), s, r);
     if (threadIdx.x == 0) scale[row] = s;
   }
 }

@@ -86,3 +86,48 @@ def test_quant_fp16_activations(kind, M, K):
     if M > 1:
         x[1] = 0
     _check_f16(x, kind)
+
+
+def _near_boundaries(kind, rows=64, K=4096, seed=3):
+    """Rows whose values sit on or next to the quantizer's rounding
+    boundaries: the bf16 values nearest to (k + 1/2) s for int8, or to the
+    midpoints between neighbouring e4m3 values times s for e4m3, with a row
+    maximum that makes s a non-power-of-two (so x / s is not exact)."""
+    rng = np.random.default_rng(seed)
+    Q = 127.0 if kind == "int8" else 448.0
+    out = np.empty((rows, K), np.float32)
+    for i in range(rows):
+        amax = np.float32(rng.uniform(0.3, 40.0))
+        s = np.float32(amax / np.float32(Q))
+        if kind == "int8":
+            mids = (rng.integers(-127, 127, K) + 0.5) * np.float64(s)
+        else:
+            vals = np.sort(np.unique(np.abs(O.e4m3_decode(np.arange(256, dtype=np.uint8)))))
+            vals = vals[np.isfinite(vals) & (vals <= 448)]
+            j = rng.integers(0, len(vals) - 1, K)
+            mids = (vals[j] + vals[j + 1]) / 2 * np.sign(rng.standard_normal(K)) * np.float64(s)
+        # nudge some by one bf16 step either way so both sides of each boundary occur
+        b = S.to_bf16_bits(mids.astype(np.float32))
+        nudge = rng.integers(-1, 2, K).astype(np.int32)
+        b = (b.astype(np.int32) + nudge * (b != 0)).astype(np.uint16)
+        row = S.bf16_bits_to_f32(b)
+        row[0] = amax
+        out[i] = np.clip(row, -amax, amax)
+    return S.to_bf16_bits(out)
+
+
+@pytest.mark.parametrize("kind", ["int8", "fp8"])
+def test_quant_near_rounding_boundaries_bit_exact(kind):
+    """The codes come from x * fl(1/s) with the IEEE divide taking over near a
+    rounding boundary; on values packed around the boundaries every code and
+    scale must still equal the IEEE-quotient codes of the oracle."""
+    xb = _near_boundaries(kind)
+    q, s = w4.w4_quant_act_per_token(bf16(xb), kind)
+    torch.cuda.synchronize()
+    if kind == "int8":
+        rq, rs = O.quant_int8_per_token(xb)
+        np.testing.assert_array_equal(q.cpu().numpy(), rq)
+    else:
+        rq, rs = O.quant_fp8_per_token(xb)
+        np.testing.assert_array_equal(q.view(torch.uint8).cpu().numpy(), rq)
+    np.testing.assert_array_equal(s.cpu().numpy().view(np.uint32), rs.view(np.uint32))
