@@ -77,11 +77,16 @@ typedef enum {
 
 /*
  * Bytes of device workspace an operation needs for M activation rows of
- * length K (N and group do not change it today but are part of the query).
- * The tensor-core GEMMs first widen the 8-bit activations once into exact
- * fp16 in this workspace, so that every output tile streams them with TMA
- * instead of converting them again. The caller allocates it (16-byte
- * aligned); its contents on entry do not matter and are overwritten.
+ * length K. The tensor-core GEMMs first widen the 8-bit activations once into
+ * exact fp16 in this workspace (M * K * 2 bytes), so that every output tile
+ * streams them with TMA instead of converting them again. For W4_OP_W4A8 the
+ * figure also depends on N and the group: when the M x N output tiles would
+ * fill the GPU's SMs poorly, the GEMM splits K into up to 4 parts, and the
+ * workspace then also holds the parts' fp32 partial sums (parts * M * N * 4
+ * bytes after the widened activations). A W4A8 workspace of only M * K * 2
+ * bytes is still accepted; the GEMM then runs unsplit. The caller allocates
+ * the workspace (16-byte aligned); its contents on entry do not matter and
+ * are overwritten.
  */
 size_t w4_workspace_bytes(int32_t op, int64_t M, int64_t N, int64_t K, int32_t group);
 

@@ -118,10 +118,14 @@ w4_status w4_quant_act_per_token(const void* x, int32_t x_dtype, int64_t M, int6
 }
 
 size_t w4_workspace_bytes(int32_t op, int64_t M, int64_t N, int64_t K, int32_t group) {
-  (void)N;
-  (void)group;
   if (M <= 0 || K <= 0) return 0;
-  if (op == W4_OP_W4A8 || op == W4_OP_W4AFP8_MOE) return w4::w4a8_workspace_bytes(M, K);
+  if (op == W4_OP_W4A8) {
+    // room for split-K partial sums too when this shape would be split
+    const int64_t g = group == -1 ? K : group;
+    if (N > 0 && N % 8 == 0 && g > 0 && K % g == 0) return w4::w4a8_workspace_bytes_split(M, N, K, static_cast<int32_t>(g));
+    return w4::w4a8_workspace_bytes(M, K);
+  }
+  if (op == W4_OP_W4AFP8_MOE) return w4::w4a8_workspace_bytes(M, K);
   if (op == W4_OP_MOE_ROUTE) return (N > 0 && N <= 1024) ? w4::moe_route_workspace_bytes(M, static_cast<int32_t>(N)) : 0;
   return 0;
 }
@@ -159,7 +163,7 @@ static w4_status w4a8_common(const void* qx, const float* x_scale, const void* q
   cudaError_t e = status_ptr(&status);
   if (e != cudaSuccess) return from_cuda(e, "device status word");
   w4::W4A8Args a{qx, x_scale, qweight, w_scale, partials ? nullptr : bias, out, nullptr, 1, M, N, K, g, partials,
-                 status, workspace};
+                 status, workspace, false, false, workspace_bytes};
   return from_cuda(w4::launch_w4a8_dense(a, static_cast<cudaStream_t>(stream)), "w4a8 launch");
 }
 
@@ -195,7 +199,8 @@ w4_status w4a8_gemm_bf16in(const void* x, const void* qweight, const void* w_sca
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   e = w4::launch_quant_widen(x, M, K, false, workspace, x_scale, s);
   if (e != cudaSuccess) return from_cuda(e, "quantize-and-widen launch");
-  w4::W4A8Args a{nullptr, x_scale, qweight, w_scale, bias, y, nullptr, 1, M, N, K, g, false, status, workspace, true};
+  w4::W4A8Args a{nullptr, x_scale, qweight, w_scale, bias, y, nullptr, 1, M, N, K, g, false, status, workspace, true,
+                 false, workspace_bytes};
   return from_cuda(w4::launch_w4a8_dense(a, s), "w4a8 launch");
 }
 

@@ -63,8 +63,13 @@ struct W4A8Args {
   void* workspace;        // fp16 [rows, K]: the activations widened once per call
   bool prewidened;        // the workspace already holds them (act unused)
   bool fp8_act;           // experts: act holds e4m3 codes [R, K] that the fp8 tensor path reads directly
+  size_t workspace_bytes; // dense y: a workspace this large may also hold split-K partial sums
 };
 size_t w4a8_workspace_bytes(int64_t rows, int64_t K);
+// The dense W4A8 workspace with room for the split-K partial sums that
+// M x N x K at this group would use (fp32 [splits][M][N] after the widened
+// activations); equal to w4a8_workspace_bytes when the GEMM is not split.
+size_t w4a8_workspace_bytes_split(int64_t M, int64_t N, int64_t K, int32_t group);
 // Sets the calling thread's w4_last_error() message and returns `st`.
 w4_status report_error(w4_status st, const char* msg);
 cudaError_t launch_w4a8_dense(const W4A8Args& a, cudaStream_t s);

@@ -109,6 +109,9 @@ struct Params {
   const int32_t* offsets;  // [E + 1] (experts)
   int E, M, N, K, group, mode;
   int raw_rows;            // word rows (k / 8) per packed-word copy: min(32, K / 8)
+  int m_tiles;             // row tiles (dense: ceil(M / 256); experts: an upper bound over all segments)
+  int splits, ksplit;      // dense y: the K range cut into `splits` parts of `ksplit` (the last may be shorter)
+  float* part;             // splits > 1: fp32 partial sums [splits][M][N], before x_scale and bias
   unsigned int* status;
 };
 
@@ -152,6 +155,7 @@ W4_DEV void bar_sync_epilogue() { asm volatile("bar.sync 1, %0;" :: "n"(kEpiWarp
 // the tile holds no rows. Every role decodes the same tiles the same way.
 struct Tile {
   int n0, row0, row_end, expert;
+  int k0, k1, split;   // the tile's k range (all of K unless the GEMM is split along K)
 };
 // Where a role's walk over the experts stands: expert e, and the row tiles of
 // the experts before it. A role visits its tiles in increasing order, so the
@@ -162,11 +166,20 @@ struct TileCursor {
 };
 W4_DEV bool decode_tile(const Params& p, int tid, int n_tiles, Tile& t, TileCursor& cur) {
   const int nx = tid % n_tiles;
-  const int yt = tid / n_tiles;
+  int yt = tid / n_tiles;
   t.n0 = nx * BM;
   t.expert = 0;
   t.row0 = 0;
   t.row_end = 0;
+  t.split = 0;
+  t.k0 = 0;
+  t.k1 = p.K;
+  if (p.splits > 1) {   // dense only: N tiles fastest, then row tiles, then splits
+    t.split = yt / p.m_tiles;
+    yt %= p.m_tiles;
+    t.k0 = t.split * p.ksplit;
+    t.k1 = min(p.K, t.k0 + p.ksplit);
+  }
   if (p.mode == kExperts) {
     for (; cur.e < p.E; ++cur.e) {
       const int a = p.offsets[cur.e], b = p.offsets[cur.e + 1];
@@ -248,8 +261,6 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
   const uint32_t tmem = *tmem_holder;
 
   const int K = p.K;
-  const int nst = (K + BK - 1) / BK;
-  const int nraw = (nst + RAW_PER - 1) / RAW_PER;
   const int group = p.group;
   const int total_tiles = n_tiles * y_tiles;
 
@@ -265,6 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
       for (int tid = blockIdx.x; tid < total_tiles && ok; tid += gridDim.x) {
         Tile t;
         if (!decode_tile(p, tid, n_tiles, t, cur)) continue;
+        const int nraw = ((t.k1 - t.k0 + BK - 1) / BK + RAW_PER - 1) / RAW_PER;
         for (int ri = 0; ri < nraw; ++ri, ++rg) {
           const int r = rg % RAW_STAGES;
           if (!tc::wait(&raw_empty[r], ((rg / RAW_STAGES) & 1) ^ 1, abort_flag, p.status, kWaitNs)) {
@@ -272,11 +284,11 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
             break;
           }
           mbar_arrive_expect_tx(&raw_full[r], static_cast<uint32_t>(p.raw_rows * BM * 4));
+          const int wrow = t.k0 / 8 + ri * RAW_PER * (BK / 8);   // first word row of the copy
           if (p.mode == kExperts)
-            tc::tma_load_3d(raw_base + r * RAW_BYTES, &p.tm_w, &raw_full[r], ri * RAW_PER * (BK / 8), t.n0,
-                            t.expert);
+            tc::tma_load_3d(raw_base + r * RAW_BYTES, &p.tm_w, &raw_full[r], wrow, t.n0, t.expert);
           else
-            tc::tma_load_2d(raw_base + r * RAW_BYTES, &p.tm_w, &raw_full[r], t.n0, ri * RAW_PER * (BK / 8));
+            tc::tma_load_2d(raw_base + r * RAW_BYTES, &p.tm_w, &raw_full[r], t.n0, wrow);
         }
       }
     }
@@ -291,6 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
       for (int tid = blockIdx.x; tid < total_tiles && ok; tid += gridDim.x) {
         Tile t;
         if (!decode_tile(p, tid, n_tiles, t, cur)) continue;
+        const int nst = (t.k1 - t.k0 + BK - 1) / BK;
         for (int s = 0; s < nst; ++s, ++sg) {
           if ((sg & 1) != mine) continue;
           const int b = sg % B_STAGES;
@@ -301,7 +314,8 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
           mbar_arrive_expect_tx(&st_full[b], B_BYTES);
 #pragma unroll
           for (int u = 0; u < SUBS; ++u)   // sub-tiles past K land as zeros
-            tc::tma_load_2d(b_base + b * B_BYTES + u * B_SUB, &p.tm_act, &st_full[b], s * BK + u * KS, t.row0);
+            tc::tma_load_2d(b_base + b * B_BYTES + u * B_SUB, &p.tm_act, &st_full[b], t.k0 + s * BK + u * KS,
+                            t.row0);
         }
       }
     }
@@ -314,6 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
     for (int tid = blockIdx.x; tid < total_tiles && ok; tid += gridDim.x) {
       Tile t;
       if (!decode_tile(p, tid, n_tiles, t, cur)) continue;
+      const int nst = (t.k1 - t.k0 + BK - 1) / BK;
       for (int s = 0; s < nst; ++s, ++sg) {
         const int sub = s % RAW_PER;   // k-stage within its packed-word copy
         const int r = rg % RAW_STAGES, a = sg % A_STAGES;
@@ -394,7 +409,8 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
         if (!decode_tile(p, tid, n_tiles, t, cur)) continue;
         ++seg;
         buf = seg & 1;
-        int seg_end = min(min(group, SEG_MAX), K);
+        const int nst = (t.k1 - t.k0 + BK - 1) / BK;
+        int seg_end = min(min((t.k0 / group + 1) * group, t.k0 + SEG_MAX), t.k1);
         uint32_t acc = 0;
         if (!tc::wait(&acc_empty[buf], ((seg >> 1) & 1) ^ 1, abort_flag, p.status, kWaitNs)) break;
         tc::fence_after_sync();
@@ -407,19 +423,19 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
           tc::fence_after_sync();
           const uint64_t ad = adesc0 + static_cast<uint64_t>((a * A_BYTES) >> 4);
           const uint64_t bd = bdesc0 + static_cast<uint64_t>((b * B_BYTES) >> 4);
-          const int kbase = s * BK;
+          const int kbase = t.k0 + s * BK;
 #pragma unroll
           for (int j = 0; j < BK / UMMA_K; ++j) {
             // MMA j: sub-tile j / 4, 32-byte step j % 4 inside its swizzle rows
             constexpr int kPerSub = KS / UMMA_K;
             const int k = kbase + j * UMMA_K;
-            if (k < K) {
+            if (k < t.k1) {
               if (k == seg_end) {  // close this accumulation, open the next buffer
                 tc::commit(&acc_full[buf]);
                 ++seg;
                 buf = seg & 1;
                 const int g = k / group;
-                seg_end = min(min((g + 1) * group, k + SEG_MAX), K);
+                seg_end = min(min((g + 1) * group, k + SEG_MAX), t.k1);
                 if (!tc::wait(&acc_empty[buf], ((seg >> 1) & 1) ^ 1, abort_flag, p.status, kWaitNs)) {
                   ok = false;
                   break;
@@ -481,9 +497,10 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
         const size_t si = (p.mode == kExperts) ? ((size_t)t.expert * N + n) * G + gg : (size_t)gg * N + n;
         return p.w_scale[si];
       };
-      uint32_t sr0 = ld_scale(0), sr1 = ld_scale(1), sr2 = ld_scale(2), sr3 = ld_scale(3);
-      int cur_g = 0;
-      for (int k0 = 0; ok && k0 < K; ++seg) {
+      const int g0 = t.k0 / group;
+      uint32_t sr0 = ld_scale(g0), sr1 = ld_scale(g0 + 1), sr2 = ld_scale(g0 + 2), sr3 = ld_scale(g0 + 3);
+      int cur_g = g0;
+      for (int k0 = t.k0; ok && k0 < t.k1; ++seg) {
         const int g = k0 / group;
         if (g != cur_g) {   // segments walk k in order: the group advances by one
           sr0 = sr1;
@@ -492,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
           sr3 = ld_scale(g + 3);
           cur_g = g;
         }
-        const int kend = min(min((g + 1) * group, k0 + SEG_MAX), K);
+        const int kend = min(min((g + 1) * group, k0 + SEG_MAX), t.k1);
         const int buf = seg & 1;
         if (!tc::wait(&acc_full[buf], (seg >> 1) & 1, abort_flag, p.status, kWaitNs)) {
           ok = false;
@@ -531,7 +548,13 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
         k0 = kend;
       }
 
-      if (ok && !partials && !*abort_flag) {
+      if (ok && !partials && !*abort_flag && p.splits > 1) {
+        // this split's fp32 sums; the reduce pass adds the splits, x_scale and bias
+        float* pp = p.part + ((size_t)t.split * p.M + t.row0 + c0) * N + n;
+#pragma unroll
+        for (int j = 0; j < kEpiCols; ++j)
+          if (n_ok && t.row0 + c0 + j < t.row_end) pp[(size_t)j * N] = T[j];
+      } else if (ok && !partials && !*abort_flag) {
         // Lanes 2i and 2i+1 hold outputs n and n+1 of the same tokens. For each
         // pair of tokens (j, j+1) they swap halves, so that the even lane stores
         // (n, n+1) of token j and the odd lane (n, n+1) of token j+1: one 4-byte
@@ -584,6 +607,40 @@ __global__ void __launch_bounds__(256) widen_kernel(const uint4* __restrict__ sr
 }
 
 // ---------------------------------------------------------------------------
+// split-K: y = bf16(x_scale[m] * (sum of the splits' fp32 partials) + bias[n])
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(256) split_reduce_kernel(const float4* __restrict__ part, int splits, int64_t M,
+                                                           int N4, const float* __restrict__ x_scale,
+                                                           const uint16_t* __restrict__ bias, uint2* __restrict__ y) {
+  const int64_t total = M * N4;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const int64_t m = i / N4;
+    const int n = static_cast<int>(i - m * N4) * 4;
+    float4 acc = part[i];
+    for (int sp = 1; sp < splits; ++sp) {   // splits in order
+      const float4 v = part[(size_t)sp * total + i];
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    const float xs = x_scale[m];
+    float b[4] = {0.f, 0.f, 0.f, 0.f};
+    if (bias != nullptr) {
+      const uint2 bb = *reinterpret_cast<const uint2*>(bias + n);
+      b[0] = bf16_lo(bb.x);
+      b[1] = bf16_hi(bb.x);
+      b[2] = bf16_lo(bb.y);
+      b[3] = bf16_hi(bb.y);
+    }
+    y[i] = make_uint2(pack_bf16x2(fmaf(xs, acc.x, b[0]), fmaf(xs, acc.y, b[1])),
+                      pack_bf16x2(fmaf(xs, acc.z, b[2]), fmaf(xs, acc.w, b[3])));
+  }
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 
@@ -630,6 +687,50 @@ cudaError_t widen(const void* src, void* dst, int64_t rows, int64_t K, bool fp8,
   else
     widen_kernel<false><<<blocks, 256, 0, s>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst), n16);
   return cudaGetLastError();
+}
+
+// Split along K when the output tiles fill the 152 SMs of a GB300 poorly.
+// The parts (1 to 4, at least 512 k each, cut on 128-k stages and on group
+// boundaries) trade waves of tiles against the partial sums' traffic:
+// estimated time = ceil(tiles * s / 152) / s * K * 11.7 ns (a 128 x 256 tile
+// at the measured ~0.45 of the bf16 peak) + 8 s M N bytes (fp32 partials
+// written and read) at 6.8 TB/s. At 4096 x 11008 x 4096 that keeps one part;
+// at 512 x 4096 x 4096 it takes two. Fixed figures keep the choice, and the
+// workspace it needs, the same on every device.
+constexpr int kSplitSms = 152;
+struct Split {
+  int splits, ksplit;
+};
+Split choose_split(int64_t M, int64_t N, int64_t K, int32_t group) {
+  const int64_t tiles = ((M + BN - 1) / BN) * ((N + BM - 1) / BM);
+  int64_t gran = 128;   // stages of the fp16 path; the cut must also fall on a group boundary
+  if (group < K) {
+    int64_t a = gran, b = group;
+    while (b) {
+      const int64_t t = a % b;
+      a = b;
+      b = t;
+    }
+    gran = gran / a * group;   // lcm(128, group)
+  }
+  auto cost = [&](int sp) {
+    const double waves = static_cast<double>((tiles * sp + kSplitSms - 1) / kSplitSms) / sp;
+    const double traffic = sp > 1 ? 8.0 * sp * static_cast<double>(M) * static_cast<double>(N) / 6.8e12 : 0.0;
+    return waves * static_cast<double>(K) * 11.7e-9 + traffic;
+  };
+  Split best{1, static_cast<int>(K)};
+  double best_t = cost(1);
+  for (int sp = 2; sp <= 4; ++sp) {
+    if (K / sp < 512) break;
+    const int64_t ks = ((K + sp - 1) / sp + gran - 1) / gran * gran;
+    if ((K + ks - 1) / ks != sp) continue;
+    const double t = cost(sp);
+    if (t < best_t * 0.97) {   // a clear gain only
+      best_t = t;
+      best = Split{sp, static_cast<int>(ks)};
+    }
+  }
+  return best;
 }
 
 template <bool FP8>
@@ -695,13 +796,34 @@ cudaError_t run_t(const W4A8Args& a, int mode, cudaStream_t s) {
 
   // tile rows: dense, one per 256 rows; experts, an upper bound on the tiles
   // of all segments together (each expert's last tile may be partial)
-  const long long y_tiles = experts ? (a.M + BN - 1) / BN + a.E : (a.M + BN - 1) / BN;
+  p.m_tiles = static_cast<int>(experts ? (a.M + BN - 1) / BN + a.E : (a.M + BN - 1) / BN);
+  p.splits = 1;
+  p.ksplit = p.K;
+  if (mode == kDenseY) {
+    // split along K when the workspace holds the partial sums after the activations
+    const Split sp = choose_split(a.M, a.N, a.K, a.group);
+    const size_t need = w4a8_workspace_bytes(a.M, a.K) + (size_t)sp.splits * a.M * a.N * 4;
+    if (sp.splits > 1 && a.workspace_bytes >= need) {
+      p.splits = sp.splits;
+      p.ksplit = sp.ksplit;
+      p.part = reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + w4a8_workspace_bytes(a.M, a.K));
+    }
+  }
+  const long long y_tiles = (long long)p.m_tiles * p.splits;
   const long long total = y_tiles * n_tiles;
   if (total > INT32_MAX) return cudaErrorInvalidConfiguration;
   // persistent: one CTA per SM (the shared-memory rings fill an SM)
   const long long grid = total < sm_count_w4a8() ? total : sm_count_w4a8();
   w4a8_tc_kernel<2, FP8><<<static_cast<unsigned>(grid), kThreads, C::SMEM, s>>>(p, n_tiles,
                                                                                  static_cast<int>(y_tiles));
+  e = cudaGetLastError();
+  if (e != cudaSuccess || p.splits == 1) return e;
+  const int64_t n4 = a.M * (a.N / 4);
+  const int64_t want = (n4 + 255) / 256;
+  const unsigned blocks = static_cast<unsigned>(want < sm_count_w4a8() * 8 ? want : sm_count_w4a8() * 8);
+  split_reduce_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const float4*>(p.part), p.splits, a.M,
+                                             static_cast<int>(a.N / 4), a.x_scale,
+                                             static_cast<const uint16_t*>(a.bias), static_cast<uint2*>(a.out));
   return cudaGetLastError();
 }
 
@@ -712,6 +834,11 @@ cudaError_t run(const W4A8Args& a, int mode, cudaStream_t s) {
 }  // namespace
 
 size_t w4a8_workspace_bytes(int64_t rows, int64_t K) { return static_cast<size_t>(rows) * static_cast<size_t>(K) * 2; }
+
+size_t w4a8_workspace_bytes_split(int64_t M, int64_t N, int64_t K, int32_t group) {
+  const Split sp = choose_split(M, N, K, group);
+  return w4a8_workspace_bytes(M, K) + (sp.splits > 1 ? (size_t)sp.splits * M * N * 4 : 0);
+}
 
 cudaError_t launch_w4a8_dense(const W4A8Args& a, cudaStream_t s) {
   return run(a, a.partials ? kDensePartials : kDenseY, s);

@@ -188,3 +188,27 @@ def test_w4a8_bf16in_full_size(M, N, K, group, outliers):
     rows = np.unique(np.concatenate([np.arange(0, M, max(1, M // 40)), [1, M - 2, M - 1]]))
     check_bf16_output(bits(y)[rows], O.w4a8_linear(qr[rows], sr[rows], qw, sw, group),
                       f"bf16in full size {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K,group,bias", [(300, 264, 2048, 128, True), (100, 136, 3072, -1, False),
+                                              (33, 128, 1536, 48, True), (512, 4096, 4096, 128, False)])
+def test_w4a8_split_k(M, N, K, group, bias):
+    """Shapes whose output tiles fill the SMs poorly run split along K (the
+    workspace w4_workspace_bytes asks for holds the parts' fp32 sums): 4 parts
+    for the first two, 2 for the last two (the group of 48 cuts on 384-k
+    boundaries). The same call with only the minimal workspace runs unsplit.
+    Both against the oracle."""
+    _, qx, sx, qw, sw = _inputs(M, N, K, group, seed=M + K, outliers=0.01)
+    bb = S.bias_bf16(N, seed=5) if bias else None
+    args = (to_dev(qx), to_dev(sx), to_dev(qw), to_dev(sw), group)
+    kw = {} if bb is None else {"bias": bf16(bb)}
+    full = w4.w4_workspace_bytes(w4.W4_OP_W4A8, M, N, K, group)
+    assert full > M * K * 2, "this shape should be split"
+    y_split = w4.w4a8_gemm(*args, **kw)
+    ws_min = torch.empty((M * K * 2,), dtype=torch.uint8, device="cuda")
+    y_one = w4.w4a8_gemm(*args, workspace=ws_min, **kw)
+    torch.cuda.synchronize()
+    r = O.w4a8_linear(qx, sx, qw, sw, group, bb)
+    check_bf16_output(bits(y_split), r, f"split M={M} N={N} K={K} g={group}")
+    check_bf16_output(bits(y_one), r, f"unsplit M={M} N={N} K={K} g={group}")
+    assert w4.w4_device_status() == w4.W4_OK
