@@ -57,15 +57,18 @@ BLOCK_CYCLES = 400_000        # ~0.2 ms at 2 GHz: longer than submitting the tim
 # kernel's source file at capture time; reported only while the source matches.
 TRAFFIC = {
     # w4a16_kernel, M=1 K=4096 N=14336 g128, caches flushed: dram__bytes_read.sum + dram__bytes_write.sum
-    # (30,329,600 + 0)
-    "w4a16": (30329600, "87d141e4bb1a5321", "w4a16.cu"),
-    # lm_head_tc_kernel, M=1 V=131072 D=2048 g128 (151,030,272 + 3,162,368)
-    "lm_head": (154192640, "5faab0d70541d2ee", "embed.cu"),
-    # quantize_chunks_kernel<bf16, 16, 2>, N=14336 K=4096 g128 (117,459,456 + 7,766,016; the codes,
+    # (30,335,232 + 0)
+    "w4a16": (30335232, "4b71e11da3cde5b1", "w4a16.cu"),
+    # w4a8_tc_kernel<2, fp16>, W4A8 diffusion M=16384 K=N=3072 g=-1 (105,703,424 + 63,735,552)
+    "w4a8_diffusion": (169438976, "b7952c95bdc84570", "w4a8.cu"),
+    # w4a8_tc_kernel<2, e4m3> in expert mode, the MoE layer's two GEMMs: gate_up (257,889,792 + 150,879,232)
+    # and down (141,700,096 + 94,450,176)
+    # lm_head_tc_kernel, M=1 V=131072 D=2048 g128 (151,032,832 + 2,898,432)
+    "lm_head": (153931264, "18cc61b739d893a3", "embed.cu"),
+    # quantize_chunks_kernel<bf16, 16, 2>, N=14336 K=4096 g128 (117,462,528 + 8,325,888; the codes,
     # scales and zeros are still in L2 when the kernel ends)
-    "quantize": (125225472, "cf9a6143ae4772be", "tools.cu"),
-    # w4a8_tc_kernel<2>, W4A8 diffusion M=16384 K=N=3072 g=-1 (105,717,248 + 62,809,856)
-    "w4a8_diffusion": (168527104, "b085096938827044", "w4a8.cu"),
+    "quantize": (125788416, "5dce2085fddf52cf", "tools.cu"),
+    "w4afp8_moe": (644919296, "b7952c95bdc84570", "w4a8.cu"),
 }
 
 
