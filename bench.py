@@ -648,43 +648,35 @@ def oracle_decode_sample(cols, seed=0):
     return xb, np.ascontiguousarray(qw), np.ascontiguousarray(sw)
 
 
-def cpu_threads():
-    try:
-        return len(os.sched_getaffinity(0))
-    except AttributeError:
-        return os.cpu_count() or 1
-
-
 def cpu_baseline(budget_s=10.0):
-    """Time the oracle's W4A16 on column blocks of the decode GEMV for ~budget_s."""
-    import oracle as O
-    ncols = 1024
-    xb, qw, sw = oracle_decode_sample(np.arange(ncols))
-    O.w4a16_linear(xb, qw, sw, DEC_G)   # warm
+    """Time the C oracle's W4A16 (plain loops in float64, threads over the output
+    columns) on the whole M=1 decode GEMV, repeated for ~budget_s."""
+    from oracle import c_oracle as C
+    xb, qw, sw = oracle_decode_sample(np.arange(DEC_N))
+    C.w4a16_linear(xb, qw, sw, DEC_G)   # warm (and build)
     n, t0 = 0, time.perf_counter()
     while time.perf_counter() - t0 < budget_s:
-        O.w4a16_linear(xb, qw, sw, DEC_G)
+        C.w4a16_linear(xb, qw, sw, DEC_G)
         n += 1
     dt = time.perf_counter() - t0
-    nbytes = decode_bytes(N=ncols)
-    return {"value": round(n * nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": cpu_threads(), "kind": "oracle",
-            "sample": f"{n} oracle W4A16 calls on a {ncols}-column block of the M=1 decode GEMV "
-                      f"(K=4096, group 128), {dt:.1f} s; numpy float64"}
+    nbytes = decode_bytes()
+    return {"value": round(n * nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": C.threads(), "kind": "oracle",
+            "sample": f"{n} calls of the C oracle (oracle/w4_oracle_c.c, float64, {C.threads()} threads) on the whole "
+                      f"M=1 decode GEMV (K=4096, N=14336, group 128), {dt:.1f} s"}
 
 
 def run_reference(args, rank, world):
     if rank != 0:
         return None
-    import oracle as O
-    ncols = 8
-    xb, qw, sw = oracle_decode_sample(np.arange(ncols))
+    from oracle import c_oracle as C
+    xb, qw, sw = oracle_decode_sample(np.arange(DEC_N))
     for _ in range(max(args.warmup, 3)):
-        O.w4a16_linear(xb, qw, sw, DEC_G)
+        C.w4a16_linear(xb, qw, sw, DEC_G)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        O.w4a16_linear(xb, qw, sw, DEC_G)
+        C.w4a16_linear(xb, qw, sw, DEC_G)
     dt = time.perf_counter() - t0
-    nbytes = decode_bytes(N=ncols)
+    nbytes = decode_bytes()
     value = args.steps * nbytes / dt / 1e9
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "GB/s", "n_gpus": world,
@@ -693,9 +685,10 @@ def run_reference(args, rank, world):
         "data": "synthetic (same generator as the GPU arm)",
         "config": {"workload": "w4a16_decode", "M": DEC_M, "K": DEC_K, "N": DEC_N, "group": DEC_G,
                    "scales": "fp16", "zeros": False,
-                   "sample": f"each step: the oracle on an {ncols}-column block of the GEMV"},
-        "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": cpu_threads(), "kind": "oracle",
-                         "sample": f"{args.steps} steps, each an {ncols}-column block of the M=1 decode GEMV"},
+                   "sample": "each step: the C oracle on the whole decode GEMV"},
+        "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": C.threads(), "kind": "oracle",
+                         "sample": f"{args.steps} steps, each the C oracle (float64, {C.threads()} threads) on the "
+                                   "whole M=1 decode GEMV"},
         "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 

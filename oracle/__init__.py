@@ -5,6 +5,9 @@ links anything here; only ``tests/``, ``__graft_entry__.smoke()`` and the
 ``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may use it. It
 shares no code with the CUDA path.
 
-Everything is plain numpy in float64 / int64 (``w4_oracle.py``).
+The oracle proper is plain numpy in float64 / int64 (``w4_oracle.py``). The W4A16
+layer is also stated in plain C (``w4_oracle_c.c``, called through
+``c_oracle.py``) for timing the CPU baseline on the host's cores; the tests pin it
+to the numpy statement.
 """
 from .w4_oracle import *  # noqa: F401,F403
