@@ -30,6 +30,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import itertools
 import json
 import os
 import statistics
@@ -39,6 +40,8 @@ import threading
 import time
 
 import numpy as np
+
+L2_BYTES = 129 * 2 ** 20          # GB300 L2
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -398,8 +401,12 @@ def bench_rows(dev, stream, bf16_tf, peak_kind, hbm_peak, only=None):
         def gemm():
             w4.w4a8_gemm(q, s, qw, sw, group, y=y, workspace=ws, stream=stream)
 
+        # the quantizer alone on rotating copies of x, together larger than L2
+        xq = [x] + [x.clone() for _ in range(max(1, -(-L2_BYTES * 2 // (M * K * 2))) - 1)]
+        xq_next = itertools.cycle(xq)
+
         def quant():
-            w4.w4_quant_act_per_token(x, "int8", q=q, scale=s, stream=stream)
+            w4.w4_quant_act_per_token(next(xq_next), "int8", q=q, scale=s, stream=stream)
 
         def fused():
             w4.w4a8_gemm_bf16in(x, qw, sw, group, y=y, x_scale=s, workspace=ws, stream=stream)
@@ -407,7 +414,7 @@ def bench_rows(dev, stream, bf16_tf, peak_kind, hbm_peak, only=None):
         t_fused = _time_graph(torch, stream, fused, 5, 10)
         t_step = _time_graph(torch, stream, step, 5, 10)
         t_gemm = _time_graph(torch, stream, gemm, 5, 10)
-        t_quant = _time_graph(torch, stream, quant, 5, 10)
+        t_quant = _time_graph(torch, stream, quant, len(xq), 10)
         ops = 2.0 * M * N * K
         tops_gemm = ops / (t_gemm * 1e-3) / 1e12
         rows[name] = {
@@ -418,6 +425,7 @@ def bench_rows(dev, stream, bf16_tf, peak_kind, hbm_peak, only=None):
             "unfused_step": "w4_quant_act_per_token + w4a8_gemm",
             "gemm_ms": t_gemm, "gemm_tops": round(tops_gemm, 1),
             "quant_ms": t_quant, "quant_gbs": round(3.0 * M * K / (t_quant * 1e-3) / 1e9, 1),
+            "quant_l2": f"{len(xq)} rotating copies of x ({len(xq) * M * K * 2 / 1e6:.0f} MB)",
             "roofline": {"bound": "tensor", "achieved": round(tops_gemm, 1), "peak": bf16_tf, "unit": "TFLOP/s",
                          "frac": round(tops_gemm / bf16_tf, 4), "traffic": _traffic(name),
                          "peak_source": f"{peak_kind} bf16_tflops (the exact int8 x int4 products run on the "

@@ -112,7 +112,10 @@ w4_status w4_quant_act_per_token(const void* x, int32_t x_dtype, int64_t M, int6
   if (!aligned(x, 16) || !aligned(q, 16) || !aligned(scale, 4))
     return fail(W4_ERR_ALIGN, "x and q must be 16-byte aligned, scale 4-byte aligned");
   if (M > INT32_MAX) return fail(W4_ERR_UNSUPPORTED, "M too large");
-  return from_cuda(w4::launch_quant_per_token(x, x_dtype == W4_FP16, M, K, q_dtype == W4_FP8_E4M3, q, scale,
+  unsigned int* status = nullptr;
+  cudaError_t e = status_ptr(&status);
+  if (e != cudaSuccess) return from_cuda(e, "device status word");
+  return from_cuda(w4::launch_quant_per_token(x, x_dtype == W4_FP16, M, K, q_dtype == W4_FP8_E4M3, q, scale, status,
                                               static_cast<cudaStream_t>(stream)),
                    "w4_quant_act_per_token launch");
 }
@@ -197,7 +200,7 @@ w4_status w4a8_gemm_bf16in(const void* x, const void* qweight, const void* w_sca
   cudaError_t e = status_ptr(&status);
   if (e != cudaSuccess) return from_cuda(e, "device status word");
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  e = w4::launch_quant_widen(x, M, K, false, workspace, x_scale, s);
+  e = w4::launch_quant_widen(x, M, K, false, workspace, x_scale, status, s);
   if (e != cudaSuccess) return from_cuda(e, "quantize-and-widen launch");
   w4::W4A8Args a{nullptr, x_scale, qweight, w_scale, bias, y, nullptr, 1, M, N, K, g, false, status, workspace, true,
                  false, workspace_bytes};

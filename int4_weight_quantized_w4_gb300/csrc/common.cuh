@@ -123,19 +123,120 @@ W4_DEV uint32_t e4m3x2_rn(float lo, float hi) {
   return c;
 }
 
-// The e4m3 codes (satfinite, round to nearest even) of fl(xl / s) and
-// fl(xh / s), lo in the low byte, given r = fl(1 / s). y = x r differs from
-// x / s by at most |x / s| (2^-23 + 2^-48) and fl(x / s) from x / s by at most
-// |x / s| 2^-24, so fl(x / s) lies inside [y (1 - 2^-20), y (1 + 2^-20)], even
-// with both ends rounded to fp32. e4m3 rounding is monotone: when both ends of
-// the bracket give the same code, that is the code of fl(x / s); otherwise the
-// IEEE divide decides (values within about 2^-20 of a rounding boundary).
-W4_DEV uint32_t e4m3x2_of_quotient(float xl, float xh, float s, float r) {
-  const float yl = xl * r, yh = xh * r;
-  const uint32_t a = e4m3x2_rn(yl * 0.99999904632568359375f, yh * 0.99999904632568359375f);
-  const uint32_t b = e4m3x2_rn(yl * 1.00000095367431640625f, yh * 1.00000095367431640625f);
-  if (a == b) return a;
-  return e4m3x2_rn(__fdiv_rn(xl, s), __fdiv_rn(xh, s));
+// Packed fp32 pairs: one f32x2 instruction for two results, round to nearest.
+W4_DEV void mul2(float& d0, float& d1, float a0, float a1, float b) {
+  asm("{.reg .b64 d, x, y; mov.b64 x, {%2, %3}; mov.b64 y, {%4, %4}; mul.rn.f32x2 d, x, y; mov.b64 {%0, %1}, d;}"
+      : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b));
+}
+W4_DEV void add2(float& d0, float& d1, float a0, float a1, float b) {
+  asm("{.reg .b64 d, x, y; mov.b64 x, {%2, %3}; mov.b64 y, {%4, %4}; add.rn.f32x2 d, x, y; mov.b64 {%0, %1}, d;}"
+      : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b));
+}
+
+// Halfwise larger magnitude of two words of two 16-bit floats (bf16, or fp16
+// with kF16); the sign bits of the result carry no meaning.
+template <bool kF16>
+W4_DEV uint32_t absmax2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  if (kF16)
+    asm("max.xorsign.abs.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  else
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// The codes of the IEEE quotient fl(x / s). With r = fl(1 / s) and the two
+// per-row factors rlo = fl(r (1 - 2^-20)), rhi = fl(r (1 + 2^-20)), the products
+// fl(x rlo) and fl(x rhi) are (x / s)(1 -+ 2^-20)(1 + e) with |e| < 3.1 * 2^-24,
+// while fl(x / s) = (x / s)(1 + e'), |e'| <= 2^-24: fl(x / s) lies between the
+// two products (a tiny x whose products underflow lies with them below every
+// rounding boundary). Rounding onto the int8 or e4m3 grid is monotone, so
+// where both products give the same code, that is the code of fl(x / s); a
+// chunk in which some element's ends differ (a value within about 2^-20 of a
+// rounding boundary) takes the IEEE divide for all of its elements.
+//
+// A subnormal s (amax below 2^-126 times the code maximum) breaks the relative
+// bounds and may overflow 1 / s: there rlo = 0 and rhi = inf, whose ends differ
+// on every element, so such rows are quantized with the divide throughout.
+struct QuotientBracket {
+  float s, rlo, rhi;
+};
+
+W4_DEV QuotientBracket quotient_bracket(float s) {
+  if (s < 1.17549435e-38f) return {s, 0.f, __int_as_float(0x7f800000)};
+  const float r = __frcp_rn(s);
+  return {s, r * 0.99999904632568359375f, r * 1.00000095367431640625f};
+}
+
+// Activation halves of a word as fp32 (exact): bf16, or fp16 (kF16).
+template <bool kF16>
+W4_DEV float act_lo(uint32_t w) {
+  return kF16 ? half_bits_to_f32(w & 0xFFFFu) : bf16_lo(w);
+}
+template <bool kF16>
+W4_DEV float act_hi(uint32_t w) {
+  return kF16 ? half_bits_to_f32(w >> 16) : bf16_hi(w);
+}
+
+// The int8 codes clamp(rne(fl(x / s)), -127, 127) of the 8 activations of a
+// 16-byte chunk, element i in byte i. Adding 1.5 * 2^23 rounds a value below
+// 2^22 in magnitude to an integer (round to nearest even) and leaves that
+// integer in the low bits of the sum, its low byte the two's-complement code.
+// On the bracket path |x / s| <= 127 (1 + 2^-22) (s normal, |x| <= amax), so
+// no code leaves [-127, 127] and no clamp is needed there.
+template <bool kF16>
+W4_DEV uint2 quant_int8_chunk(const uint4& v, const QuotientBracket& b) {
+  constexpr float kMagic = 12582912.f;
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t c[8];
+  uint32_t diff = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float xl = act_lo<kF16>(w[i]), xh = act_hi<kF16>(w[i]);
+    float l0, l1, h0, h1;
+    mul2(l0, l1, xl, xh, b.rlo);
+    mul2(h0, h1, xl, xh, b.rhi);
+    add2(l0, l1, l0, l1, kMagic);
+    add2(h0, h1, h0, h1, kMagic);
+    c[2 * i] = __float_as_uint(l0);
+    c[2 * i + 1] = __float_as_uint(l1);
+    diff |= (c[2 * i] ^ __float_as_uint(h0)) | (c[2 * i + 1] ^ __float_as_uint(h1));
+  }
+  if (diff != 0) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float ql = fmaxf(-127.f, fminf(127.f, __fdiv_rn(act_lo<kF16>(w[i]), b.s)));
+      const float qh = fmaxf(-127.f, fminf(127.f, __fdiv_rn(act_hi<kF16>(w[i]), b.s)));
+      c[2 * i] = __float_as_uint(ql + kMagic);
+      c[2 * i + 1] = __float_as_uint(qh + kMagic);
+    }
+  }
+  return make_uint2(prmt(prmt(c[0], c[1], 0x0040u), prmt(c[2], c[3], 0x0040u), 0x5410u),
+                    prmt(prmt(c[4], c[5], 0x0040u), prmt(c[6], c[7], 0x0040u), 0x5410u));
+}
+
+// The e4m3 codes (satfinite, round to nearest even) of fl(x / s) for the 8
+// activations of a 16-byte chunk, element i in byte i.
+template <bool kF16>
+W4_DEV uint2 quant_e4m3_chunk(const uint4& v, const QuotientBracket& b) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t p[4];
+  uint32_t diff = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float xl = act_lo<kF16>(w[i]), xh = act_hi<kF16>(w[i]);
+    float l0, l1, h0, h1;
+    mul2(l0, l1, xl, xh, b.rlo);
+    mul2(h0, h1, xl, xh, b.rhi);
+    p[i] = e4m3x2_rn(l0, l1);
+    diff |= p[i] ^ e4m3x2_rn(h0, h1);
+  }
+  if (diff != 0) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      p[i] = e4m3x2_rn(__fdiv_rn(act_lo<kF16>(w[i]), b.s), __fdiv_rn(act_hi<kF16>(w[i]), b.s));
+  }
+  return make_uint2(prmt(p[0], p[1], 0x5410u), prmt(p[2], p[3], 0x5410u));
 }
 
 // ---------------------------------------------------------------------------

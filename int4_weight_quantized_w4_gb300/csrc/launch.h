@@ -24,8 +24,9 @@ inline int current_sm_count() {
 // Polls a bounded wait makes before it gives up (about a second of spinning).
 constexpr long long kWaitLimit = 1LL << 24;
 
+// status: the device status word (a timed-out wait records W4_ERR_TIMEOUT there).
 cudaError_t launch_quant_per_token(const void* x, bool x_f16, int64_t M, int64_t K, bool fp8, void* q,
-                                   float* scale, cudaStream_t s);
+                                   float* scale, unsigned int* status, cudaStream_t s);
 
 struct W4A16Args {
   const void* x;
@@ -43,7 +44,7 @@ cudaError_t launch_w4a16(const W4A16Args& a, cudaStream_t s);
 // Per-token quantization whose output is the codes' exact fp16 values in the
 // W4A8 operand order (fp16 [M, K] into `wide`), plus the fp32 scales.
 cudaError_t launch_quant_widen(const void* x, int64_t M, int64_t K, bool fp8, void* wide, float* scale,
-                               cudaStream_t s);
+                               unsigned int* status, cudaStream_t s);
 // Shared memory the decode kernel needs for one token row beside a minimal ring.
 size_t w4a16_smem_bytes(int64_t N, int64_t K, int32_t group);
 

@@ -201,11 +201,13 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(int32_t* __restrict_
 }
 
 // silu(g) = g / (1 + e^-g) in fp32 with the fast exponential and divide (a
-// few ulp; the bf16 result it feeds is what the reading fixes). Below -80,
-// where 1 + e^-g passes the fast divide's range, silu(g) = g e^g to within
-// e^-80 relative.
+// few ulp; the bf16 result it feeds is what the reading fixes), written with
+// the one exponential t = e^-|g| in (0, 1]: g / (1 + t) for g >= 0 and
+// g t / (1 + t) for g < 0 (numerator and denominator multiplied by e^g). The
+// denominator stays in [1, 2], inside the fast divide's range for every g.
 W4_DEV float silu_f32(float g) {
-  return g > -80.f ? __fdividef(g, 1.f + __expf(-g)) : g * __expf(g);
+  const float t = __expf(-fabsf(g));
+  return __fdividef(g >= 0.f ? g : g * t, 1.f + t);
 }
 
 // act = bf16(silu(g) * u) for one chunk of 8 gate and 8 up values.
@@ -221,17 +223,9 @@ W4_DEV uint4 silu_mul_chunk(const uint4& g, const uint4& u) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-W4_DEV float chunk_absmax_bf16(const uint4& v) {
-  float m = fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x)));
-  m = fmaxf(m, fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y))));
-  m = fmaxf(m, fmaxf(fabsf(bf16_lo(v.z)), fabsf(bf16_hi(v.z))));
-  m = fmaxf(m, fmaxf(fabsf(bf16_lo(v.w)), fabsf(bf16_hi(v.w))));
-  return m;
-}
-
-// The e4m3 codes of fl(x / s) for the two activations of a word (r = fl(1 / s)).
-W4_DEV uint32_t e4m3_pair(uint32_t w, float s, float r) {
-  return e4m3x2_of_quotient(bf16_lo(w), bf16_hi(w), s, r);
+// Halfwise magnitude maximum of a chunk of bf16 pairs.
+W4_DEV uint32_t chunk_absmax2_bf16(uint32_t m, const uint4& v) {
+  return absmax2<false>(absmax2<false>(m, v.x), absmax2<false>(absmax2<false>(v.y, v.z), v.w));
 }
 
 // One CTA per row; NCH chunks of 8 per thread kept in registers (NCH == 0:
@@ -248,47 +242,93 @@ __global__ void __launch_bounds__(kActThreads) silu_mul_quant_kernel(const uint4
   auto amax_of = [&](float m) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    const int lane = threadIdx.x & 31;
+    if (lane == 0) red[threadIdx.x >> 5] = m;
     __syncthreads();
-    float r = 0.f;
-    for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) r = fmaxf(r, red[i]);
+    // every group of 8 lanes holds the (up to 8) warp maxima, zero past the
+    // last warp; a butterfly within the group leaves the maximum in every lane
+    float r = (lane & 7) < static_cast<int>(blockDim.x >> 5) ? red[lane & 7] : 0.f;
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) r = fmaxf(r, __shfl_xor_sync(0xffffffffu, r, o));
     return r;
   };
-  auto store = [&](size_t i, const uint4& a, float s) {
-    const float r = __frcp_rn(s);
-    uint2 c;
-    c.x = e4m3_pair(a.x, s, r) | (e4m3_pair(a.y, s, r) << 16);
-    c.y = e4m3_pair(a.z, s, r) | (e4m3_pair(a.w, s, r) << 16);
-    q[o0 + i] = c;
+  auto store = [&](size_t i, const uint4& a, const QuotientBracket& b) {
+    q[o0 + i] = quant_e4m3_chunk<false>(a, b);
     if (act != nullptr) act[o0 + i] = a;
   };
+  auto amax_word = [](uint32_t m2) { return fmaxf(fabsf(bf16_lo(m2)), fabsf(bf16_hi(m2))); };
   if constexpr (NCH > 0) {
     uint4 a[NCH];
-    float m = 0.f;
+    uint32_t m2 = 0;
 #pragma unroll
     for (int c = 0; c < NCH; ++c) {
       const int i = threadIdx.x + c * blockDim.x;
       a[c] = i < I8 ? silu_mul_chunk(ld_stream_v4(hr + i), ld_stream_v4(hr + I8 + i)) : make_uint4(0, 0, 0, 0);
-      m = fmaxf(m, chunk_absmax_bf16(a[c]));
+      m2 = chunk_absmax2_bf16(m2, a[c]);
     }
-    const float amax = amax_of(m);
+    const float amax = amax_of(amax_word(m2));
     const float s = amax == 0.f ? 1.f : __fdiv_rn(amax, 448.f);
+    const QuotientBracket b = quotient_bracket(s);
 #pragma unroll
     for (int c = 0; c < NCH; ++c) {
       const int i = threadIdx.x + c * blockDim.x;
-      if (i < I8) store(i, a[c], s);
+      if (i < I8) store(i, a[c], b);
     }
     if (threadIdx.x == 0) scale[row] = s;
   } else {
-    float m = 0.f;
+    uint32_t m2 = 0;
     for (int i = threadIdx.x; i < I8; i += blockDim.x)
-      m = fmaxf(m, chunk_absmax_bf16(silu_mul_chunk(ld_nc_v4(hr + i), ld_nc_v4(hr + I8 + i))));
-    const float amax = amax_of(m);
+      m2 = chunk_absmax2_bf16(m2, silu_mul_chunk(ld_nc_v4(hr + i), ld_nc_v4(hr + I8 + i)));
+    const float amax = amax_of(amax_word(m2));
     const float s = amax == 0.f ? 1.f : __fdiv_rn(amax, 448.f);
+    const QuotientBracket b = quotient_bracket(s);
     for (int i = threadIdx.x; i < I8; i += blockDim.x)
-      store(i, silu_mul_chunk(ld_stream_v4(hr + i), ld_stream_v4(hr + I8 + i)), s);
+      store(i, silu_mul_chunk(ld_stream_v4(hr + i), ld_stream_v4(hr + I8 + i)), b);
     if (threadIdx.x == 0) scale[row] = s;
   }
+}
+
+// One warp per row for many rows of I up to 2048 (NCH <= 8 chunks per lane),
+// four rows a CTA: the gate and up chunks of the whole row are loaded before
+// any is used, the row maximum is a shuffle butterfly with no block barrier.
+constexpr int kActRowsPerCta = 4;
+template <int NCH>
+__global__ void __launch_bounds__(32 * kActRowsPerCta) silu_mul_quant_warp(const uint4* __restrict__ h, int64_t R,
+                                                                          int I8, uint2* __restrict__ q,
+                                                                          float* __restrict__ scale,
+                                                                          uint4* __restrict__ act) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kActRowsPerCta + (threadIdx.x >> 5);
+  if (row >= R) return;                       // the whole warp
+  const uint4* hr = h + static_cast<size_t>(row) * 2 * static_cast<size_t>(I8);
+  const size_t o0 = static_cast<size_t>(row) * static_cast<size_t>(I8);
+  uint4 g[NCH], u[NCH];
+#pragma unroll
+  for (int j = 0; j < NCH; ++j) {
+    const int c = lane + 32 * j;
+    g[j] = c < I8 ? ld_stream_v4(hr + c) : make_uint4(0, 0, 0, 0);
+    u[j] = c < I8 ? ld_stream_v4(hr + I8 + c) : make_uint4(0, 0, 0, 0);
+  }
+  uint32_t m2 = 0;
+#pragma unroll
+  for (int j = 0; j < NCH; ++j) {
+    g[j] = silu_mul_chunk(g[j], u[j]);        // zero chunks give zero activations
+    m2 = chunk_absmax2_bf16(m2, g[j]);
+  }
+  float amax = fmaxf(fabsf(bf16_lo(m2)), fabsf(bf16_hi(m2)));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float s = amax == 0.f ? 1.f : __fdiv_rn(amax, 448.f);
+  const QuotientBracket b = quotient_bracket(s);
+#pragma unroll
+  for (int j = 0; j < NCH; ++j) {
+    const int c = lane + 32 * j;
+    if (c < I8) {
+      q[o0 + c] = quant_e4m3_chunk<false>(g[j], b);
+      if (act != nullptr) act[o0 + c] = g[j];
+    }
+  }
+  if (lane == 0) scale[row] = s;
 }
 
 // out[t, 8c..8c+7] = bf16(sum_j w[t, j] * y[row_of[t, j], 8c..8c+7]), fp32,
@@ -383,13 +423,30 @@ cudaError_t launch_moe_route(const void* logits, bool bf16, int64_t T, int32_t E
 cudaError_t launch_silu_mul_quant(const void* h, int64_t R, int64_t I, void* q, float* scale, void* act,
                                   cudaStream_t s) {
   const int I8 = static_cast<int>(I / 8);
+  if (R == 0 || I8 == 0) return cudaSuccess;
+  auto hp = static_cast<const uint4*>(h);
+  auto qp = static_cast<uint2*>(q);
+  auto ap = static_cast<uint4*>(act);
+  // one warp per row for many short rows, one CTA per row otherwise (the same
+  // trade as the per-token quantizer's)
+  const int need = (I8 + 31) / 32;
+  if (need <= 8 && R * I8 >= (int64_t{1} << 19)) {
+    const dim3 grid(static_cast<unsigned>((R + kActRowsPerCta - 1) / kActRowsPerCta));
+    constexpr int kT = 32 * kActRowsPerCta;
+    switch (need) {
+      case 1: silu_mul_quant_warp<1><<<grid, kT, 0, s>>>(hp, R, I8, qp, scale, ap); break;
+      case 2: silu_mul_quant_warp<2><<<grid, kT, 0, s>>>(hp, R, I8, qp, scale, ap); break;
+      case 3: silu_mul_quant_warp<3><<<grid, kT, 0, s>>>(hp, R, I8, qp, scale, ap); break;
+      case 4: silu_mul_quant_warp<4><<<grid, kT, 0, s>>>(hp, R, I8, qp, scale, ap); break;
+      case 5: case 6: silu_mul_quant_warp<6><<<grid, kT, 0, s>>>(hp, R, I8, qp, scale, ap); break;
+      default: silu_mul_quant_warp<8><<<grid, kT, 0, s>>>(hp, R, I8, qp, scale, ap); break;
+    }
+    return cudaGetLastError();
+  }
   int threads = ((I8 + 31) / 32) * 32;
   if (threads > kActThreads) threads = kActThreads;
   const int nch = (I8 + threads - 1) / threads;
   const dim3 grid(static_cast<unsigned>(R));
-  auto hp = static_cast<const uint4*>(h);
-  auto qp = static_cast<uint2*>(q);
-  auto ap = static_cast<uint4*>(act);
   switch (nch) {
     case 1: silu_mul_quant_kernel<1><<<grid, threads, 0, s>>>(hp, I8, qp, scale, ap); break;
     case 2: silu_mul_quant_kernel<2><<<grid, threads, 0, s>>>(hp, I8, qp, scale, ap); break;

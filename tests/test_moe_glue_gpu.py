@@ -71,6 +71,25 @@ def test_gather_quant_bit_exact_and_bad_row():
     assert not qb[1:].any() and np.all(s.cpu().numpy()[1:] == 1.0)
 
 
+def test_gather_quant_many_rows_and_bad_rows():
+    """Enough gathered rows for the warp-per-row form (R x K >= 2^22), with
+    repeated tokens and two ids outside [0, T) among them."""
+    T, K, R = 1000, 2048, 2100
+    x = S.activations_bf16(T, K, seed=22)
+    rows = (S.raw_u64(23, 5, R) % T).astype(np.int32)
+    rows[5], rows[R - 1] = T, -1
+    q, s = w4.w4_moe_gather_quant_fp8(bf16(x), to_dev(rows))
+    torch.cuda.synchronize()
+    assert w4.w4_device_status() == w4.W4_ERR_SHAPE
+    qb, sb = q.view(torch.uint8).cpu().numpy(), s.cpu().numpy()
+    good = np.ones(R, bool)
+    good[[5, R - 1]] = False
+    rq, rs = O.moe_gather_quant_fp8(x, rows[good])
+    np.testing.assert_array_equal(qb[good], rq)
+    np.testing.assert_array_equal(sb[good], rs)
+    assert not qb[~good].any() and np.all(sb[~good] == 1.0)
+
+
 @pytest.mark.parametrize("T,E,k,N,K,g", [(64, 8, 2, 256, 256, 128), (200, 16, 4, 384, 512, -1)])
 def test_moe_gemm_bf16in_equals_gather_then_gemm(T, E, k, N, K, g):
     """The fused gather + quant + GEMM is bit-identical to the two-step path,
@@ -131,25 +150,28 @@ def _act_check(h, what):
     return qg, sg, a
 
 
-@pytest.mark.parametrize("R,I", [(300, 1408), (5, 8), (17, 2056), (3, 8200)])
+@pytest.mark.parametrize("R,I", [(300, 1408), (5, 8), (9, 512), (6, 768), (5, 1024), (7, 2048), (17, 2056),
+                                 (3, 5000), (2, 8192), (3, 8200), (65536, 64), (8200, 512), (6000, 704),
+                                 (4097, 1024), (2979, 1408), (2049, 2048)])
 def test_silu_mul_quant(R, I):
-    """Row lengths for one, two and several chunks per thread and for the
-    long-row path."""
+    """Row lengths for each chunk count of the CTA-per-row form and, with many
+    rows (R x I >= 2^22, I <= 2048), of the warp-per-row form; row counts that
+    leave part of a CTA empty; the long-row path."""
     h = S.activations_bf16(R, 2 * I, seed=R + I)
     _act_check(h, f"silu R={R} I={I}")
 
 
 def test_silu_mul_quant_edge_values():
     """Gates far below zero (silu -> -0), a zero row (scale 1, codes 0), large
-    gates (silu(g) = g), and gates from -100 to -60 (tiny activations on both
-    sides of the kernel's switch to g e^g)."""
+    gates (silu(g) = g), and gates from -100 to -60 (tiny activations, down
+    into the fp32 subnormals)."""
     R, I = 4, 64
     h = S.activations_bf16(R, 2 * I, seed=3)
     gf = S.bf16_bits_to_f32(h).copy()
     gf[0, :I] = -200.0
     gf[1, :] = 0.0
     gf[2, :I] = 90.0
-    gf[3, :I] = np.linspace(-100.0, -60.0, I)   # across the switch to g e^g
+    gf[3, :I] = np.linspace(-100.0, -60.0, I)
     _act_check(S.to_bf16_bits(gf), "silu edges")
 
 

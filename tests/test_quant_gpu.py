@@ -28,16 +28,29 @@ def _check(xb, kind):
 
 
 @pytest.mark.parametrize("kind", ["int8", "fp8"])
-@pytest.mark.parametrize("M,K", [(1, 8), (3, 256), (16, 256), (7, 1408), (33, 2048), (64, 3072),
-                                 (5, 4096), (9, 8200), (4, 16384), (2, 24)])
+@pytest.mark.parametrize("M,K", [(1, 8), (3, 256), (16, 256), (9, 512), (5, 768), (6, 1000), (7, 1408), (33, 2048),
+                                 (64, 3072), (5, 4096), (3, 5000), (2, 8192), (9, 8200), (4, 16384), (2, 24)])
 def test_quant_parity(kind, M, K):
+    """Row lengths for each chunk count of the warp-per-row form (K <= 4096)
+    and of the CTA-per-row form (3 and 4 chunks a thread, and longer rows read
+    twice), with row counts that leave part of a CTA empty."""
     _check(S.activations_bf16(M, K, seed=M * 7 + K, outlier_frac=0.01), kind)
+
+
+@pytest.mark.parametrize("kind", ["int8", "fp8"])
+@pytest.mark.parametrize("M,K", [(16384, 256), (8200, 512), (5462, 768), (4100, 1024), (2981, 1408), (2049, 2048),
+                                 (1366, 3072)])
+def test_quant_warp_form(kind, M, K):
+    """Many short rows (M x K >= 2^22, K <= 3072) take one warp per row: each
+    chunk count of that form, row counts that leave part of a CTA empty."""
+    _check(S.activations_bf16(M, K, seed=M + K, outlier_frac=0.01), kind)
 
 
 @pytest.mark.parametrize("kind", ["int8", "fp8"])
 def test_quant_special_rows(kind):
     """Zero rows (s = 1), rows whose amax is the code maximum (s = 1, ties at
-    x.5), tiny and huge magnitudes, and sign mixtures."""
+    x.5), tiny and huge magnitudes, rows whose scale is subnormal, and sign
+    mixtures."""
     K = 64
     rows = []
     rows.append(np.zeros(K))
@@ -46,6 +59,13 @@ def test_quant_special_rows(kind):
     rows.append(np.full(K, -3.0e-30))
     rows.append(np.linspace(-1e30, 1e30, K))
     t = np.zeros(K); t[K - 1] = 1e-3; rows.append(t)
+    # rows so small that s is subnormal and fl(1 / s) may overflow: the codes
+    # are still those of the IEEE quotient x / s
+    rng = np.random.default_rng(7)
+    rows.append(rng.uniform(-3e-39, 3e-39, K))
+    rows.append(rng.uniform(-1e-37, 1e-37, K))
+    t = np.zeros(K); t[:4] = [9.2e-41, -4e-40, 1e-39, -1e-39]; rows.append(t)
+    t = rng.uniform(-1e-36, 1e-36, K); t[0] = 2e-36; rows.append(t)
     xb = S.to_bf16_bits(np.stack(rows))
     _check(xb, kind)
 
@@ -77,7 +97,7 @@ def _check_f16(xh, kind):
 
 
 @pytest.mark.parametrize("kind", ["int8", "fp8"])
-@pytest.mark.parametrize("M,K", [(3, 256), (33, 2048), (5, 4096), (9, 8200)])
+@pytest.mark.parametrize("M,K", [(3, 256), (33, 2048), (5, 4096), (9, 8200), (2049, 2048)])
 def test_quant_fp16_activations(kind, M, K):
     """fp16 activations ([INC] class docstring: bf16 or fp16), with the fp16
     extremes in one row: 65504, subnormals, and zeros."""
