@@ -81,10 +81,13 @@ typedef enum {
  * exact fp16 in this workspace (M * K * 2 bytes), so that every output tile
  * streams them with TMA instead of converting them again. For W4_OP_W4A8 the
  * figure also depends on N and the group: when the M x N output tiles would
- * fill the GPU's SMs poorly, the GEMM splits K into up to 4 parts, and the
- * workspace then also holds the parts' fp32 partial sums (parts * M * N * 4
- * bytes after the widened activations). A W4A8 workspace of only M * K * 2
- * bytes is still accepted; the GEMM then runs unsplit. The caller allocates
+ * fill the GPU's SMs poorly, the GEMM splits K, and the workspace then also
+ * holds the parts' fp32 partial sums after the widened activations. Either
+ * every tile is split into up to 4 parts (parts * M * N * 4 bytes), or, when
+ * only the last wave of tiles is at most half full, each of that wave's r
+ * tiles is split into up to 16 parts (r * parts * 128 * 256 * 4 bytes). A W4A8
+ * workspace of only M * K * 2 bytes is still accepted; the GEMM then runs
+ * unsplit. The caller allocates
  * the workspace (16-byte aligned); its contents on entry do not matter and
  * are overwritten.
  */

@@ -112,6 +112,11 @@ struct Params {
   int m_tiles;             // row tiles (dense: ceil(M / 256); experts: an upper bound over all segments)
   int splits, ksplit;      // dense y: the K range cut into `splits` parts of `ksplit` (the last may be shorter)
   float* part;             // splits > 1: fp32 partial sums [splits][M][N], before x_scale and bias
+  // dense y, the last wave only: work items 0 .. full_tiles - 1 are whole tiles; item full_tiles + j is part
+  // j % tail_splits (tail_ksplit of k) of tile full_tiles + j / tail_splits
+  int full_tiles, tail_tiles, tail_splits, tail_ksplit;
+  float* tail_part;        // tail_splits > 1: fp32 partial sums [tail tile][part][BN rows][BM outputs]
+  int items;               // work items the persistent CTAs walk
   unsigned int* status;
 };
 
@@ -156,6 +161,7 @@ W4_DEV void bar_sync_epilogue() { asm volatile("bar.sync 1, %0;" :: "n"(kEpiWarp
 struct Tile {
   int n0, row0, row_end, expert;
   int k0, k1, split;   // the tile's k range (all of K unless the GEMM is split along K)
+  int tail;            // index among the last wave's split tiles, or -1
 };
 // Where a role's walk over the experts stands: expert e, and the row tiles of
 // the experts before it. A role visits its tiles in increasing order, so the
@@ -165,6 +171,14 @@ struct TileCursor {
   int e = 0, base = 0;
 };
 W4_DEV bool decode_tile(const Params& p, int tid, int n_tiles, Tile& t, TileCursor& cur) {
+  t.tail = -1;
+  int part = 0;
+  if (p.tail_splits > 1 && tid >= p.full_tiles) {   // a K part of one of the last wave's tiles
+    const int j = tid - p.full_tiles;
+    t.tail = j / p.tail_splits;
+    part = j - t.tail * p.tail_splits;
+    tid = p.full_tiles + t.tail;
+  }
   const int nx = tid % n_tiles;
   int yt = tid / n_tiles;
   t.n0 = nx * BM;
@@ -179,6 +193,11 @@ W4_DEV bool decode_tile(const Params& p, int tid, int n_tiles, Tile& t, TileCurs
     yt %= p.m_tiles;
     t.k0 = t.split * p.ksplit;
     t.k1 = min(p.K, t.k0 + p.ksplit);
+  }
+  if (t.tail >= 0) {
+    t.split = part;
+    t.k0 = part * p.tail_ksplit;
+    t.k1 = min(p.K, t.k0 + p.tail_ksplit);
   }
   if (p.mode == kExperts) {
     for (; cur.e < p.E; ++cur.e) {
@@ -262,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
 
   const int K = p.K;
   const int group = p.group;
-  const int total_tiles = n_tiles * y_tiles;
+  const int total_tiles = p.items;   // n_tiles * y_tiles, plus the last wave's extra K parts
 
   if (warp >= kEpiWarps) {
   // producer warpgroups give registers to the epilogue warpgroups
@@ -548,7 +567,14 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
         k0 = kend;
       }
 
-      if (ok && !partials && !*abort_flag && p.splits > 1) {
+      if (ok && !partials && !*abort_flag && t.tail >= 0) {
+        // a K part of a last-wave tile: its fp32 sums, every row and output of
+        // the tile (rows and outputs past the matrix hold finite values the
+        // reduce pass never reads), 128 contiguous bytes per warp and token
+        float* pp = p.tail_part + ((size_t)(t.tail * p.tail_splits + t.split) * BN + c0) * BM + 32 * q + lane;
+#pragma unroll
+        for (int j = 0; j < kEpiCols; ++j) pp[(size_t)j * BM] = T[j];
+      } else if (ok && !partials && !*abort_flag && p.splits > 1) {
         // this split's fp32 sums; the reduce pass adds the splits, x_scale and bias
         float* pp = p.part + ((size_t)t.split * p.M + t.row0 + c0) * N + n;
 #pragma unroll
@@ -640,6 +666,47 @@ __global__ void __launch_bounds__(256) split_reduce_kernel(const float4* __restr
   }
 }
 
+// The last wave's tiles: y = bf16(x_scale[m] * (sum of the tile's K parts, in
+// order) + bias[n]) for the outputs of tail tiles first_tile .. first_tile +
+// tail_tiles - 1, four outputs a thread.
+__global__ void __launch_bounds__(256) tail_reduce_kernel(const float4* __restrict__ part, int tail_tiles, int parts,
+                                                          int first_tile, int n_tiles, int64_t M, int N,
+                                                          const float* __restrict__ x_scale,
+                                                          const uint16_t* __restrict__ bias, uint2* __restrict__ y) {
+  constexpr int kRow4 = BM / 4;   // float4 per tile row
+  const int64_t total = (int64_t)tail_tiles * BN * kRow4;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const int tt = static_cast<int>(i / (BN * kRow4));
+    const int rem = static_cast<int>(i - (int64_t)tt * BN * kRow4);
+    const int r = rem / kRow4, c4 = rem - r * kRow4;
+    const int tile = first_tile + tt;
+    const int64_t m = (int64_t)(tile / n_tiles) * BN + r;
+    const int n = (tile % n_tiles) * BM + 4 * c4;
+    if (m >= M || n >= N) continue;   // N is a multiple of 8: n < N puts all four in range
+    const size_t base = ((size_t)tt * parts * BN + r) * kRow4 + c4;
+    float4 acc = part[base];
+    for (int sp = 1; sp < parts; ++sp) {   // parts in order
+      const float4 v = part[base + (size_t)sp * BN * kRow4];
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    const float xs = x_scale[m];
+    float b[4] = {0.f, 0.f, 0.f, 0.f};
+    if (bias != nullptr) {
+      const uint2 bb = *reinterpret_cast<const uint2*>(bias + n);
+      b[0] = bf16_lo(bb.x);
+      b[1] = bf16_hi(bb.x);
+      b[2] = bf16_lo(bb.y);
+      b[3] = bf16_hi(bb.y);
+    }
+    y[(m * N + n) / 4] = make_uint2(pack_bf16x2(fmaf(xs, acc.x, b[0]), fmaf(xs, acc.y, b[1])),
+                                    pack_bf16x2(fmaf(xs, acc.z, b[2]), fmaf(xs, acc.w, b[3])));
+  }
+}
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
@@ -690,16 +757,23 @@ cudaError_t widen(const void* src, void* dst, int64_t rows, int64_t K, bool fp8,
 }
 
 // Split along K when the output tiles fill the 152 SMs of a GB300 poorly.
-// The parts (1 to 4, at least 512 k each, cut on 128-k stages and on group
-// boundaries) trade waves of tiles against the partial sums' traffic:
-// estimated time = ceil(tiles * s / 152) / s * K * 11.7 ns (a 128 x 256 tile
-// at the measured ~0.45 of the bf16 peak) + 8 s M N bytes (fp32 partials
-// written and read) at 6.8 TB/s. At 4096 x 11008 x 4096 that keeps one part;
-// at 512 x 4096 x 4096 it takes two. Fixed figures keep the choice, and the
+// Two forms, priced against no split with a tile's MMA time t = K * 11.7 ns
+// (a 128 x 256 tile at the measured ~0.45 of the bf16 peak), the fp32
+// partials' traffic at 6.8 TB/s and 2 us for the reduce launch:
+//  * every tile in s parts (1 to 4, at least 512 k each): ceil(tiles s / 152)
+//    / s waves of t, plus 8 s M N bytes;
+//  * the last wave only, when it is at most half full: the whole waves as they
+//    are, then each of its r tiles in s parts (2 to 16, at least 256 k each):
+//    ceil(r s / 152) waves of t / s, plus 2 * 4 r s 128 * 256 bytes.
+// Parts are cut on 128-k stages and on group boundaries. At 4096 x 11008 x
+// 4096 the second form splits the 8 tiles of the tenth wave; at 512 x 4096 x
+// 4096 the first takes two parts. Fixed figures keep the choice, and the
 // workspace it needs, the same on every device.
 constexpr int kSplitSms = 152;
 struct Split {
-  int splits, ksplit;
+  int splits, ksplit;                // every tile
+  int tail_splits, tail_ksplit;      // the last wave's tiles
+  int64_t full_tiles, tail_tiles;
 };
 Split choose_split(int64_t M, int64_t N, int64_t K, int32_t group) {
   const int64_t tiles = ((M + BN - 1) / BN) * ((N + BM - 1) / BM);
@@ -713,24 +787,51 @@ Split choose_split(int64_t M, int64_t N, int64_t K, int32_t group) {
     }
     gran = gran / a * group;   // lcm(128, group)
   }
-  auto cost = [&](int sp) {
-    const double waves = static_cast<double>((tiles * sp + kSplitSms - 1) / kSplitSms) / sp;
-    const double traffic = sp > 1 ? 8.0 * sp * static_cast<double>(M) * static_cast<double>(N) / 6.8e12 : 0.0;
-    return waves * static_cast<double>(K) * 11.7e-9 + traffic;
+  const double t_tile = static_cast<double>(K) * 11.7e-9, launch = 2e-6;
+  // the part size for s parts, or 0 when the cut does not give exactly s parts
+  auto part_k = [&](int sp) -> int64_t {
+    const int64_t ks = ((K + sp - 1) / sp + gran - 1) / gran * gran;
+    return (K + ks - 1) / ks == sp ? ks : 0;
   };
-  Split best{1, static_cast<int>(K)};
-  double best_t = cost(1);
+  const Split none{1, static_cast<int>(K), 0, 0, tiles, 0};
+  const double none_t = static_cast<double>((tiles + kSplitSms - 1) / kSplitSms) * t_tile;
+  Split best = none;
+  double best_t = 1e30;   // the cheapest split; taken only if clearly cheaper than none
   for (int sp = 2; sp <= 4; ++sp) {
     if (K / sp < 512) break;
-    const int64_t ks = ((K + sp - 1) / sp + gran - 1) / gran * gran;
-    if ((K + ks - 1) / ks != sp) continue;
-    const double t = cost(sp);
-    if (t < best_t * 0.97) {   // a clear gain only
+    const int64_t ks = part_k(sp);
+    if (ks == 0) continue;
+    const double waves = static_cast<double>((tiles * sp + kSplitSms - 1) / kSplitSms) / sp;
+    const double t = waves * t_tile + 8.0 * sp * static_cast<double>(M) * static_cast<double>(N) / 6.8e12 + launch;
+    if (t < best_t) {
       best_t = t;
-      best = Split{sp, static_cast<int>(ks)};
+      best = Split{sp, static_cast<int>(ks), 0, 0, tiles, 0};
     }
   }
-  return best;
+  const int64_t r = tiles % kSplitSms;
+  if (tiles > kSplitSms && r > 0 && 2 * r <= kSplitSms) {
+    const int64_t full = tiles - r;
+    for (int sp = 2; sp <= 16; ++sp) {
+      if (K / sp < 256) break;
+      const int64_t ks = part_k(sp);
+      if (ks == 0) continue;
+      const double t = static_cast<double>(full / kSplitSms) * t_tile +
+                       static_cast<double>((r * sp + kSplitSms - 1) / kSplitSms) * t_tile / sp +
+                       2.0 * 4.0 * r * sp * BM * BN / 6.8e12 + launch;
+      if (t < best_t) {
+        best_t = t;
+        best = Split{1, static_cast<int>(K), sp, static_cast<int>(ks), full, r};
+      }
+    }
+  }
+  return best_t < none_t * 0.97 ? best : none;   // a clear gain only
+}
+
+// Workspace bytes of the split partials for a plan.
+size_t split_bytes(const Split& sp, int64_t M, int64_t N) {
+  if (sp.splits > 1) return (size_t)sp.splits * M * N * 4;
+  if (sp.tail_splits > 1) return (size_t)sp.tail_tiles * sp.tail_splits * BM * BN * 4;
+  return 0;
 }
 
 template <bool FP8>
@@ -799,25 +900,48 @@ cudaError_t run_t(const W4A8Args& a, int mode, cudaStream_t s) {
   p.m_tiles = static_cast<int>(experts ? (a.M + BN - 1) / BN + a.E : (a.M + BN - 1) / BN);
   p.splits = 1;
   p.ksplit = p.K;
+  p.tail_splits = 0;
   if (mode == kDenseY) {
     // split along K when the workspace holds the partial sums after the activations
     const Split sp = choose_split(a.M, a.N, a.K, a.group);
-    const size_t need = w4a8_workspace_bytes(a.M, a.K) + (size_t)sp.splits * a.M * a.N * 4;
-    if (sp.splits > 1 && a.workspace_bytes >= need) {
-      p.splits = sp.splits;
-      p.ksplit = sp.ksplit;
-      p.part = reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + w4a8_workspace_bytes(a.M, a.K));
+    const size_t extra = split_bytes(sp, a.M, a.N);
+    float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + w4a8_workspace_bytes(a.M, a.K));
+    if (extra > 0 && a.workspace_bytes >= w4a8_workspace_bytes(a.M, a.K) + extra) {
+      if (sp.splits > 1) {
+        p.splits = sp.splits;
+        p.ksplit = sp.ksplit;
+        p.part = part;
+      } else {
+        p.tail_splits = sp.tail_splits;
+        p.tail_ksplit = sp.tail_ksplit;
+        p.full_tiles = static_cast<int>(sp.full_tiles);
+        p.tail_tiles = static_cast<int>(sp.tail_tiles);
+        p.tail_part = part;
+      }
     }
   }
   const long long y_tiles = (long long)p.m_tiles * p.splits;
-  const long long total = y_tiles * n_tiles;
-  if (total > INT32_MAX) return cudaErrorInvalidConfiguration;
+  const long long total = p.tail_splits > 1 ? (long long)p.full_tiles + (long long)p.tail_tiles * p.tail_splits
+                                            : y_tiles * n_tiles;
+  if (total > INT32_MAX || y_tiles * n_tiles > INT32_MAX) return cudaErrorInvalidConfiguration;
+  p.items = static_cast<int>(total);
   // persistent: one CTA per SM (the shared-memory rings fill an SM)
   const long long grid = total < sm_count_w4a8() ? total : sm_count_w4a8();
   w4a8_tc_kernel<2, FP8><<<static_cast<unsigned>(grid), kThreads, C::SMEM, s>>>(p, n_tiles,
                                                                                  static_cast<int>(y_tiles));
   e = cudaGetLastError();
-  if (e != cudaSuccess || p.splits == 1) return e;
+  if (e != cudaSuccess) return e;
+  if (p.tail_splits > 1) {
+    const int64_t n4 = (int64_t)p.tail_tiles * BN * (BM / 4);
+    const int64_t want = (n4 + 255) / 256;
+    const unsigned blocks = static_cast<unsigned>(want < sm_count_w4a8() * 8 ? want : sm_count_w4a8() * 8);
+    tail_reduce_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const float4*>(p.tail_part), p.tail_tiles,
+                                              p.tail_splits, p.full_tiles, n_tiles, a.M, static_cast<int>(a.N),
+                                              a.x_scale, static_cast<const uint16_t*>(a.bias),
+                                              static_cast<uint2*>(a.out));
+    return cudaGetLastError();
+  }
+  if (p.splits == 1) return e;
   const int64_t n4 = a.M * (a.N / 4);
   const int64_t want = (n4 + 255) / 256;
   const unsigned blocks = static_cast<unsigned>(want < sm_count_w4a8() * 8 ? want : sm_count_w4a8() * 8);
@@ -836,8 +960,7 @@ cudaError_t run(const W4A8Args& a, int mode, cudaStream_t s) {
 size_t w4a8_workspace_bytes(int64_t rows, int64_t K) { return static_cast<size_t>(rows) * static_cast<size_t>(K) * 2; }
 
 size_t w4a8_workspace_bytes_split(int64_t M, int64_t N, int64_t K, int32_t group) {
-  const Split sp = choose_split(M, N, K, group);
-  return w4a8_workspace_bytes(M, K) + (sp.splits > 1 ? (size_t)sp.splits * M * N * 4 : 0);
+  return w4a8_workspace_bytes(M, K) + split_bytes(choose_split(M, N, K, group), M, N);
 }
 
 cudaError_t launch_w4a8_dense(const W4A8Args& a, cudaStream_t s) {

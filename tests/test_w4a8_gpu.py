@@ -190,6 +190,32 @@ def test_w4a8_bf16in_full_size(M, N, K, group, outliers):
                       f"bf16in full size {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("M,N,K,group,bias", [(300, 10240, 1024, 128, True), (700, 6656, 1024, 64, False),
+                                              (1000, 5120, 2048, -1, True)])
+def test_w4a8_last_wave_split(M, N, K, group, bias):
+    """Shapes whose last wave of tiles would leave most SMs idle (160, 156 and
+    160 tiles on 152 SMs): the whole waves run as tiles, the last wave's 8, 4
+    and 8 tiles in 4, 4 and 8 K parts whose fp32 sums a reduce pass adds. The
+    split tiles are the last ones, in the last, ragged row tile. Outputs on
+    every row of that tile and on rows of the whole tiles, against the oracle;
+    the same call with only the minimal workspace (unsplit) likewise."""
+    _, qx, sx, qw, sw = _inputs(M, N, K, group, seed=M + K, outliers=0.01)
+    bb = S.bias_bf16(N, seed=5) if bias else None
+    args = (to_dev(qx), to_dev(sx), to_dev(qw), to_dev(sw), group)
+    kw = {} if bb is None else {"bias": bf16(bb)}
+    assert w4.w4_workspace_bytes(w4.W4_OP_W4A8, M, N, K, group) > M * K * 2, "this shape should be split"
+    y_split = w4.w4a8_gemm(*args, **kw)
+    ws_min = torch.empty((M * K * 2,), dtype=torch.uint8, device="cuda")
+    y_one = w4.w4a8_gemm(*args, workspace=ws_min, **kw)
+    torch.cuda.synchronize()
+    last = (M - 1) // 256 * 256
+    rows = np.unique(np.concatenate([np.arange(0, last, 37), np.arange(last, M)]))
+    r = O.w4a8_linear(qx[rows], sx[rows], qw, sw, group, bb)
+    check_bf16_output(bits(y_split)[rows], r, f"last-wave split M={M} N={N} K={K} g={group}")
+    check_bf16_output(bits(y_one)[rows], r, f"unsplit M={M} N={N} K={K} g={group}")
+    assert w4.w4_device_status() == w4.W4_OK
+
+
 @pytest.mark.parametrize("M,N,K,group,bias", [(300, 264, 2048, 128, True), (100, 136, 3072, -1, False),
                                               (33, 128, 1536, 48, True), (512, 4096, 4096, 128, False)])
 def test_w4a8_split_k(M, N, K, group, bias):
