@@ -170,10 +170,14 @@ struct Tile {
 struct TileCursor {
   int e = 0, base = 0;
 };
+// kTail: the launch splits the last wave's tiles (a separate instantiation:
+// the remapping below, in the decode every role runs, measured ~4% slower per
+// tile on grouped shapes, so launches without it do not carry it).
+template <bool kTail>
 W4_DEV bool decode_tile(const Params& p, int tid, int n_tiles, Tile& t, TileCursor& cur) {
   t.tail = -1;
   int part = 0;
-  if (p.tail_splits > 1 && tid >= p.full_tiles) {   // a K part of one of the last wave's tiles
+  if (kTail && tid >= p.full_tiles) {   // a K part of one of the last wave's tiles
     const int j = tid - p.full_tiles;
     t.tail = j / p.tail_splits;
     part = j - t.tail * p.tail_splits;
@@ -194,7 +198,7 @@ W4_DEV bool decode_tile(const Params& p, int tid, int n_tiles, Tile& t, TileCurs
     t.k0 = t.split * p.ksplit;
     t.k1 = min(p.K, t.k0 + p.ksplit);
   }
-  if (t.tail >= 0) {
+  if (kTail && t.tail >= 0) {
     t.split = part;
     t.k0 = part * p.tail_ksplit;
     t.k1 = min(p.K, t.k0 + p.tail_ksplit);
@@ -225,7 +229,7 @@ W4_DEV bool decode_tile(const Params& p, int tid, int n_tiles, Tile& t, TileCurs
 // operand B, the two TMEM accumulators) keeps counting across tiles, so the
 // copies and conversions of the next tile run while this tile's last groups
 // are multiplied and its output is written.
-template <int SUBS, bool FP8>
+template <int SUBS, bool FP8, bool kTail>
 __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_constant__ Params p, int n_tiles,
                                                               int y_tiles) {
   using C = Cfg<SUBS, FP8>;
@@ -281,7 +285,8 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
 
   const int K = p.K;
   const int group = p.group;
-  const int total_tiles = p.items;   // n_tiles * y_tiles, plus the last wave's extra K parts
+  // n_tiles * y_tiles, or (kTail) the whole tiles plus the last wave's K parts
+  const int total_tiles = kTail ? p.items : n_tiles * y_tiles;
 
   if (warp >= kEpiWarps) {
   // producer warpgroups give registers to the epilogue warpgroups
@@ -294,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
       TileCursor cur;
       for (int tid = blockIdx.x; tid < total_tiles && ok; tid += gridDim.x) {
         Tile t;
-        if (!decode_tile(p, tid, n_tiles, t, cur)) continue;
+        if (!decode_tile<kTail>(p, tid, n_tiles, t, cur)) continue;
         const int nraw = ((t.k1 - t.k0 + BK - 1) / BK + RAW_PER - 1) / RAW_PER;
         for (int ri = 0; ri < nraw; ++ri, ++rg) {
           const int r = rg % RAW_STAGES;
@@ -321,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
       TileCursor cur;
       for (int tid = blockIdx.x; tid < total_tiles && ok; tid += gridDim.x) {
         Tile t;
-        if (!decode_tile(p, tid, n_tiles, t, cur)) continue;
+        if (!decode_tile<kTail>(p, tid, n_tiles, t, cur)) continue;
         const int nst = (t.k1 - t.k0 + BK - 1) / BK;
         for (int s = 0; s < nst; ++s, ++sg) {
           if ((sg & 1) != mine) continue;
@@ -346,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
     TileCursor cur;
     for (int tid = blockIdx.x; tid < total_tiles && ok; tid += gridDim.x) {
       Tile t;
-      if (!decode_tile(p, tid, n_tiles, t, cur)) continue;
+      if (!decode_tile<kTail>(p, tid, n_tiles, t, cur)) continue;
       const int nst = (t.k1 - t.k0 + BK - 1) / BK;
       for (int s = 0; s < nst; ++s, ++sg) {
         const int sub = s % RAW_PER;   // k-stage within its packed-word copy
@@ -425,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
       TileCursor cur;
       for (int tid = blockIdx.x; tid < total_tiles && ok; tid += gridDim.x) {
         Tile t;
-        if (!decode_tile(p, tid, n_tiles, t, cur)) continue;
+        if (!decode_tile<kTail>(p, tid, n_tiles, t, cur)) continue;
         ++seg;
         buf = seg & 1;
         const int nst = (t.k1 - t.k0 + BK - 1) / BK;
@@ -496,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
     TileCursor cur;
     for (int tid = blockIdx.x; tid < total_tiles; tid += gridDim.x) {
       Tile t;
-      if (!decode_tile(p, tid, n_tiles, t, cur)) continue;
+      if (!decode_tile<kTail>(p, tid, n_tiles, t, cur)) continue;
       const int n = t.n0 + 32 * q + lane;
       const bool n_ok = n < N;
       bar_sync_epilogue();   // the previous tile's output is written: xs_s may change
@@ -567,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
         k0 = kend;
       }
 
-      if (ok && !partials && !*abort_flag && t.tail >= 0) {
+      if (kTail && ok && !partials && !*abort_flag && t.tail >= 0) {
         // a K part of a last-wave tile: its fp32 sums, every row and output of
         // the tile (rows and outputs past the matrix hold finite values the
         // reduce pass never reads), 128 contiguous bytes per warp and token
@@ -764,10 +769,12 @@ cudaError_t widen(const void* src, void* dst, int64_t rows, int64_t K, bool fp8,
 //    / s waves of t, plus 8 s M N bytes;
 //  * the last wave only, when it is at most half full: the whole waves as they
 //    are, then each of its r tiles in s parts (2 to 16, at least 256 k each):
-//    ceil(r s / 152) waves of t / s, plus 2 * 4 r s 128 * 256 bytes.
+//    ceil(r s / 152) waves of t / s, plus 2 * 4 r s 128 * 256 bytes, plus the
+//    measured costs of that kernel instantiation (below).
 // Parts are cut on 128-k stages and on group boundaries. At 4096 x 11008 x
-// 4096 the second form splits the 8 tiles of the tenth wave; at 512 x 4096 x
-// 4096 the first takes two parts. Fixed figures keep the choice, and the
+// 4096 the second form only just wins (the tenth wave's 8 tiles), at 16384 x
+// 3072 x 3072 it splits the last 16 tiles, and at 512 x 4096 x 4096 the
+// first form takes two parts. Fixed figures keep the choice, and the
 // workspace it needs, the same on every device.
 constexpr int kSplitSms = 152;
 struct Split {
@@ -811,13 +818,17 @@ Split choose_split(int64_t M, int64_t N, int64_t K, int32_t group) {
   const int64_t r = tiles % kSplitSms;
   if (tiles > kSplitSms && r > 0 && 2 * r <= kSplitSms) {
     const int64_t full = tiles - r;
+    // measured on GB300: the instantiation that splits the last wave runs its
+    // whole tiles ~4% slower when the group is smaller than K, and the short
+    // items' fill, drain and the reduce cost ~8 us in all
+    const double slow = group < K ? 1.04 : 1.0, fixed = 8e-6;
     for (int sp = 2; sp <= 16; ++sp) {
       if (K / sp < 256) break;
       const int64_t ks = part_k(sp);
       if (ks == 0) continue;
-      const double t = static_cast<double>(full / kSplitSms) * t_tile +
+      const double t = static_cast<double>(full / kSplitSms) * t_tile * slow +
                        static_cast<double>((r * sp + kSplitSms - 1) / kSplitSms) * t_tile / sp +
-                       2.0 * 4.0 * r * sp * BM * BN / 6.8e12 + launch;
+                       2.0 * 4.0 * r * sp * BM * BN / 6.8e12 + fixed;
       if (t < best_t) {
         best_t = t;
         best = Split{1, static_cast<int>(K), sp, static_cast<int>(ks), full, r};
@@ -839,7 +850,8 @@ cudaError_t run_t(const W4A8Args& a, int mode, cudaStream_t s) {
   using C = Cfg<2, FP8>;
   // set on every call: the attribute belongs to the current device, and a
   // once-per-process flag would race between host threads
-  cudaError_t e = cudaFuncSetAttribute(w4a8_tc_kernel<2, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t e = cudaFuncSetAttribute(w4a8_tc_kernel<2, FP8, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::SMEM);
   if (e != cudaSuccess) return e;
   const bool experts = mode == kExperts;
   // the activation operand TMA reads: the e4m3 codes themselves (fp8 path),
@@ -927,8 +939,17 @@ cudaError_t run_t(const W4A8Args& a, int mode, cudaStream_t s) {
   p.items = static_cast<int>(total);
   // persistent: one CTA per SM (the shared-memory rings fill an SM)
   const long long grid = total < sm_count_w4a8() ? total : sm_count_w4a8();
-  w4a8_tc_kernel<2, FP8><<<static_cast<unsigned>(grid), kThreads, C::SMEM, s>>>(p, n_tiles,
-                                                                                 static_cast<int>(y_tiles));
+  if (p.tail_splits > 1) {
+    if constexpr (!FP8) {   // dense only
+      e = cudaFuncSetAttribute(w4a8_tc_kernel<2, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+      if (e != cudaSuccess) return e;
+      w4a8_tc_kernel<2, false, true><<<static_cast<unsigned>(grid), kThreads, C::SMEM, s>>>(p, n_tiles,
+                                                                                          static_cast<int>(y_tiles));
+    }
+  } else {
+    w4a8_tc_kernel<2, FP8, false><<<static_cast<unsigned>(grid), kThreads, C::SMEM, s>>>(p, n_tiles,
+                                                                                        static_cast<int>(y_tiles));
+  }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (p.tail_splits > 1) {

@@ -190,12 +190,12 @@ def test_w4a8_bf16in_full_size(M, N, K, group, outliers):
                       f"bf16in full size {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("M,N,K,group,bias", [(300, 10240, 1024, 128, True), (700, 6656, 1024, 64, False),
+@pytest.mark.parametrize("M,N,K,group,bias", [(300, 10240, 2048, 128, True), (700, 6656, 2048, 64, False),
                                               (1000, 5120, 2048, -1, True)])
 def test_w4a8_last_wave_split(M, N, K, group, bias):
     """Shapes whose last wave of tiles would leave most SMs idle (160, 156 and
     160 tiles on 152 SMs): the whole waves run as tiles, the last wave's 8, 4
-    and 8 tiles in 4, 4 and 8 K parts whose fp32 sums a reduce pass adds. The
+    and 8 tiles in 8 K parts each, whose fp32 sums a reduce pass adds. The
     split tiles are the last ones, in the last, ragged row tile. Outputs on
     every row of that tile and on rows of the whole tiles, against the oracle;
     the same call with only the minimal workspace (unsplit) likewise."""
