@@ -47,6 +47,14 @@ def test_quant_warp_form(kind, M, K):
 
 
 @pytest.mark.parametrize("kind", ["int8", "fp8"])
+@pytest.mark.parametrize("M,K", [(1300, 5000), (1300, 6144), (1300, 8192), (1300, 4096)])
+def test_quant_many_long_rows(kind, M, K):
+    """At least 8 rows per SM with rows longer than 3072: one CTA of up to 128
+    threads per row, 5 (rounded up to 6), 6, 8 and 4 chunks a thread."""
+    _check(S.activations_bf16(M, K, seed=M + K, outlier_frac=0.01), kind)
+
+
+@pytest.mark.parametrize("kind", ["int8", "fp8"])
 def test_quant_special_rows(kind):
     """Zero rows (s = 1), rows whose amax is the code maximum (s = 1, ties at
     x.5), tiny and huge magnitudes, rows whose scale is subnormal, and sign
