@@ -129,13 +129,17 @@ W4_DEV uint32_t pack_f16x2(float lo, float hi) {
   return d;
 }
 
-// Shared-memory carve-up (byte offsets from the 1024-aligned base).
+// Shared-memory carve-up (byte offsets from the 1024-aligned base). The strip
+// partials take [pstrips][kConsumers][rows][kStrip] floats, or with the
+// partials in tensor memory only their per-quadrant sums, [pstrips][4][32
+// lanes][8] floats.
 struct Layout {
   int scl, red, bars, xrdy, exs, xsum, xs, total;
-  __host__ __device__ Layout(int nseg, int xchunks, int rows, int ring, int scb, int pstrips) {
+  __host__ __device__ Layout(int nseg, int xchunks, int rows, int ring, int scb, int pstrips, bool tmem_red) {
     scl = ring * kStageBytes;             // ring x scb: scale (and zero) rows per slot
-    red = scl + ring * scb;               // [pstrips][kConsumers][rows][kStrip] strip partials
-    bars = red + pstrips * kConsumers * rows * kStrip * 4;   // full, per-warp x, slot counters, abort flag
+    red = scl + ring * scb;               // strip partials, or their quadrant sums
+    bars = red + (tmem_red ? pstrips * 4 * 32 * 8 * 4 : pstrips * kConsumers * rows * kStrip * 4);
+    // bars: full, per-warp x, slot counters, abort flag, the TMEM base
     xrdy = bars + 512;                    // [nseg] mbarriers: x segment converted
     exs = xrdy + nseg * 8;                // [nseg][kTok] 2^-e per segment and token
     xsum = exs + nseg * kTok * 4;         // [nseg * 4][kTok] 2^-24 sums of x over 64-k blocks
@@ -178,7 +182,14 @@ __global__ void __launch_bounds__(32) w4a16_prefetch_kernel(const uint8_t* w, si
 // 120 registers a thread, not the 128 that 512 threads could have: a
 // sub-partition then keeps room for the one-warp prefetch grid of the next
 // call (4 x 32 x 120 + 768 <= 16384), which must run beside this grid.
-template <bool kScaleBf16, bool kZero, int kSPF>
+// tot is set at every strip change before flush reads it; the compiler cannot
+// see that through the lambda (a zero initializer measurably changes the
+// register allocation of every instantiation, so the warning is silenced)
+#pragma nv_diag_suppress 549
+// kTmemRed: the warps' strip partials go to tensor memory instead of shared
+// memory (at M = 5..8 the shared-memory partials would cost the ring half its
+// depth); the block sums them per TMEM lane quadrant, then across quadrants.
+template <bool kScaleBf16, bool kZero, int kSPF, bool kTmemRed>
 __global__ void __maxnreg__(120) w4a16_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
@@ -187,7 +198,7 @@ __global__ void __maxnreg__(120) w4a16_kernel(const __grid_constant__ Params p) 
   const int M = p.M;
   const int nseg = S * (kStageK / kUnitK);   // 256-k x segments (padded to whole stages)
   const int xch = p.xstride / 8;             // 16-byte chunks per token row
-  const Layout L(nseg, xch, M, R, p.scb, p.pstrips);
+  const Layout L(nseg, xch, M, R, p.scb, p.pstrips, kTmemRed);
   uint8_t* ring = smem;                                      // R x 16 KB, 1024-aligned
   const uint8_t* scl = smem + L.scl;                         // R x scb
   float* red = reinterpret_cast<float*>(smem + L.red);
@@ -195,6 +206,10 @@ __global__ void __maxnreg__(120) w4a16_kernel(const __grid_constant__ Params p) 
   uint64_t* xbar = full + kRingMax;                          // [kConsumers] a warp's x copies landed
   unsigned int* done = reinterpret_cast<unsigned int*>(xbar + kConsumers);   // [kRingMax] units finished per slot
   volatile int* abort_flag = reinterpret_cast<volatile int*>(done + kRingMax);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.bars + 256);
+  // TMEM columns: 8 per (local strip, warp / 4) in each lane quadrant
+  uint32_t tmem_cols = 32;
+  while (kTmemRed && tmem_cols < 32u * static_cast<uint32_t>(p.pstrips)) tmem_cols <<= 1;
   uint64_t* xrdy = reinterpret_cast<uint64_t*>(smem + L.xrdy);
   float* exs = reinterpret_cast<float*>(smem + L.exs);
   float* xsum = reinterpret_cast<float*>(smem + L.xsum);
@@ -211,9 +226,24 @@ __global__ void __maxnreg__(120) w4a16_kernel(const __grid_constant__ Params p) 
     *abort_flag = 0;
     fence_mbar_init();
   }
+  if (kTmemRed && warp == 0) tc::tmem_alloc(tmem_holder, tmem_cols);
+  if (kTmemRed) tc::fence_before_sync();
   __syncthreads();
+  if (kTmemRed) tc::fence_after_sync();
 
   const int my_strips = p.strips > (int)blockIdx.x ? (p.strips - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  // this warp's columns for local strip su, in its lane quadrant
+  const uint32_t tmem = kTmemRed ? *tmem_holder : 0u;
+  auto tcol = [&](int su) {
+    return tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + static_cast<uint32_t>((su * 4 + (warp >> 2)) * 8);
+  };
+  if (kTmemRed) {
+    // zeros for the strips this warp contributes nothing to (fewer than 16
+    // units a strip), written before any partial of the same columns
+    const uint32_t zero[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    for (int su = 0; su < my_strips; ++su) tc::tmem_st8(tcol(su), zero);
+    tc::tmem_wait_st();
+  }
 
   // the next call on the stream may start now: its grids do not touch this
   // call's x or y before they wait for it
@@ -298,6 +328,13 @@ __global__ void __maxnreg__(120) w4a16_kernel(const __grid_constant__ Params p) 
     int cur = -1;                                        // strip whose partial tot holds
     bool ok = true;
     auto flush = [&](int su) {
+      if constexpr (kTmemRed) {
+        const uint32_t v[8] = {__float_as_uint(tot[0][0]), __float_as_uint(tot[0][1]), __float_as_uint(tot[0][2]),
+                               __float_as_uint(tot[0][3]), __float_as_uint(tot[1][0]), __float_as_uint(tot[1][1]),
+                               __float_as_uint(tot[1][2]), __float_as_uint(tot[1][3])};
+        tc::tmem_st8(tcol(su), v);
+        return;
+      }
       float* dst = red + (su * kConsumers + warp) * M * kStrip;
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
@@ -449,17 +486,44 @@ __global__ void __maxnreg__(120) w4a16_kernel(const __grid_constant__ Params p) 
       }
     }
     if (ok && cur >= 0) flush(cur);
+    if (kTmemRed) {
+      tc::tmem_wait_st();
+      tc::fence_before_sync();
+    }
     __syncthreads();
+    if (kTmemRed && !*abort_flag) {
+      // ---- the partials of the four warps of each TMEM lane quadrant, summed
+      // in warp order: lane l holds (token 2c + i % 2, output 4r + 2j + i / 2)
+      // in column 4j + i, r = l / 4, c = l % 4 ----
+      tc::fence_after_sync();
+      for (int su = warp >> 2; su < my_strips; su += 4) {
+        uint32_t v[32];
+        tc::tmem_ld32(tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + static_cast<uint32_t>(su * 32), v);
+        float* qd = red + ((su * 4 + (warp & 3)) * 32 + lane) * 8;
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          qd[e] = ((__uint_as_float(v[e]) + __uint_as_float(v[8 + e])) + __uint_as_float(v[16 + e])) +
+                  __uint_as_float(v[24 + e]);
+      }
+      tc::fence_before_sync();
+      __syncthreads();
+    }
     if (!*abort_flag) {
       // ---- sum the strip partials of the warps that worked on each strip in
-      // a fixed order, scale back, add the bias, write y ----
+      // a fixed order (with TMEM partials: the quadrant sums in order), scale
+      // back, add the bias, write y ----
       const int nout = my_strips * M * kStrip;
       for (int o = threadIdx.x; o < nout; o += kConsumers * 32) {
         const int su = o / (M * kStrip), m = (o / kStrip) % M, nl = o % kStrip;
         const int n = (blockIdx.x + su * gridDim.x) * kStrip + nl;
         const int v0 = su * units, v1 = v0 + min(units, kConsumers);
         float s = 0.f;
-        for (int vv = v0; vv < v1; ++vv) s += red[((su * kConsumers + vv % kConsumers) * M + m) * kStrip + nl];
+        if constexpr (kTmemRed) {
+          const int ln = 4 * (nl >> 2) + (m >> 1), e = 4 * ((nl >> 1) & 1) + 2 * (nl & 1) + (m & 1);
+          for (int qq = 0; qq < 4; ++qq) s += red[((su * 4 + qq) * 32 + ln) * 8 + e];
+        } else {
+          for (int vv = v0; vv < v1; ++vv) s += red[((su * kConsumers + vv % kConsumers) * M + m) * kStrip + nl];
+        }
         if (n < p.N) {
           s *= 16777216.f;                                       // undo 2^-24 (exact)
           if (p.bias != nullptr) s += __uint_as_float(static_cast<uint32_t>(p.bias[n]) << 16);
@@ -468,6 +532,11 @@ __global__ void __maxnreg__(120) w4a16_kernel(const __grid_constant__ Params p) 
       }
     }
   }
+  if (kTmemRed && warp == 0) {
+    // every TMEM load and store of the block completed before the last barrier
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, tmem_cols);
+  }
   if (*abort_flag) {
     // let copies already issued land before the shared memory goes away
     const uint64_t t0 = tc::globaltimer_ns();
@@ -475,6 +544,8 @@ __global__ void __maxnreg__(120) w4a16_kernel(const __grid_constant__ Params p) 
     }
   }
 }
+
+#pragma nv_diag_default 549
 
 int sm_count() { return current_sm_count(); }
 
@@ -537,10 +608,10 @@ int x_stride(int K) {
   return stages * kStageK + 8;   // +16 bytes: token rows start in different banks
 }
 
-size_t smem_bytes(int K, int rows, int ring, int scb, int pstrips) {
+size_t smem_bytes(int K, int rows, int ring, int scb, int pstrips, bool tmem_red = false) {
   const int stages = (K + kStageK - 1) / kStageK;
   return 1024 + static_cast<size_t>(
-                    Layout(stages * (kStageK / kUnitK), x_stride(K) / 8, rows, ring, scb, pstrips).total);
+                    Layout(stages * (kStageK / kUnitK), x_stride(K) / 8, rows, ring, scb, pstrips, tmem_red).total);
 }
 constexpr size_t kSmemMax = 227 * 1024;
 
@@ -560,8 +631,8 @@ cudaLaunchConfig_t pdl_config(int grid, int block, size_t smem, cudaStream_t s, 
 }
 
 template <bool kScaleBf16, bool kZero, int kSPF>
-cudaError_t launch_t(const Params& p, int grid, size_t smem, cudaStream_t s) {
-  auto k = w4a16_kernel<kScaleBf16, kZero, kSPF>;
+cudaError_t launch_t(const Params& p, bool tmem_red, int grid, size_t smem, cudaStream_t s) {
+  auto k = tmem_red ? w4a16_kernel<kScaleBf16, kZero, kSPF, true> : w4a16_kernel<kScaleBf16, kZero, kSPF, false>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
@@ -570,12 +641,12 @@ cudaError_t launch_t(const Params& p, int grid, size_t smem, cudaStream_t s) {
 }
 
 template <bool kScaleBf16>
-cudaError_t launch_spf(const Params& p, bool z, int spf, int grid, size_t smem, cudaStream_t s) {
+cudaError_t launch_spf(const Params& p, bool z, int spf, bool tr, int grid, size_t smem, cudaStream_t s) {
   switch (spf) {
-    case 2: return z ? launch_t<kScaleBf16, true, 2>(p, grid, smem, s) : launch_t<kScaleBf16, false, 2>(p, grid, smem, s);
-    case 4: return z ? launch_t<kScaleBf16, true, 4>(p, grid, smem, s) : launch_t<kScaleBf16, false, 4>(p, grid, smem, s);
-    case 8: return z ? launch_t<kScaleBf16, true, 8>(p, grid, smem, s) : launch_t<kScaleBf16, false, 8>(p, grid, smem, s);
-    default: return z ? launch_t<kScaleBf16, true, 0>(p, grid, smem, s) : launch_t<kScaleBf16, false, 0>(p, grid, smem, s);
+    case 2: return z ? launch_t<kScaleBf16, true, 2>(p, tr, grid, smem, s) : launch_t<kScaleBf16, false, 2>(p, tr, grid, smem, s);
+    case 4: return z ? launch_t<kScaleBf16, true, 4>(p, tr, grid, smem, s) : launch_t<kScaleBf16, false, 4>(p, tr, grid, smem, s);
+    case 8: return z ? launch_t<kScaleBf16, true, 8>(p, tr, grid, smem, s) : launch_t<kScaleBf16, false, 8>(p, tr, grid, smem, s);
+    default: return z ? launch_t<kScaleBf16, true, 0>(p, tr, grid, smem, s) : launch_t<kScaleBf16, false, 0>(p, tr, grid, smem, s);
   }
 }
 
@@ -638,9 +709,15 @@ cudaError_t launch_w4a16(const W4A16Args& a, cudaStream_t s) {
     p.y = static_cast<uint16_t*>(a.y) + m0 * a.N;
     p.M = static_cast<int>(a.M - m0 < block ? a.M - m0 : block);
     p.ring = bytes(p.M, 8) <= kSmemMax ? 8 : 4;
+    // when the shared-memory partials cost the ring half its depth, the
+    // partials go to tensor memory (8 columns per strip and warp group:
+    // at most 16 strips a CTA in its 512 columns)
+    const bool tmem_red = p.ring == 4 && p.pstrips <= 16 && smem_bytes(p.K, p.M, 8, p.scb, p.pstrips, true) <= kSmemMax;
+    if (tmem_red) p.ring = 8;
     p.ring_shift = p.ring == 8 ? 3 : 2;
-    const size_t smem = bytes(p.M, p.ring);
-    e = a.scale_bf16 ? launch_spf<true>(p, z, spf, grid, smem, s) : launch_spf<false>(p, z, spf, grid, smem, s);
+    const size_t smem = smem_bytes(p.K, p.M, p.ring, p.scb, p.pstrips, tmem_red);
+    e = a.scale_bf16 ? launch_spf<true>(p, z, spf, tmem_red, grid, smem, s)
+                     : launch_spf<false>(p, z, spf, tmem_red, grid, smem, s);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

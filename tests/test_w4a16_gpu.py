@@ -56,6 +56,16 @@ def test_w4a16_variants(scale_dtype, zeros, bias):
     _case(4, 328, 1024, 128, scale_dtype=scale_dtype, zeros=zeros, bias=bias, seed=11)
 
 
+@pytest.mark.parametrize("M,N,K,group,zeros,bias", [(8, 6400, 4096, 128, False, True), (5, 5120, 8192, 128, False, False),
+                                                    (7, 20000, 2048, 64, False, True), (6, 20000, 3072, -1, True, True)])
+def test_w4a16_partials_in_tensor_memory(M, N, K, group, zeros, bias):
+    """Token blocks whose strip partials in shared memory would leave room for
+    only a 4-deep ring: the partials go to tensor memory. 16, 32, 8 and 12
+    units of 256 k a strip (8 and 12: some warps add nothing to a strip, whose
+    columns stay zero), 2 to 5 strips a CTA; every output column."""
+    _case(M, N, K, group, zeros=zeros, bias=bias, seed=M + K)
+
+
 @pytest.mark.parametrize("M", [9, 17, 40])
 def test_w4a16_more_than_8_tokens(M):
     _case(M, 136, 512, 64, zeros=True, bias=True, seed=M)
