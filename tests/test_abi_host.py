@@ -264,3 +264,21 @@ def test_w4a16_host_entry_validation(lib):
     assert call(wdt=w4.W4_INT8) == w4.W4_ERR_DTYPE
     assert call(group=96) == w4.W4_ERR_GROUP
     assert call(M=0, xh=None, yh=None) == w4.W4_OK
+
+
+@pytest.mark.parametrize("M,N,K,group,extra", [
+    (4096, 11008, 4096, 128, 8 * 11 * 128 * 256 * 4),    # 1,376 tiles: the last wave's 8 in 11 K parts
+    (16384, 3072, 3072, -1, 16 * 8 * 128 * 256 * 4),     # 1,536 tiles: the last 16 in 8 parts
+    (4096, 4096, 4096, 128, 56 * 2 * 128 * 256 * 4),     # 512 tiles: the last 56 in 2 parts
+    (512, 4096, 4096, 128, 2 * 512 * 4096 * 4),          # 64 tiles: every tile in 2 parts
+    (300, 264, 2048, 128, 4 * 300 * 264 * 4),            # 6 tiles: every tile in 4 parts
+    (1024, 4096, 4096, 128, 0),                          # 128 tiles: one wave, no split
+    (2048, 11008, 4096, 128, 0),                         # 688 tiles: the last wave over half full, no split
+    (300, 10240, 1024, 128, 0),                          # a last-wave split would not pay at K = 1024
+])
+def test_w4a8_split_plans(lib, M, N, K, group, extra):
+    """The W4A8 workspace holds the widened activations (M K 2 bytes) plus the
+    fp32 partial sums of the plan the GEMM takes: none, every tile split along
+    K, or only the last wave's tiles split (compact [tile][part][256][128]).
+    The plan is fixed arithmetic over a 152-SM GB300, so it is the same here."""
+    assert lib.w4_workspace_bytes(w4.W4_OP_W4A8, M, N, K, group) == M * K * 2 + extra
