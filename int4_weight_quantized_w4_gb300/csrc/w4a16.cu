@@ -74,7 +74,8 @@ constexpr int kStrip = 32;          // output columns per strip
 constexpr int kStageRows = 128;     // word rows per stage (1024 k)
 constexpr int kStageK = kStageRows * 8;
 constexpr int kStageBytes = kStrip * kStageRows * 4;   // 16 KB
-constexpr int kRingMax = 8;
+constexpr int kRingMax = 16;      // stage barriers: a ring of 4 or 8, or up to 16 resident stages
+constexpr int kFirstFill = 8;     // stages issued when the CTA starts
 constexpr int kConsumers = 16;
 constexpr int kUnitRows = 32;       // word rows per consumer unit (256 k, 8 steps)
 constexpr int kUnitK = kUnitRows * 8;
@@ -94,7 +95,9 @@ struct Params {
   int M, N, K, group;    // M <= 8 here
   int strips, stages;    // per strip: stages = ceil(K / 1024)
   int xstride;           // shared-memory row stride of x, in fp16 elements
-  int ring;              // stages in the ring: 4 or 8
+  int ring;              // stage index -> slot i & (ring - 1): 4 or 8, or 16 when resident
+  int slots;             // stage slots in shared memory (ring, or every stage of a CTA when resident)
+  int resident;          // every stage of a CTA has its own slot: no slot is ever refilled
   int gh;                // scale rows per stage tile: most groups one stage's k range meets
   int zoff;              // byte offset of the zero rows inside a slot's scale area
   int scb;               // bytes of one slot's scale area (scales, then zeros)
@@ -198,15 +201,15 @@ __global__ void __maxnreg__(120) w4a16_kernel(const __grid_constant__ Params p) 
   const int M = p.M;
   const int nseg = S * (kStageK / kUnitK);   // 256-k x segments (padded to whole stages)
   const int xch = p.xstride / 8;             // 16-byte chunks per token row
-  const Layout L(nseg, xch, M, R, p.scb, p.pstrips, kTmemRed);
-  uint8_t* ring = smem;                                      // R x 16 KB, 1024-aligned
-  const uint8_t* scl = smem + L.scl;                         // R x scb
+  const Layout L(nseg, xch, M, p.slots, p.scb, p.pstrips, kTmemRed);
+  uint8_t* ring = smem;                                      // slots x 16 KB, 1024-aligned
+  const uint8_t* scl = smem + L.scl;                         // slots x scb
   float* red = reinterpret_cast<float*>(smem + L.red);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* xbar = full + kRingMax;                          // [kConsumers] a warp's x copies landed
   unsigned int* done = reinterpret_cast<unsigned int*>(xbar + kConsumers);   // [kRingMax] units finished per slot
   volatile int* abort_flag = reinterpret_cast<volatile int*>(done + kRingMax);
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.bars + 256);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.bars + 384);
   // TMEM columns: 8 per (local strip, warp / 4) in each lane quadrant
   uint32_t tmem_cols = 32;
   while (kTmemRed && tmem_cols < 32u * static_cast<uint32_t>(p.pstrips)) tmem_cols <<= 1;
@@ -263,8 +266,10 @@ __global__ void __maxnreg__(120) w4a16_kernel(const __grid_constant__ Params p) 
     if (kZero) tc::tma_load_2d(sdst + p.zoff, &p.tm_z, &full[slot], col, gst);
   };
   // initial fill: warp w issues stage w, so no one warp spends its start
-  // issuing the whole ring (a TMA issue can stall while the copy engine is busy)
-  if (lane == 0 && warp < R && warp < total) {
+  // issuing the whole ring (a TMA issue can stall while the copy engine is busy).
+  // With resident stages the ones past the first eight wait for the x
+  // prologue: issued all at once (measured), they delay the first tiles.
+  if (lane == 0 && warp < R && warp < kFirstFill && warp < total) {
     tc::prefetch_tmap(&p.tm_w);
     tc::prefetch_tmap(&p.tm_s);
     if (kZero) tc::prefetch_tmap(&p.tm_z);
@@ -315,6 +320,8 @@ __global__ void __maxnreg__(120) w4a16_kernel(const __grid_constant__ Params p) 
       __syncwarp();
       if (lane == 0) mbar_arrive(&xrdy[u]);   // releases this warp's writes of the segment
     }
+
+    if (p.resident && lane == 0 && warp >= kFirstFill && warp < total) issue(warp);
 
     // ---- main loop over this warp's 256-k units ----
     const int r = lane >> 2, c = lane & 3;
@@ -471,7 +478,8 @@ __global__ void __maxnreg__(120) w4a16_kernel(const __grid_constant__ Params p) 
       // the last of the four units of round i / R reads 4 (i / R) + 3). Every
       // reading thread orders its generic-proxy reads of the slot before the
       // asynchronous copy that will overwrite it, before the warp counts the
-      // unit done.
+      // unit done. Resident stages are never overwritten: nothing to count.
+      if (p.resident) continue;
       tc::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
@@ -714,8 +722,19 @@ cudaError_t launch_w4a16(const W4A16Args& a, cudaStream_t s) {
     // at most 16 strips a CTA in its 512 columns)
     const bool tmem_red = p.ring == 4 && p.pstrips <= 16 && smem_bytes(p.K, p.M, 8, p.scb, p.pstrips, true) <= kSmemMax;
     if (tmem_red) p.ring = 8;
-    p.ring_shift = p.ring == 8 ? 3 : 2;
-    const size_t smem = smem_bytes(p.K, p.M, p.ring, p.scb, p.pstrips, tmem_red);
+    p.slots = p.ring;
+    p.resident = 0;
+    // every stage of a CTA in its own slot when they fit: no slot is
+    // refilled, so the units skip the per-unit release (fences, counter,
+    // refill copy), which measured as long as a unit's math
+    const int share = p.pstrips * p.stages;
+    if (!tmem_red && share <= kRingMax && bytes(p.M, share) <= kSmemMax) {
+      p.ring = share <= 8 ? 8 : kRingMax;
+      p.slots = share;
+      p.resident = 1;
+    }
+    p.ring_shift = p.ring == 16 ? 4 : p.ring == 8 ? 3 : 2;
+    const size_t smem = smem_bytes(p.K, p.M, p.slots, p.scb, p.pstrips, tmem_red);
     e = a.scale_bf16 ? launch_spf<true>(p, z, spf, tmem_red, grid, smem, s)
                      : launch_spf<false>(p, z, spf, tmem_red, grid, smem, s);
     if (e != cudaSuccess) return e;
