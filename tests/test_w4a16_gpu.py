@@ -66,6 +66,17 @@ def test_w4a16_partials_in_tensor_memory(M, N, K, group, zeros, bias):
     _case(M, N, K, group, zeros=zeros, bias=bias, seed=M + K)
 
 
+@pytest.mark.parametrize("M,N,K,group,zeros", [(1, 20000, 2048, 128, False), (1, 4096, 8192, 64, True),
+                                               (1, 6400, 3072, -1, False), (2, 14336, 4096, 128, False),
+                                               (1, 9728, 5120, 128, True)])
+def test_w4a16_resident_stages(M, N, K, group, zeros):
+    """Shares of a CTA (strips x 1024-k stages) that take a slot per stage:
+    five strips of 2 stages and two strips of 5 (10, on 16-slot indexing),
+    one strip of 8, two strips of 3; and three strips of 4 at M = 2, whose
+    shared memory does not fit them (the refilled ring)."""
+    _case(M, N, K, group, zeros=zeros, seed=N + K)
+
+
 @pytest.mark.parametrize("M", [9, 17, 40])
 def test_w4a16_more_than_8_tokens(M):
     _case(M, 136, 512, 64, zeros=True, bias=True, seed=M)
