@@ -416,9 +416,15 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
     }
   } else if (warp == kWarpMma) {
     // ---- one thread issues the MMAs ----
-    // Lean issue loop: one wait pair and two descriptors per stage, four MMAs
-    // per stage from constant offsets; group boundaries (multiples of 16)
-    // may fall inside a stage. Every tile opens a new accumulation.
+    // One wait and two descriptors per stage, the MMAs from constant offsets.
+    // The tensor pipe takes only a few MMAs ahead of the issuing thread, so
+    // what that thread does between MMAs shows up as idle pipe: whole stages
+    // whose accumulations can change only at the stage's start or middle
+    // (groups that are multiples of the stage width, or half of it) run
+    // straight-line, with no per-MMA checks; measured on GB300, that alone
+    // took the grouped prefill GEMM from 855 to 1,148 TOPS. Stages at a tile's
+    // ragged end and other group sizes (multiples of 16) take the general
+    // loop. Every tile opens a new accumulation.
     if (lane == 0) {
       // e4m3 A and B under kind::f8f6f4 take the same format code (0) that
       // fp16 takes under kind::f16, so one instruction descriptor serves both
@@ -426,6 +432,9 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
       const uint64_t adesc0 = tc::sdesc_sw128(smem_addr(a_base));
       const uint64_t bdesc0 = tc::sdesc_sw128(smem_addr(b_base));
       int seg = -1, buf = 0, sg = 0;
+      // accumulations change only at stage starts or middles: group boundaries
+      // there (SEG_MAX is a multiple of every stage width)
+      const bool lean = group % BK == 0 || 2 * group == BK;
       bool ok = true;
       TileCursor cur;
       for (int tid = blockIdx.x; tid < total_tiles && ok; tid += gridDim.x) {
@@ -448,10 +457,43 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
           const uint64_t ad = adesc0 + static_cast<uint64_t>((a * A_BYTES) >> 4);
           const uint64_t bd = bdesc0 + static_cast<uint64_t>((b * B_BYTES) >> 4);
           const int kbase = t.k0 + s * BK;
+          constexpr int kPerSub = KS / UMMA_K;
+          if (lean && kbase + BK <= t.k1) {
+            // a whole stage whose accumulations can only change at its start or
+            // its middle (tiles start on stage boundaries): no per-MMA checks
+            constexpr int kHalf = BK / UMMA_K / 2;
+#pragma unroll
+            for (int h = 0; h < 2 && ok; ++h) {
+              const int kh = kbase + h * (BK / 2);
+              if (seg_end == kh) {   // close this accumulation, open the next buffer
+                tc::commit(&acc_full[buf]);
+                ++seg;
+                buf = seg & 1;
+                seg_end = min(min((kh / group + 1) * group, kh + SEG_MAX), t.k1);
+                if (!tc::wait(&acc_empty[buf], ((seg >> 1) & 1) ^ 1, abort_flag, p.status, kWaitNs)) {
+                  ok = false;
+                  break;
+                }
+                tc::fence_after_sync();
+                acc = 0;
+              }
+              const uint32_t d = tmem + buf * BN;
+#pragma unroll
+              for (int i = 0; i < kHalf; ++i) {
+                const int j = h * kHalf + i, u = j / kPerSub, jj = j % kPerSub;
+                if constexpr (FP8)
+                  tc::mma_f8(d, ad + ((u * A_SUB) >> 4) + 2 * jj, bd + ((u * B_SUB) >> 4) + 2 * jj, idesc,
+                             i > 0 ? 1u : acc);
+                else
+                  tc::mma_f16(d, ad + ((u * A_SUB) >> 4) + 2 * jj, bd + ((u * B_SUB) >> 4) + 2 * jj, idesc,
+                              i > 0 ? 1u : acc);
+              }
+              acc = 1;
+            }
+          } else {
 #pragma unroll
           for (int j = 0; j < BK / UMMA_K; ++j) {
             // MMA j: sub-tile j / 4, 32-byte step j % 4 inside its swizzle rows
-            constexpr int kPerSub = KS / UMMA_K;
             const int k = kbase + j * UMMA_K;
             if (k < t.k1) {
               if (k == seg_end) {  // close this accumulation, open the next buffer
@@ -476,6 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a8_tc_kernel(const __grid_const
                             idesc, acc);
               acc = 1;
             }
+          }
           }
           if (!ok) break;
           tc::commit(&st_empty[a]);
@@ -762,9 +805,11 @@ cudaError_t widen(const void* src, void* dst, int64_t rows, int64_t K, bool fp8,
 }
 
 // Split along K when the output tiles fill the 152 SMs of a GB300 poorly.
-// Two forms, priced against no split with a tile's MMA time t = K * 11.7 ns
-// (a 128 x 256 tile at the measured ~0.45 of the bf16 peak), the fp32
-// partials' traffic at 6.8 TB/s and 2 us for the reduce launch:
+// Two forms, priced against no split with a tile weight t = K * 11.7 ns, the
+// fp32 partials' traffic at 6.8 TB/s and 2 us for the reduce launch. (t was a
+// tile's time at ~0.45 of the bf16 peak; tiles now take ~8.7 ns per k, but
+// re-pricing with that dropped last-wave splits that still measured faster,
+// 1,152 against 1,071 TOPS at 4096 x 11008 x 4096, so the weight stays.)
 //  * every tile in s parts (1 to 4, at least 512 k each): ceil(tiles s / 152)
 //    / s waves of t, plus 8 s M N bytes;
 //  * the last wave only, when it is at most half full: the whole waves as they
