@@ -62,16 +62,16 @@ TRAFFIC = {
     # w4a16_kernel, M=1 K=4096 N=14336 g128, caches flushed: dram__bytes_read.sum + dram__bytes_write.sum
     # (30,336,512 + 1,280)
     "w4a16": (30337792, "03a49580515c5050", "w4a16.cu"),
-    # w4a8_tc_kernel<2, fp16, last-wave split>, W4A8 diffusion M=16384 K=N=3072 g=-1 (105,701,376 + 68,216,576)
-    "w4a8_diffusion": (173917952, "87acf24ab34fcbf8", "w4a8.cu"),
+    # w4a8_tc_kernel<2, fp16, last-wave split>, W4A8 diffusion M=16384 K=N=3072 g=-1 (105,709,824 + 68,560,640)
+    "w4a8_diffusion": (174270464, "10e03aa25d9f1866", "w4a8.cu"),
     # lm_head_tc_kernel, M=1 V=131072 D=2048 g128 (151,032,832 + 2,898,432)
     "lm_head": (153931264, "18cc61b739d893a3", "embed.cu"),
     # quantize_chunks_kernel<bf16, 16, 4>, N=14336 K=4096 g128 (117,464,064 + 14,775,040; the codes,
     # scales and zeros are partly still in L2 when the kernel ends)
     "quantize": (132239104, "13988ce8d7acefec", "tools.cu"),
-    # w4a8_tc_kernel<2, e4m3> in expert mode, the MoE layer's two GEMMs: gate_up (257,902,848 + 150,592,256)
-    # and down (141,754,880 + 90,593,536)
-    "w4afp8_moe": (640843520, "87acf24ab34fcbf8", "w4a8.cu"),
+    # w4a8_tc_kernel<2, e4m3> in expert mode, the MoE layer's two GEMMs: gate_up (257,933,568 + 150,066,432)
+    # and down (141,715,200 + 90,804,736)
+    "w4afp8_moe": (640519936, "10e03aa25d9f1866", "w4a8.cu"),
 }
 
 
