@@ -39,12 +39,14 @@ def test_moe_small(counts, N, K, group):
 
 @pytest.mark.parametrize("counts,N,K,group", [([5, 0, 40], 128, 32, 32), ([5, 0, 40], 128, 32, -1),
                                               ([17, 3], 136, 96, 32), ([64] * 8, 192, 384, 128),
-                                              ([33, 100], 128, 384, 48), ([9, 250], 256, 1024, 16)])
+                                              ([33, 100], 128, 384, 48), ([9, 250], 256, 1024, 16),
+                                              ([70, 260], 136, 1280, 256)])
 def test_moe_stage_edges(counts, N, K, group):
     """Expert tiles against the 128-k stages: K shorter than one stage (32,
     96: most of the stage's MMAs skipped, a packed-word copy narrower than a
-    slot), an odd stage count whose last copy is half used (384), and groups
-    that close inside a stage (48, 16)."""
+    slot), an odd stage count whose last copy is half used (384), groups
+    that close inside a stage (48, 16), and groups of exactly one 256-k e4m3
+    stage (K = 1280, five stages)."""
     qx8, sx, off, qw, sw = _case(counts, N, K, group, seed=len(counts) + K)
     y = _run(qx8, sx, off, qw, sw, group)
     check_bf16_output(y, O.moe_grouped_linear(qx8, sx, off, qw, sw, group), f"moe edges {counts} K={K} g={group}")

@@ -68,6 +68,20 @@ def test_w4a8_outputs(M, N, K, group, bias):
     check_bf16_output(bits(y), O.w4a8_linear(qx, sx, qw, sw, group, bb), f"w4a8 M={M} N={N} K={K} g={group}")
 
 
+@pytest.mark.parametrize("M,N,K,group", [(70, 264, 1088, 64), (300, 520, 4160, 64), (40, 136, 2048, 512),
+                                         (260, 392, 1280, 256)])
+def test_w4a8_stage_paths(M, N, K, group):
+    """Whole k-stages whose accumulations change only at the stage's start or
+    middle run without per-MMA checks; a tile's ragged last stage and other
+    groups take the checked loop. Groups of 64 (two per stage) with a half
+    stage left over at the end (K = 1088, 4160), and groups spanning several
+    stages (512 over four, 256 over two with a K of ten stages)."""
+    _, qx, sx, qw, sw = _inputs(M, N, K, group, seed=M + K, outliers=0.01)
+    y = w4.w4a8_gemm(to_dev(qx), to_dev(sx), to_dev(qw), to_dev(sw), group)
+    torch.cuda.synchronize()
+    check_bf16_output(bits(y), O.w4a8_linear(qx, sx, qw, sw, group), f"w4a8 stages M={M} N={N} K={K} g={group}")
+
+
 def test_w4a8_layer_from_bf16():
     """The whole W4A8 layer: per-token int8 quantization then the GEMM, both on
     the GPU, against the oracle's quantizer and GEMM (16 tokens, K=N=256, g128)."""
