@@ -329,8 +329,9 @@ def run_ours(args, rank, world, local_rank):
                      "algorithmic_bytes_per_launch": nbytes},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": DEC_M * DEC_K * 2,
                 "d2h_bytes_per_step": DEC_M * DEC_N * 2, "steps": e2e_steps,
-                "how": "per step one w4a16_gemm_host call (C ABI, host buffers): page-locked H2D of x, the GEMM, "
-                       "D2H of y into page-locked memory; host wall clock over all steps and the final sync"},
+                "how": "per step one w4a16_gemm_host call (C ABI, host buffers): page-locked x in, the GEMM, y out "
+                       "into page-locked memory (both copies kernels chained with the GEMV); host wall clock over "
+                       "all steps and the final sync"},
         "gpu_launches": 2 * steps,   # per call: the L2 prefetch grid and the GEMV grid
         "clocks": clocks,
         "sm_count": torch.cuda.get_device_properties(dev).multi_processor_count,

@@ -223,10 +223,14 @@ w4_status w4a16_gemm(const void* x, const void* qweight, const void* w_scale, in
  * w4a16_gemm from and to host memory, for a caller whose activations and
  * results live on the host: one call queues on `stream` the copy of x_host
  * [M, K] bf16 into x_dev, the w4a16_gemm of x_dev into y_dev, and the copy of
- * y_dev [M, N] into y_host (each copy one cudaMemcpyAsync). x_dev and y_dev are
- * caller-owned device buffers (16- and 8-byte aligned). For the copies to run
- * asynchronously x_host and y_host must be page-locked; y_host holds the
- * result once `stream` has been synchronized. Other arguments and errors as
+ * y_dev [M, N] into y_host. x_dev and y_dev are caller-owned device buffers
+ * (16- and 8-byte aligned) and hold x and y afterwards. When x_host and y_host
+ * are both page-locked (16- and 8-byte aligned) the two copies are kernels
+ * chained with the GEMV's programmatic dependent launches, so consecutive
+ * calls on a stream overlap as device-only calls do; otherwise each copy is
+ * one cudaMemcpyAsync, asynchronous only for page-locked memory. y_host holds
+ * the result once `stream` has been synchronized; x_host and y_host must not
+ * be touched by the host until then. Other arguments and errors as
  * w4a16_gemm; nothing is queued when validation fails.
  */
 w4_status w4a16_gemm_host(const void* x_host, void* x_dev, const void* qweight, const void* w_scale,

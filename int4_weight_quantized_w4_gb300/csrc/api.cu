@@ -237,6 +237,18 @@ static w4_status check_w4a16(const void* x, const void* qweight, const void* w_s
   return W4_OK;
 }
 
+// The device address of page-locked (registered or cudaHostAlloc'd) host
+// memory, or null for anything else: pageable memory, device memory, or a
+// pointer the runtime does not know.
+static const void* page_locked(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();   // clear the error the query left
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
 static w4_status launch_w4a16_checked(const void* x, const void* qweight, const void* w_scale, int32_t w_scale_dtype,
                                       const void* zeros, int32_t g, const void* bias, void* y, int64_t M, int64_t N,
                                       int64_t K, cudaStream_t s) {
@@ -267,12 +279,24 @@ w4_status w4a16_gemm_host(const void* x_host, void* x_dev, const void* qweight, 
   if (M == 0) return ok();
   if (!x_host || !y_host) return fail(W4_ERR_NULL, "x_host and y_host must be non-NULL");
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemcpyAsync(x_dev, x_host, static_cast<size_t>(M) * K * 2, cudaMemcpyHostToDevice, s);
+  const size_t xb = static_cast<size_t>(M) * K * 2, yb = static_cast<size_t>(M) * N * 2;
+  // page-locked host buffers (the device address of each, asked per call):
+  // the copies run as kernels in the GEMV's launch chain
+  const void* xh = page_locked(x_host);
+  void* yh = const_cast<void*>(page_locked(y_host));
+  if (xh && yh && aligned(xh, 16) && aligned(yh, 8) &&
+      xb % 16 == 0 && yb % 8 == 0) {
+    cudaError_t e = w4::launch_w4a16_copy(xh, x_dev, xb, false, s);
+    if (e != cudaSuccess) return from_cuda(e, "copy of x to the device");
+    st = launch_w4a16_checked(x_dev, qweight, w_scale, w_scale_dtype, zeros, g, bias, y_dev, M, N, K, s);
+    if (st != W4_OK) return st;
+    return from_cuda(w4::launch_w4a16_copy(y_dev, yh, yb, true, s), "copy of y to the host");
+  }
+  cudaError_t e = cudaMemcpyAsync(x_dev, x_host, xb, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return from_cuda(e, "copy of x to the device");
   st = launch_w4a16_checked(x_dev, qweight, w_scale, w_scale_dtype, zeros, g, bias, y_dev, M, N, K, s);
   if (st != W4_OK) return st;
-  return from_cuda(cudaMemcpyAsync(y_host, y_dev, static_cast<size_t>(M) * N * 2, cudaMemcpyDeviceToHost, s),
-                   "copy of y to the host");
+  return from_cuda(cudaMemcpyAsync(y_host, y_dev, yb, cudaMemcpyDeviceToHost, s), "copy of y to the host");
 }
 
 static w4_status check_experts(int64_t R, int64_t N, int64_t K, int32_t group, int32_t E, int32_t w_scale_dtype,

@@ -663,7 +663,45 @@ cudaError_t launch_spf(const Params& p, bool z, int spf, bool tr, int grid, size
   }
 }
 
+// The host entry point's copies (x_host -> x_dev before the GEMV, y_dev ->
+// y_host after it) as kernels with programmatic dependent launch, for
+// page-locked host buffers: kernels chain with the GEMV's grids, where
+// copy-engine jobs would end the chain before and after every call (measured
+// on GB300: a decode call from host buffers took ~24 us of stream time with
+// cudaMemcpyAsync against ~9 us for the GEMV in a chain). Copy in: each
+// thread reads its first element from the host before the dependency wait
+// (the kernels before may still read dst, none writes src), then stores.
+// Copy out: waits for the GEMV, then copies.
+template <typename T, bool kOut>
+__global__ void __launch_bounds__(256) w4a16_copy_kernel(const T* __restrict__ src, T* __restrict__ dst, size_t n) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  T first{};
+  if (!kOut && i < n) first = src[i];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (!kOut && i < n) {
+    dst[i] = first;
+    i += stride;
+  }
+  for (; i < n; i += stride) dst[i] = src[i];
+}
+
 }  // namespace
+
+cudaError_t launch_w4a16_copy(const void* src, void* dst, size_t bytes, bool to_host, cudaStream_t s) {
+  const size_t unit = to_host ? sizeof(uint2) : sizeof(uint4);
+  const size_t n = bytes / unit;
+  if (n == 0) return cudaSuccess;
+  const size_t blocks = (n + 255) / 256;
+  const int grid = static_cast<int>(blocks < static_cast<size_t>(sm_count()) ? blocks : static_cast<size_t>(sm_count()));
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg = pdl_config(grid, 256, 0, s, attr);
+  return to_host ? cudaLaunchKernelEx(&cfg, w4a16_copy_kernel<uint2, true>, static_cast<const uint2*>(src),
+                                      static_cast<uint2*>(dst), n)
+                 : cudaLaunchKernelEx(&cfg, w4a16_copy_kernel<uint4, false>, static_cast<const uint4*>(src),
+                                      static_cast<uint4*>(dst), n);
+}
 
 size_t w4a16_smem_bytes(int64_t N, int64_t K, int32_t group) {
   int zoff;

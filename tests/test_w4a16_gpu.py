@@ -163,19 +163,51 @@ def test_w4a16_back_to_back_chain_reads_previous_output():
         prev = yb
 
 
-def test_w4a16_host_entry_matches_device_entry():
-    """w4a16_gemm_host (x and y in page-locked host memory) gives the bytes of
-    w4a16_gemm on device buffers, and matches the oracle."""
+@pytest.mark.parametrize("x_pinned,y_pinned", [(True, True), (True, False), (False, True), (False, False)])
+def test_w4a16_host_entry_matches_device_entry(x_pinned, y_pinned):
+    """w4a16_gemm_host gives the bytes of w4a16_gemm on device buffers and
+    matches the oracle, and x_dev and y_dev hold x and y afterwards. With both
+    host buffers page-locked the copies run as chained kernels, otherwise as
+    copy-engine jobs."""
     M, K, N, g = 3, 1024, 512, 128
     xb = S.activations_bf16(M, K, seed=41)
     qw_np, sw_np = S.random_words((K // 8, N), seed=1), S.scales_f16((K // g, N), seed=2)
     qw, sw = to_dev(qw_np), to_dev(sw_np)
-    x_host = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).pin_memory()
-    y_host = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    x_host = torch.from_numpy(xb.view(np.int16).copy()).view(torch.bfloat16)
+    y_host = torch.empty((M, N), dtype=torch.bfloat16)
+    if x_pinned:
+        x_host = x_host.pin_memory()
+    if y_pinned:
+        y_host = y_host.pin_memory()
     x_dev = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
     y_dev = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     w4.w4a16_gemm_host(x_host, x_dev, qw, sw, g, y_dev, y_host)
     y_ref = w4.w4a16_gemm(bf16(xb), qw, sw, g)
     torch.cuda.synchronize()
     np.testing.assert_array_equal(y_host.view(torch.int16).numpy().view(np.uint16), bits(y_ref))
+    np.testing.assert_array_equal(bits(y_dev), bits(y_ref))
+    np.testing.assert_array_equal(bits(x_dev), xb)
     check_bf16_output(bits(y_ref), O.w4a16_linear(xb, qw_np, sw_np, g), "host entry")
+
+
+def test_w4a16_host_entry_chain():
+    """Eight host-entry calls queued back to back on one stream, each with its
+    own x and y host buffers but the same x_dev and y_dev: every call's copy
+    into x_dev waits for the GEMV before it, and every y_host gets its own
+    call's result."""
+    M, K, N, g, calls = 1, 4096, 2048, 128, 8
+    qw_np, sw_np = S.random_words((K // 8, N), seed=3), S.scales_f16((K // g, N), seed=4)
+    qw, sw = to_dev(qw_np), to_dev(sw_np)
+    xs = [S.activations_bf16(M, K, seed=100 + i) for i in range(calls)]
+    x_hosts = [torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16).pin_memory() for x in xs]
+    y_hosts = [torch.empty((M, N), dtype=torch.bfloat16).pin_memory() for _ in range(calls)]
+    x_dev = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    y_dev = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    for i in range(calls):
+        w4.w4a16_gemm_host(x_hosts[i], x_dev, qw, sw, g, y_dev, y_hosts[i])
+    torch.cuda.synchronize()
+    for i in range(calls):
+        y_ref = w4.w4a16_gemm(bf16(xs[i]), qw, sw, g)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(y_hosts[i].view(torch.int16).numpy().view(np.uint16), bits(y_ref),
+                                      err_msg=f"call {i}")
