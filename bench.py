@@ -330,8 +330,8 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": DEC_M * DEC_K * 2,
                 "d2h_bytes_per_step": DEC_M * DEC_N * 2, "steps": e2e_steps,
                 "how": "per step one w4a16_gemm_host call (C ABI, host buffers): page-locked x in, the GEMM, y out "
-                       "into page-locked memory (both copies kernels chained with the GEMV); host wall clock over "
-                       "all steps and the final sync"},
+                       "into page-locked memory (x copied by the call's L2-prefetch grid, y written by the GEMV); "
+                       "host wall clock over all steps and the final sync"},
         "gpu_launches": 2 * steps,   # per call: the L2 prefetch grid and the GEMV grid
         "clocks": clocks,
         "sm_count": torch.cuda.get_device_properties(dev).multi_processor_count,

@@ -225,10 +225,11 @@ w4_status w4a16_gemm(const void* x, const void* qweight, const void* w_scale, in
  * [M, K] bf16 into x_dev, the w4a16_gemm of x_dev into y_dev, and the copy of
  * y_dev [M, N] into y_host. x_dev and y_dev are caller-owned device buffers
  * (16- and 8-byte aligned) and hold x and y afterwards. When x_host and y_host
- * are both page-locked (16- and 8-byte aligned) the two copies are kernels
- * chained with the GEMV's programmatic dependent launches, so consecutive
- * calls on a stream overlap as device-only calls do; otherwise each copy is
- * one cudaMemcpyAsync, asynchronous only for page-locked memory. y_host holds
+ * are both page-locked (x_host 16-byte aligned) no copy-engine job is queued:
+ * the call's L2-prefetch grid copies x_host into x_dev and the GEMV writes
+ * y_host along with y_dev, so consecutive calls on a stream overlap as
+ * device-only calls do; otherwise each copy is one cudaMemcpyAsync,
+ * asynchronous only for page-locked memory. y_host holds
  * the result once `stream` has been synchronized; x_host and y_host must not
  * be touched by the host until then. Other arguments and errors as
  * w4a16_gemm; nothing is queued when validation fails.

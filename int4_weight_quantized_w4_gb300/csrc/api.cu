@@ -251,11 +251,14 @@ static const void* page_locked(const void* p) {
 
 static w4_status launch_w4a16_checked(const void* x, const void* qweight, const void* w_scale, int32_t w_scale_dtype,
                                       const void* zeros, int32_t g, const void* bias, void* y, int64_t M, int64_t N,
-                                      int64_t K, cudaStream_t s) {
+                                      int64_t K, cudaStream_t s, const void* x_host = nullptr,
+                                      void* y_host = nullptr) {
   unsigned int* status = nullptr;
   cudaError_t e = status_ptr(&status);
   if (e != cudaSuccess) return from_cuda(e, "device status word");
   w4::W4A16Args a{x, qweight, w_scale, w_scale_dtype == W4_BF16, zeros, bias, y, M, N, K, g, status};
+  a.x_host = x_host;
+  a.y_host = y_host;
   return from_cuda(w4::launch_w4a16(a, s), "w4a16 launch");
 }
 
@@ -281,17 +284,12 @@ w4_status w4a16_gemm_host(const void* x_host, void* x_dev, const void* qweight, 
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t xb = static_cast<size_t>(M) * K * 2, yb = static_cast<size_t>(M) * N * 2;
   // page-locked host buffers (the device address of each, asked per call):
-  // the copies run as kernels in the GEMV's launch chain
+  // the L2-prefetch grid copies x in and the GEMV writes y out as well, so
+  // the call launches no more grids than w4a16_gemm
   const void* xh = page_locked(x_host);
   void* yh = const_cast<void*>(page_locked(y_host));
-  if (xh && yh && aligned(xh, 16) && aligned(yh, 8) &&
-      xb % 16 == 0 && yb % 8 == 0) {
-    cudaError_t e = w4::launch_w4a16_copy(xh, x_dev, xb, false, s);
-    if (e != cudaSuccess) return from_cuda(e, "copy of x to the device");
-    st = launch_w4a16_checked(x_dev, qweight, w_scale, w_scale_dtype, zeros, g, bias, y_dev, M, N, K, s);
-    if (st != W4_OK) return st;
-    return from_cuda(w4::launch_w4a16_copy(y_dev, yh, yb, true, s), "copy of y to the host");
-  }
+  if (xh && yh && aligned(xh, 16) && aligned(yh, 2) && xb % 16 == 0)
+    return launch_w4a16_checked(x_dev, qweight, w_scale, w_scale_dtype, zeros, g, bias, y_dev, M, N, K, s, xh, yh);
   cudaError_t e = cudaMemcpyAsync(x_dev, x_host, xb, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return from_cuda(e, "copy of x to the device");
   st = launch_w4a16_checked(x_dev, qweight, w_scale, w_scale_dtype, zeros, g, bias, y_dev, M, N, K, s);

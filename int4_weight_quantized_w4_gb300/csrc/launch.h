@@ -39,14 +39,12 @@ struct W4A16Args {
   int64_t M, N, K;
   int32_t group;  // effective group (K when the caller passed -1)
   unsigned int* status;
+  // host entry point, page-locked host buffers (device addresses): x is copied
+  // from x_host into x by the L2-prefetch grid, y written to y_host as well
+  const void* x_host = nullptr;
+  void* y_host = nullptr;
 };
 cudaError_t launch_w4a16(const W4A16Args& a, cudaStream_t s);
-// bytes from src to dst on `stream` by a kernel chained with programmatic
-// dependent launch (the copy in waits for the kernels before it, the copy out
-// for the one before it). to_host: 8-byte words (dst page-locked host
-// memory), else 16-byte words (src page-locked host memory); bytes a multiple
-// of the word, both pointers aligned to it.
-cudaError_t launch_w4a16_copy(const void* src, void* dst, size_t bytes, bool to_host, cudaStream_t s);
 // Per-token quantization whose output is the codes' exact fp16 values in the
 // W4A8 operand order (fp16 [M, K] into `wide`), plus the fp32 scales.
 cudaError_t launch_quant_widen(const void* x, int64_t M, int64_t K, bool fp8, void* wide, float* scale,

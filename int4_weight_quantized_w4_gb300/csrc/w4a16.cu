@@ -93,6 +93,7 @@ struct Params {
   const uint16_t* x;     // bf16 [M, K]
   const uint16_t* bias;  // bf16 [N] or null
   uint16_t* y;           // bf16 [M, N]
+  uint16_t* y_host;      // page-locked host copy of y (host entry point), or null
   int M, N, K, group;    // M <= 8 here
   int strips, stages;    // per strip: stages = ceil(K / 1024)
   int xstride;           // shared-memory row stride of x, in fp16 elements
@@ -169,14 +170,29 @@ W4_DEV void prefetch_share(const uint8_t* base, size_t bytes) {
 // the previous call's GEMV. It lets its dependent (this call's GEMV) launch at
 // once and touches nothing but L2, so it needs no dependency wait of its own:
 // the GEMV's griddepcontrol.wait covers every prerequisite grid in flight.
+// For the host entry point it also copies x (x16 16-byte words) from
+// page-locked host memory into x: each thread reads its first word before
+// the dependency wait (nothing before writes x_host) and writes after it (the
+// kernels before may still read x). As a kernel, not a copy-engine job, the
+// copy keeps consecutive calls chained (measured on GB300: a decode call from
+// host buffers took ~24 us of stream time with cudaMemcpyAsync copies).
 __global__ void __launch_bounds__(32) w4a16_prefetch_kernel(const uint8_t* w, size_t wb, const uint8_t* s,
-                                                            size_t sb, const uint8_t* z, size_t zb) {
+                                                            size_t sb, const uint8_t* z, size_t zb,
+                                                            const uint4* __restrict__ xh, uint4* __restrict__ x,
+                                                            size_t x16) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) {
     prefetch_share(w, wb);
     prefetch_share(s, sb);
     prefetch_share(z, zb);
   }
+  if (x16 == 0) return;
+  const size_t stride = static_cast<size_t>(gridDim.x) * 32;
+  size_t i = static_cast<size_t>(blockIdx.x) * 32 + threadIdx.x;
+  const uint4 first = i < x16 ? xh[i] : make_uint4(0, 0, 0, 0);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (i < x16) x[i] = first;
+  for (i += stride; i < x16; i += stride) x[i] = xh[i];
 }
 
 // kSPF: steps (32 k each) per scale group inside a 256-k unit when the fold
@@ -540,7 +556,9 @@ __global__ void __maxnreg__(120) w4a16_kernel(const __grid_constant__ Params p) 
         if (n < p.N) {
           s *= 16777216.f;                                       // undo 2^-24 (exact)
           if (p.bias != nullptr) s += __uint_as_float(static_cast<uint32_t>(p.bias[n]) << 16);
-          p.y[(size_t)m * p.N + n] = static_cast<uint16_t>(f32_to_bf16_bits(s));
+          const uint16_t yv = static_cast<uint16_t>(f32_to_bf16_bits(s));
+          p.y[(size_t)m * p.N + n] = yv;
+          if (p.y_host != nullptr) p.y_host[(size_t)m * p.N + n] = yv;
         }
       }
     }
@@ -663,45 +681,7 @@ cudaError_t launch_spf(const Params& p, bool z, int spf, bool tr, int grid, size
   }
 }
 
-// The host entry point's copies (x_host -> x_dev before the GEMV, y_dev ->
-// y_host after it) as kernels with programmatic dependent launch, for
-// page-locked host buffers: kernels chain with the GEMV's grids, where
-// copy-engine jobs would end the chain before and after every call (measured
-// on GB300: a decode call from host buffers took ~24 us of stream time with
-// cudaMemcpyAsync against ~9 us for the GEMV in a chain). Copy in: each
-// thread reads its first element from the host before the dependency wait
-// (the kernels before may still read dst, none writes src), then stores.
-// Copy out: waits for the GEMV, then copies.
-template <typename T, bool kOut>
-__global__ void __launch_bounds__(256) w4a16_copy_kernel(const T* __restrict__ src, T* __restrict__ dst, size_t n) {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
-  size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  T first{};
-  if (!kOut && i < n) first = src[i];
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (!kOut && i < n) {
-    dst[i] = first;
-    i += stride;
-  }
-  for (; i < n; i += stride) dst[i] = src[i];
-}
-
 }  // namespace
-
-cudaError_t launch_w4a16_copy(const void* src, void* dst, size_t bytes, bool to_host, cudaStream_t s) {
-  const size_t unit = to_host ? sizeof(uint2) : sizeof(uint4);
-  const size_t n = bytes / unit;
-  if (n == 0) return cudaSuccess;
-  const size_t blocks = (n + 255) / 256;
-  const int grid = static_cast<int>(blocks < static_cast<size_t>(sm_count()) ? blocks : static_cast<size_t>(sm_count()));
-  cudaLaunchAttribute attr[1];
-  const cudaLaunchConfig_t cfg = pdl_config(grid, 256, 0, s, attr);
-  return to_host ? cudaLaunchKernelEx(&cfg, w4a16_copy_kernel<uint2, true>, static_cast<const uint2*>(src),
-                                      static_cast<uint2*>(dst), n)
-                 : cudaLaunchKernelEx(&cfg, w4a16_copy_kernel<uint4, false>, static_cast<const uint4*>(src),
-                                      static_cast<uint4*>(dst), n);
-}
 
 size_t w4a16_smem_bytes(int64_t N, int64_t K, int32_t group) {
   int zoff;
@@ -752,12 +732,15 @@ cudaError_t launch_w4a16(const W4A16Args& a, cudaStream_t s) {
     const cudaLaunchConfig_t cfg = pdl_config(sm_count(), 32, 0, s, attr);
     e = cudaLaunchKernelEx(&cfg, w4a16_prefetch_kernel, static_cast<const uint8_t*>(a.qweight), wb,
                            static_cast<const uint8_t*>(a.w_scale), sb, static_cast<const uint8_t*>(a.zeros),
-                           z ? sb : size_t(0));
+                           z ? sb : size_t(0), static_cast<const uint4*>(a.x_host),
+                           static_cast<uint4*>(const_cast<void*>(a.x)),
+                           a.x_host != nullptr ? static_cast<size_t>(a.M) * a.K * 2 / 16 : size_t(0));
     if (e != cudaSuccess) return e;
   }
   for (int64_t m0 = 0; m0 < a.M; m0 += block) {
     p.x = static_cast<const uint16_t*>(a.x) + m0 * a.K;
     p.y = static_cast<uint16_t*>(a.y) + m0 * a.N;
+    p.y_host = a.y_host != nullptr ? static_cast<uint16_t*>(a.y_host) + m0 * a.N : nullptr;
     p.M = static_cast<int>(a.M - m0 < block ? a.M - m0 : block);
     p.ring = bytes(p.M, 8) <= kSmemMax ? 8 : 4;
     // when the shared-memory partials cost the ring half its depth, the
