@@ -163,13 +163,15 @@ def test_w4a16_back_to_back_chain_reads_previous_output():
         prev = yb
 
 
-@pytest.mark.parametrize("x_pinned,y_pinned", [(True, True), (True, False), (False, True), (False, False)])
-def test_w4a16_host_entry_matches_device_entry(x_pinned, y_pinned):
+@pytest.mark.parametrize("x_pinned,y_pinned,M", [(True, True, 3), (True, False, 3), (False, True, 3),
+                                                  (False, False, 3), (True, True, 17)])
+def test_w4a16_host_entry_matches_device_entry(x_pinned, y_pinned, M):
     """w4a16_gemm_host gives the bytes of w4a16_gemm on device buffers and
     matches the oracle, and x_dev and y_dev hold x and y afterwards. With both
-    host buffers page-locked the copies run as chained kernels, otherwise as
-    copy-engine jobs."""
-    M, K, N, g = 3, 1024, 512, 128
+    host buffers page-locked, the call's L2-prefetch grid copies x in and the
+    GEMV writes y out (17 tokens: three GEMV launches of up to 8 tokens, one
+    copy of x); otherwise the copies are copy-engine jobs."""
+    K, N, g = 1024, 512, 128
     xb = S.activations_bf16(M, K, seed=41)
     qw_np, sw_np = S.random_words((K // 8, N), seed=1), S.scales_f16((K // g, N), seed=2)
     qw, sw = to_dev(qw_np), to_dev(sw_np)
