@@ -61,6 +61,9 @@
 //  * Each warp keeps its strip partial in registers and stores it once per
 //    strip; after the last unit the block sums the partials in a fixed order,
 //    adds the bias and writes y once in bf16.
+//  * From page-locked host buffers (w4a16_gemm_host) the prefetch grid copies
+//    x in and the GEMV writes y out as well, so such a call launches the same
+//    two grids as a device call and chains with its neighbours the same way.
 #include <cuda.h>
 
 #include "common.cuh"
