@@ -54,10 +54,11 @@
 //    tot += s 2^-e acc + (z - 8 s) X, X = 2^-24 sum x over the group's k
 //    (since sum x (q - 8) = 2^24 2^-e acc - 8 sum x); tot is scaled by 2^24
 //    at the end (exact). Fold points are compile-time for groups of 64, 128
-//    and multiples of 256. For one token and groups of 128 the unit's two
-//    groups go to two MMA columns (the other columns read a zero row), so
-//    they accumulate side by side and the unit folds once (decode chains
-//    measured 3-4% faster on GB300, outputs bit-identical).
+//    and multiples of 256. For up to 4 tokens and groups of 128 the unit's
+//    two groups go to two MMA columns per token (unused columns read a zero
+//    row), so they accumulate side by side and the unit folds once (decode
+//    chains measured 3-4% faster on GB300 at one token and 2% at four,
+//    outputs bit-identical).
 //  * The k order inside each 32-wide step is permuted consistently for both
 //    operands; word rows 2c + (step parity) make the 16-byte shared loads of
 //    a quarter-warp land in 8 distinct swizzled chunks.
@@ -216,9 +217,12 @@ __global__ void __launch_bounds__(32) w4a16_prefetch_kernel(const uint8_t* w, si
 // kTmemRed: the warps' strip partials go to tensor memory instead of shared
 // memory (at M = 5..8 the shared-memory partials would cost the ring half its
 // depth); the block sums them per TMEM lane quadrant, then across quadrants.
-template <bool kScaleBf16, bool kZero, int kSPF, bool kTmemRed, bool kM1 = false>
+template <bool kScaleBf16, bool kZero, int kSPF, bool kTmemRed, int kGC = 0>
 __global__ void __maxnreg__(120) w4a16_kernel(const __grid_constant__ Params p) {
-  static_assert(!kM1 || (kSPF == 4 && !kTmemRed), "the one-token form folds two 128-k groups per unit");
+  // kGC (group columns, groups of 128): 1 for one token, 4 for two to four.
+  // MMA column n holds token n / 2's sums over the unit's group n % 2, so the
+  // unit folds once
+  static_assert(kGC == 0 || (kSPF == 4 && !kTmemRed), "the group-column form folds two 128-k groups per unit");
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   const int S = p.stages;
@@ -243,7 +247,7 @@ __global__ void __maxnreg__(120) w4a16_kernel(const __grid_constant__ Params p) 
   float* xsum = reinterpret_cast<float*>(smem + L.xsum);
   uint4* xs = reinterpret_cast<uint4*>(smem + L.xs);
   const uint4* zrow = reinterpret_cast<const uint4*>(smem + L.zro);
-  if (kM1 && threadIdx.x < 32) reinterpret_cast<uint4*>(smem + L.zro)[threadIdx.x] = make_uint4(0, 0, 0, 0);
+  if (kGC != 0 && threadIdx.x < 32) reinterpret_cast<uint4*>(smem + L.zro)[threadIdx.x] = make_uint4(0, 0, 0, 0);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -374,16 +378,25 @@ __global__ void __maxnreg__(120) w4a16_kernel(const __grid_constant__ Params p) 
         return;
       }
       float* dst = red + (su * kConsumers + warp) * M * kStrip;
+      if constexpr (kGC == 4) {   // lane (r, c) holds token c's two outputs of each tile
+        if (c < M)
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int nl = 4 * r + 2 * j;
-        if (2 * c < M) {
-          dst[(2 * c) * kStrip + nl] = tot[j][0];
-          dst[(2 * c) * kStrip + nl + 1] = tot[j][2];
-        }
-        if (2 * c + 1 < M) {
-          dst[(2 * c + 1) * kStrip + nl] = tot[j][1];
-          dst[(2 * c + 1) * kStrip + nl + 1] = tot[j][3];
+          for (int j = 0; j < 2; ++j) {
+            dst[c * kStrip + 4 * r + 2 * j] = tot[j][0];
+            dst[c * kStrip + 4 * r + 2 * j + 1] = tot[j][2];
+          }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int nl = 4 * r + 2 * j;
+          if (2 * c < M) {
+            dst[(2 * c) * kStrip + nl] = tot[j][0];
+            dst[(2 * c) * kStrip + nl + 1] = tot[j][2];
+          }
+          if (2 * c + 1 < M) {
+            dst[(2 * c + 1) * kStrip + nl] = tot[j][1];
+            dst[(2 * c + 1) * kStrip + nl + 1] = tot[j][3];
+          }
         }
       }
     };
@@ -417,12 +430,15 @@ __global__ void __maxnreg__(120) w4a16_kernel(const __grid_constant__ Params p) 
         const uint8_t* we = wbase + w_off_e;
         const uint8_t* wo = wbase + w_off_o;
         const uint4* xe = xrow + kunit / 8 + 2 * c;
-        const uint4* xo = xe + 1;
-        // one token: MMA column r takes the unit's first 128-k group (r = 0) or
-        // its second (r = 1), the other columns zeros, so both groups
-        // accumulate side by side and the unit folds once
-        const uint4* xe0 = kM1 && r != 0 ? zrow + 2 * c : xe;
-        const uint4* xe1 = kM1 && r != 1 ? zrow + 2 * c : xe;
+        // group columns: MMA column r takes token r / 2's x over the unit's
+        // first 128-k group (r even) or its second (r odd), zeros elsewhere, so
+        // both groups accumulate side by side and the unit folds once
+        const uint4* xg = kGC == 4 ? xs + min(r >> 1, M - 1) * xch + kunit / 8 + 2 * c : xe;
+        const uint4* xe0 = kGC == 1 ? (r != 0 ? zrow + 2 * c : xe)
+                                    : ((r & 1) != 0 || (r >> 1) >= M ? zrow + 2 * c : xg);
+        const uint4* xe1 = kGC == 1 ? (r != 1 ? zrow + 2 * c : xe)
+                                    : ((r & 1) != 1 || (r >> 1) >= M ? zrow + 2 * c : xg);
+        const int ct = kGC == 4 ? c : 0;   // the token whose sums this lane folds
         const float* xb = xsum + (kunit / 64) * kTok + 2 * c;
         const float2 f = *reinterpret_cast<const float2*>(exs + seg * kTok + 2 * c);   // 2^-e, tokens 2c, 2c+1
         // scale rows of the slot: this unit's first group is row kunit / group - gst
@@ -472,11 +488,11 @@ __global__ void __maxnreg__(120) w4a16_kernel(const __grid_constant__ Params p) 
           }
           X0 = X1 = 0.f;
         };
-        // one token: acc[.][0] and acc[.][2] (rows r, r+8) hold the first
-        // group, acc[.][1] and acc[.][3] the second (lanes with c = 0; other
-        // lanes hold zeros and are never stored)
-        auto fold_m1 = [&](int row_a, int row_b) {
-          const float f0 = exs[seg * kTok];
+        // group columns: acc[.][0] and acc[.][2] (rows r, r+8) hold token ct's
+        // first group, acc[.][1] and acc[.][3] its second (lanes past the
+        // tokens hold zeros and are never stored)
+        auto fold_gc = [&](int row_a, int row_b) {
+          const float f0 = exs[seg * kTok + ct];
           const uint2 sa = *reinterpret_cast<const uint2*>(sbase + row_a * (kStrip * 2));
           const uint2 sb2 = *reinterpret_cast<const uint2*>(sbase + row_b * (kStrip * 2));
           const uint2 za = kZero ? *reinterpret_cast<const uint2*>(sbase + p.zoff + row_a * (kStrip * 2))
@@ -508,13 +524,13 @@ __global__ void __maxnreg__(120) w4a16_kernel(const __grid_constant__ Params p) 
 #pragma unroll
         for (int t = 0; t < kUnitRows / 4; ++t) {
           const uint4 w = *reinterpret_cast<const uint4*>((t & 1 ? wo : we) + (t >> 1) * 1024);
-          const uint4* xsel = kM1 ? (t < 4 ? xe0 : xe1) : xe;
+          const uint4* xsel = kGC != 0 ? (t < 4 ? xe0 : xe1) : xe;
           const uint4 xv = (t & 1 ? xsel + 1 : xsel)[(t >> 1) * 8];
           // nibble pairs as fp16 subnormals: (i, i+4) at bits 0-3 -> q 2^-24,
           // at bits 4-7 -> 16 q 2^-24 (its activations carry the 1/16)
           const uint32_t xh = w.x >> 8, yh = w.y >> 8, zh = w.z >> 8, wh = w.w >> 8;
           // tile 0: rows r <-> n0, r+8 <-> n0+1; tile 1: rows r <-> n0+2, r+8 <-> n0+3
-          if (kM1 ? t == 0 : (kSPF != 0 && t % (kSPF > 0 ? kSPF : 1) == 0)) {   // fresh accumulators
+          if (kGC != 0 ? t == 0 : (kSPF != 0 && t % (kSPF > 0 ? kSPF : 1) == 0)) {   // fresh accumulators
             mma_f16_first(acc[0], w.x & 0x000F000Fu, w.y & 0x000F000Fu, w.x & 0x00F000F0u, w.y & 0x00F000F0u, xv.x, xv.y);
             mma_f16_first(acc[1], xh & 0x000F000Fu, yh & 0x000F000Fu, xh & 0x00F000F0u, yh & 0x00F000F0u, xv.z, xv.w);
             mma_f16_first(acc[2], w.z & 0x000F000Fu, w.w & 0x000F000Fu, w.z & 0x00F000F0u, w.w & 0x00F000F0u, xv.x, xv.y);
@@ -525,11 +541,11 @@ __global__ void __maxnreg__(120) w4a16_kernel(const __grid_constant__ Params p) 
             mma_f16(acc[2], w.z & 0x000F000Fu, w.w & 0x000F000Fu, w.z & 0x00F000F0u, w.w & 0x00F000F0u, xv.x, xv.y);
             mma_f16(acc[3], zh & 0x000F000Fu, wh & 0x000F000Fu, zh & 0x00F000F0u, wh & 0x00F000F0u, xv.z, xv.w);
           }
-          if (kM1 && (t & 1)) {
+          if (kGC != 0 && (t & 1)) {
             // the token's x sums over the unit's two groups (X0: first, X1: second)
-            const float bs = xsum[(kunit / 64 + (t >> 1)) * kTok];
+            const float bs = xsum[(kunit / 64 + (t >> 1)) * kTok + ct];
             if (t < 4) X0 += bs; else X1 += bs;
-            if (t == kUnitRows / 4 - 1) fold_m1(min(row0, p.gh - 1), min(row0 + 1, p.gh - 1));
+            if (t == kUnitRows / 4 - 1) fold_gc(min(row0, p.gh - 1), min(row0 + 1, p.gh - 1));
           } else if (t & 1) {
             // a 64-k block ends: add its x sums (tokens 2c, 2c+1)
             const float2 bs = *reinterpret_cast<const float2*>(xb + (t >> 1) * kTok);
@@ -719,7 +735,8 @@ template <bool kScaleBf16, bool kZero, int kSPF>
 cudaError_t launch_t(const Params& p, bool tmem_red, int grid, size_t smem, cudaStream_t s) {
   auto k = tmem_red ? w4a16_kernel<kScaleBf16, kZero, kSPF, true> : w4a16_kernel<kScaleBf16, kZero, kSPF, false>;
   if constexpr (kSPF == 4)
-    if (!tmem_red && p.M == 1) k = w4a16_kernel<kScaleBf16, kZero, 4, false, true>;
+    if (!tmem_red && p.M <= 4)
+      k = p.M == 1 ? w4a16_kernel<kScaleBf16, kZero, 4, false, 1> : w4a16_kernel<kScaleBf16, kZero, 4, false, 4>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
