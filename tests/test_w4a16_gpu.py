@@ -77,6 +77,15 @@ def test_w4a16_resident_stages(M, N, K, group, zeros):
     _case(M, N, K, group, zeros=zeros, seed=N + K)
 
 
+@pytest.mark.parametrize("M,N,K,zeros", [(1, 1024, 1152, False), (4, 520, 640, True), (2, 4096, 4224, False),
+                                         (3, 136, 128, True)])
+def test_w4a16_group_columns_ragged_units(M, N, K, zeros):
+    """Groups of 128 at up to four tokens fold a 256-k unit's two groups at
+    once: K an odd number of groups leaves the last unit half past K (nine,
+    five and 33 groups), and K = 128 is a single half unit."""
+    _case(M, N, K, 128, zeros=zeros, seed=M * 100 + K)
+
+
 @pytest.mark.parametrize("M", [9, 17, 40])
 def test_w4a16_more_than_8_tokens(M):
     _case(M, 136, 512, 64, zeros=True, bias=True, seed=M)
