@@ -674,30 +674,55 @@ def cpu_baseline(budget_s=10.0):
                       f"M=1 decode GEMV (K=4096, N=14336, group 128), {dt:.1f} s"}
 
 
+REF_BUDGET_S = 60.0   # the reference arm's timed steps, whatever K is
+
+
+def ref_columns(steps, t_full, budget_s=REF_BUDGET_S):
+    """Output columns per reference step: all of them when `steps` whole calls
+    (t_full seconds each) fit in budget_s, else the largest multiple of 32
+    (at least 32) that keeps the steps within it."""
+    if steps * t_full <= budget_s:
+        return DEC_N
+    return max(32, int(DEC_N * budget_s / (steps * t_full)) // 32 * 32)
+
+
 def run_reference(args, rank, world):
+    """The C oracle on the decode GEMV, K steps. A step is the whole GEMV when
+    K of them fit in REF_BUDGET_S; otherwise a block of its output columns
+    (a multiple of 32) sized from one timed whole call, so that the run ends
+    within minutes at any K."""
     if rank != 0:
         return None
     from oracle import c_oracle as C
     xb, qw, sw = oracle_decode_sample(np.arange(DEC_N))
+    t0 = time.perf_counter()
+    C.w4a16_linear(xb, qw, sw, DEC_G)
+    t_full = max(time.perf_counter() - t0, 1e-6)
+    steps = max(1, args.steps)
+    cols = ref_columns(steps, t_full)
+    if cols < DEC_N:
+        xb, qw, sw = oracle_decode_sample(np.arange(cols))
     for _ in range(max(args.warmup, 3)):
         C.w4a16_linear(xb, qw, sw, DEC_G)
     t0 = time.perf_counter()
-    for _ in range(args.steps):
+    for _ in range(steps):
         C.w4a16_linear(xb, qw, sw, DEC_G)
     dt = time.perf_counter() - t0
-    nbytes = decode_bytes()
-    value = args.steps * nbytes / dt / 1e9
+    nbytes = decode_bytes(N=cols)
+    value = steps * nbytes / dt / 1e9
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (same generator as the GPU arm)",
         "config": {"workload": "w4a16_decode", "M": DEC_M, "K": DEC_K, "N": DEC_N, "group": DEC_G,
                    "scales": "fp16", "zeros": False,
-                   "sample": "each step: the C oracle on the whole decode GEMV"},
+                   "sample": ("each step: the C oracle on the whole decode GEMV" if cols == DEC_N else
+                              f"each step: the C oracle on output columns 0..{cols - 1} of the decode GEMV")},
         "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": C.threads(), "kind": "oracle",
-                         "sample": f"{args.steps} steps, each the C oracle (float64, {C.threads()} threads) on the "
-                                   "whole M=1 decode GEMV"},
+                         "sample": f"{steps} steps, each the C oracle (float64, {C.threads()} threads) on "
+                                   + ("the whole M=1 decode GEMV" if cols == DEC_N else
+                                      f"{cols} of the {DEC_N} output columns of the M=1 decode GEMV")},
         "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 

@@ -65,6 +65,17 @@ def test_max_over_ranks_gloo_world_2():
     assert bench.max_over_ranks(3.0, "cpu", 1) == 3.0
 
 
+def test_reference_arm_step_size_is_bounded():
+    """At any K the reference arm's steps fit its time budget: whole GEMVs
+    while they fit, else a block of output columns (a multiple of 32)."""
+    import bench
+    assert bench.ref_columns(20, 2.6e-3) == bench.DEC_N
+    for steps in (50000, 200000, 10 ** 7):
+        cols = bench.ref_columns(steps, 2.6e-3)
+        assert cols % 32 == 0 and 32 <= cols < bench.DEC_N
+        assert steps * 2.6e-3 * cols / bench.DEC_N <= bench.REF_BUDGET_S or cols == 32
+
+
 def test_reference_arm_under_torchrun_prints_once():
     port = _free_port()
     out = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
