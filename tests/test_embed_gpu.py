@@ -79,18 +79,20 @@ def test_lm_head_tensor_core_shapes(V, D, g, M):
 
 @pytest.mark.parametrize("V,D,g,M", [(4099, 1152, 128, 1), (37, 8192, 256, 1), (48, 1024, 512, 1), (17, 256, 256, 1),
                                      (161, 640, 128, 1), (3000, 768, 384, 1), (2500, 2048, 128, 1),
-                                     (2433, 1920, 128, 2), (4099, 1280, 256, 5)])
+                                     (1, 128, 128, 1), (15, 8192, -1, 1), (2433, 1920, 128, 2), (4099, 1280, 256, 5)])
 def test_lm_head_tensor_core_split_tiles(V, D, g, M):
     """Tiles shared by several warps of a CTA (every CTA's run of tiles is
     cut into equal runs of segments), for one token (eight segments to a
     window of MMA columns: 9, 5, 15 and 6 segments leave a partial window;
     scale groups of 2, 3 and 4 segments; 64 segments cut mid-window by 24
-    warps) and for several tokens."""
-    packed, sc, z = _table(V, D, g, seed=V + D)
+    warps; a one-row table of one segment; a row as one scale group) and for
+    several tokens."""
+    gg = D if g == -1 else g
+    packed, sc, z = _table(V, D, gg, seed=V + D)
     h = S.activations_bf16(M, D, seed=V * 7 + M)
     y = w4.w4_lm_head_gemv(bf16(h), to_dev(packed), to_dev(sc), to_dev(z), g)
     torch.cuda.synchronize()
-    check_bf16_output(bits(y), O.lm_head_logits(h, packed, sc, z, g), f"lm_head split V={V} D={D} g={g} M={M}")
+    check_bf16_output(bits(y), O.lm_head_logits(h, packed, sc, z, gg), f"lm_head split V={V} D={D} g={g} M={M}")
 
 
 def test_lm_head_one_token_wide_range_h():
