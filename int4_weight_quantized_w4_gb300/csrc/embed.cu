@@ -251,8 +251,8 @@ __global__ void __launch_bounds__(kTcWarps * 32) lm_head_tc_kernel(const uint16_
   const int64_t wg = static_cast<int64_t>(blockIdx.x) * kTcWarps + warp;
   const int64_t nw = static_cast<int64_t>(gridDim.x) * kTcWarps;
   if (wg >= ntiles) return;
-  const int64_t my_tiles = (ntiles - 1 - wg) / nw + 1;
-  const int64_t npos = my_tiles * S;
+  // 32-bit position counters: a warp's share is at most a few thousand segments
+  const int npos = static_cast<int>((ntiles - 1 - wg) / nw + 1) * S;
   const int64_t rowb = D / 2;
   const int G = D / group, spg = group / 128;   // segments per scale group
 
@@ -307,7 +307,7 @@ __global__ void __launch_bounds__(kTcWarps * 32) lm_head_tc_kernel(const uint16_
   const uint8_t* bbase = smem + stage_offset(0, g, t);
   float tot[4] = {0.f, 0.f, 0.f, 0.f};
   float s0 = 0.f, s1 = 0.f, b0 = 0.f, b1 = 0.f;
-  for (int64_t pos0 = 0; pos0 < npos; pos0 += kTcAhead) {
+  for (int pos0 = 0; pos0 < npos; pos0 += kTcAhead) {
 #pragma unroll
     for (int p = 0; p < kTcAhead; ++p) {
       if (pos0 + p < npos) {
@@ -400,13 +400,14 @@ __global__ void __launch_bounds__(kTc1Warps * 32) lm_head_tc1_kernel(const uint1
   auto blk = [](int seg, int zblk, int tt) { return (seg * 2 + zblk) * kSegBytes + tt * 64 + (tt >> 1) * 16; };
 
   // this warp's run [p0, p1) of the CTA's positions (every CTA has a tile)
-  int64_t npos, tile0;
+  int npos;   // positions in the run (a run is at most one CTA's share of the table)
+  int64_t tile0;
   int seg0;
   {
     const int64_t T0 = static_cast<int64_t>(blockIdx.x) * ntiles / gridDim.x;
     const int64_t P = (static_cast<int64_t>(blockIdx.x + 1) * ntiles / gridDim.x - T0) * S;
     const int64_t p0 = warp * P / kTc1Warps;
-    npos = (warp + 1) * P / kTc1Warps - p0;
+    npos = static_cast<int>((warp + 1) * P / kTc1Warps - p0);
     tile0 = T0 + p0 / S;
     seg0 = static_cast<int>(p0 % S);
   }
@@ -510,7 +511,7 @@ __global__ void __launch_bounds__(kTc1Warps * 32) lm_head_tc1_kernel(const uint1
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     // scale s and b = z - 8 s of rows g, g + 8 for segments 8w + 2t (s0, s1) and 8w + 2t + 1 (s2, s3)
     float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f, b0 = 0.f, b1 = 0.f, b2 = 0.f, b3 = 0.f;
-    for (int64_t pos0 = 0; pos0 < npos; pos0 += kTc1Ahead) {
+    for (int pos0 = 0; pos0 < npos; pos0 += kTc1Ahead) {
 #pragma unroll
       for (int p = 0; p < kTc1Ahead; ++p) {
         if (pos0 + p < npos) {
