@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(kTcWarps * 32) lm_head_tc_kernel(const uint16_
   const int64_t wg = static_cast<int64_t>(blockIdx.x) * kTcWarps + warp;
   const int64_t nw = static_cast<int64_t>(gridDim.x) * kTcWarps;
   if (wg >= ntiles) return;
-  // 32-bit position counters: a warp's share is at most a few thousand segments
+  // 32-bit position counters: a warp's share of any table that fits in memory is far below 2^31 segments
   const int npos = static_cast<int>((ntiles - 1 - wg) / nw + 1) * S;
   const int64_t rowb = D / 2;
   const int G = D / group, spg = group / 128;   // segments per scale group
@@ -400,7 +400,7 @@ __global__ void __launch_bounds__(kTc1Warps * 32) lm_head_tc1_kernel(const uint1
   auto blk = [](int seg, int zblk, int tt) { return (seg * 2 + zblk) * kSegBytes + tt * 64 + (tt >> 1) * 16; };
 
   // this warp's run [p0, p1) of the CTA's positions (every CTA has a tile)
-  int npos;   // positions in the run (a run is at most one CTA's share of the table)
+  int npos;   // positions in the run: 32 bits, far more than a warp's share of any table that fits in memory
   int64_t tile0;
   int seg0;
   {
